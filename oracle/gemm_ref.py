@@ -1,0 +1,131 @@
+"""Oracle for D = alpha*A*B + beta*C (TEST INFRASTRUCTURE ONLY).
+
+Thin ctypes wrapper over ``gemm_ref.c`` plus the acceptance bound.  Only tests/, the
+smoke check and the bench's CPU-baseline leg may import this module; the product path
+never does.
+
+Definitions followed:
+  * "CUTLASS, in depth", section "The problem CUTLASS solves": D = alpha*A*B + beta*C.
+  * "Day 84: CUTLASS and CuTe layouts", section "Two programs": the reference sums the
+    same half values in double precision.
+  * The acceptance rule for a GPU result d against the fp64 reference r (stated with the
+    workload definition): |d - r| <= 2^-9 * (|alpha| * sum_k |a_ik b_kj| + |beta c_ij|)
+    + one output ulp at |r|; integer-valued workloads must match exactly.
+"""
+import ctypes
+import math
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F16, BF16 = 0, 1
+K_MAJOR, MN_MAJOR = 0, 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_gemm.restype = ctypes.c_int
+        lib.oracle_gemm.argtypes = [i64, i64, i64, dbl, vp, i64, ctypes.c_int, vp, i64,
+                                    ctypes.c_int, dbl, vp, i64, ctypes.c_int, vp, vp, i64,
+                                    vp, vp, ctypes.c_int]
+        lib.oracle_decode.restype = None
+        lib.oracle_decode.argtypes = [ctypes.c_int, vp, i64, vp]
+        lib.oracle_round.restype = None
+        lib.oracle_round.argtypes = [ctypes.c_int, vp, i64, vp]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def dtype_code(name):
+    return {"f16": F16, "fp16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16}[name]
+
+
+def _bits(arr):
+    a = np.ascontiguousarray(arr)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle operands are raw 16-bit patterns (uint16)")
+    return a
+
+
+def decode(dtype, bits):
+    """16-bit patterns -> exact float64 values."""
+    b = _bits(bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_decode(dtype, b.ctypes.data, b.size, out.ctypes.data)
+    return out
+
+
+def round_to(dtype, values):
+    """float64 -> 16-bit patterns, round to nearest, ties to even."""
+    v = np.ascontiguousarray(values, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round(dtype, v.ctypes.data, v.size, out.ctypes.data)
+    return out
+
+
+def max_threads():
+    return _load().oracle_max_threads()
+
+
+def gemm(M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, ldc, dtype,
+         rows=None, cols=None, threads=0):
+    """fp64 reference outputs and sum_k |a b| for the requested entries.
+
+    A, B, C are flat uint16 arrays holding the stored operands (C may be None when
+    beta == 0).  With rows/cols None every output is returned as an (M, N) array;
+    otherwise 1-D arrays for the entries (rows[e], cols[e]).
+    """
+    A = _bits(A)
+    B = _bits(B)
+    Cp = None
+    if C is not None:
+        C = _bits(C)
+        Cp = C.ctypes.data
+    if rows is None:
+        n = M * N
+        r_p = c_p = None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        n = rows.size
+        r_p, c_p = rows.ctypes.data, cols.ctypes.data
+    ref = np.empty(n, dtype=np.float64)
+    sab = np.empty(n, dtype=np.float64)
+    rc = _load().oracle_gemm(M, N, K, float(alpha), A.ctypes.data, lda, majorA,
+                             B.ctypes.data, ldb, majorB, float(beta), Cp, ldc, dtype,
+                             r_p, c_p, n, ref.ctypes.data, sab.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    if rows is None:
+        return ref.reshape(M, N), sab.reshape(M, N)
+    return ref, sab
+
+
+def ulp_out(dtype, r):
+    """Spacing of the output format at |r| (the smallest subnormal spacing near zero)."""
+    r = np.abs(np.asarray(r, dtype=np.float64))
+    if dtype == F16:
+        emin, frac = -14, 10
+    else:
+        emin, frac = -126, 7
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(r > 0, r, 1.0)))
+    e = np.where(r > 0, np.maximum(e, emin), emin)
+    return np.ldexp(1.0, (e - frac).astype(np.int64))
+
+
+def bound(dtype, alpha, beta, ref, sumabs, c_values=None):
+    """Acceptance bound 2^-9 (|alpha| S + |beta c|) + ulp_out(ref)."""
+    t = abs(alpha) * np.asarray(sumabs, dtype=np.float64)
+    if c_values is not None and beta != 0:
+        t = t + np.abs(beta * np.asarray(c_values, dtype=np.float64))
+    return math.ldexp(1.0, -9) * t + ulp_out(dtype, ref)
