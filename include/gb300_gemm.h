@@ -1,0 +1,130 @@
+/*
+ * gb300_gemm.h — C ABI of the sm_103a tiled GEMM  D = alpha * A * B + beta * C.
+ *
+ * Operation ("CUTLASS, in depth" — "The problem CUTLASS solves"): A is M x K, B is
+ * K x N, C and D are M x N; 16-bit inputs (fp16 or bf16, named by the symbol), products
+ * accumulated in fp32, alpha/beta applied in fp32, D rounded to nearest even.
+ *
+ * A CTA owns a 128 x 256 output tile and walks K in steps of 64 with A/B slices staged
+ * in shared memory ("CUTLASS, in depth" — "The problem CUTLASS solves", tiling); tile
+ * and element addressing come from shape:stride layouts divided into (tile, grid) modes
+ * ("Day 84: CUTLASS and CuTe layouts" — "A layout is a shape and a stride").
+ *
+ * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
+ * "One notation, and no more transposes"):
+ *   A (M x K): GB_K_MAJOR  A(m,k) = A[m*lda + k]   (row-major, lda >= K)
+ *              GB_MN_MAJOR A(m,k) = A[m + k*lda]   (column-major, lda >= M)
+ *   B (K x N): GB_K_MAJOR  B(k,n) = B[n*ldb + k]   (column-major, ldb >= K)
+ *              GB_MN_MAJOR B(k,n) = B[k*ldb + n]   (row-major, ldb >= N)
+ *   C, D (M x N): row-major, leading dimension N.  C and D have the symbol's dtype.
+ *
+ * Ownership and execution: every buffer is caller-owned device memory; the call
+ * allocates nothing, is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream) and returns once the kernel is queued.  The call reads no C when
+ * beta == 0, and then C may be NULL.  M == 0 or N == 0 is a no-op; K == 0 gives
+ * D = beta*C.
+ *
+ * Errors are reported before any launch (validation "can_implement", "CUTLASS, in
+ * depth" — "Failure modes"; "Day 84" — "Pitfalls"):
+ *   GB_ERR_INVALID_ARG      negative size, bad major, NULL operand that is needed,
+ *                           leading dimension smaller than the contiguous extent, or a
+ *                           size beyond the tensor-copy limits (M, N, K < 2^31).
+ *   GB_ERR_MISALIGNED       a pointer not 16-byte aligned, or lda/ldb not a multiple of
+ *                           8 elements (16 bytes): tile copies need 16-byte rows.
+ *   GB_ERR_UNSUPPORTED_ARCH the current device is not compute capability 10.3.
+ *   GB_ERR_LAUNCH           the CUDA launch or descriptor encoding failed.
+ * A wait inside the kernel that runs past its limit (default 2 s) makes the kernel stop,
+ * record a code in a device status word and return; gb_last_device_status reads it.
+ */
+#ifndef GB300_GEMM_H
+#define GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GB_OK = 0,
+  GB_ERR_INVALID_ARG = 1,
+  GB_ERR_MISALIGNED = 2,
+  GB_ERR_UNSUPPORTED_ARCH = 3,
+  GB_ERR_LAUNCH = 4,
+  GB_ERR_TIMEOUT = 5,
+  GB_ERR_CUDA = 6
+} gb_status;
+
+typedef enum { GB_K_MAJOR = 0, GB_MN_MAJOR = 1 } gb_major;
+
+typedef enum { GB_F16 = 0, GB_BF16 = 1 } gb_dtype;
+
+/* D = alpha*A*B + beta*C with fp16 operands (fp32 accumulate). */
+gb_status gb_gemm_f16(int64_t M, int64_t N, int64_t K, float alpha,
+                      const void* A, int64_t lda, int majorA,
+                      const void* B, int64_t ldb, int majorB,
+                      float beta, const void* C, void* D, void* stream);
+
+/* Same with bf16 operands. */
+gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+                       const void* A, int64_t lda, int majorA,
+                       const void* B, int64_t ldb, int majorB,
+                       float beta, const void* C, void* D, void* stream);
+
+/* Synchronises `stream`, then returns GB_ERR_TIMEOUT if any kernel of this library on the
+   current device recorded a wait that ran out since the last call (the raw code goes to
+   *detail when detail != NULL: bits 0-7 the wait that ran out, bits 8-31 the CTA), and
+   clears the record.  GB_ERR_CUDA if synchronising failed. */
+gb_status gb_last_device_status(void* stream, uint32_t* detail);
+
+/* Name of a status code. */
+const char* gb_status_string(int status);
+
+/* Host-side plan of one call: the tile grid and tensor-copy geometry the layouts give.
+   Pure host computation (no GPU needed), same validation as the GEMM call except the
+   pointer and device checks. */
+typedef struct {
+  int64_t m_tiles, n_tiles, k_blocks;   /* grid of 128 x 256 output tiles, K steps of 64 */
+  int64_t tile_m, tile_n, tile_k;       /* 128, 256, 64 */
+  int64_t a_dim[2], a_row_bytes;        /* A copy: extents (inner first), row pitch */
+  int64_t a_box[2], a_boxes;            /* box extents (inner first) and boxes per stage */
+  int64_t b_dim[2], b_row_bytes;
+  int64_t b_box[2], b_boxes;
+  int64_t d_grid_stride[2];             /* D offset step per tile along M and along N */
+  int64_t d_elem_stride[2];             /* D offset step per row and per column */
+  uint32_t instr_desc;                  /* tensor-core instruction descriptor */
+  int32_t vector_epilogue;              /* 1 when 16-byte C/D accesses are legal */
+} gb_gemm_plan;
+
+gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
+                            int64_t ldb, int majorB, gb_gemm_plan* plan);
+
+/* Robustness knobs (process-wide, read at launch; not thread-safe with concurrent calls):
+   the limit on every in-kernel wait, in nanoseconds (0 restores the 2 s default), and a
+   test hook that makes the copy stage skip the k-block with the given running index
+   (-1 disables), so that the consumer's bounded wait runs out and the timeout path is
+   exercised without faulting the device. */
+gb_status gb_set_wait_timeout_ns(uint64_t ns);
+gb_status gb_debug_skip_k_block(int64_t k_block);
+
+/* Test hook: evaluate, on the device, the D-offset map the epilogue uses for tile
+   (m_tile, n_tile) of an M x N problem: out[r*256 + c] = offset of in-tile element
+   (r, c) (r < 128, c < 256), or -1 when the element lies outside M x N.  out is a device
+   buffer of 32768 int64.  Asynchronous on stream. */
+gb_status gb_debug_epilogue_map(int64_t M, int64_t N, int64_t m_tile, int64_t n_tile,
+                                int64_t* out, void* stream);
+
+/* Test hook: copy one pipeline stage of operand A (which = 0) or B (which = 1) for
+   (tile, k_block) into shared memory exactly as the GEMM's copy stage does, then write
+   the raw shared-memory bytes to `out` (a device buffer of 16384 bytes for A, 32768 for
+   B).  Checks the tensor-copy geometry and the 128-byte swizzle. */
+gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, int majorA,
+                               const void* B, int64_t ldb, int majorB,
+                               int64_t tile, int64_t k_block, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_GEMM_H */

@@ -1,0 +1,87 @@
+/*
+ * layout_algebra.h — C ABI of the host shape:stride layout library.
+ *
+ * Layouts cross this boundary as text in the pages' own notation, Shape:Stride with
+ * nested parentheses, e.g. "((2,2),3):((24,2),8)" or "8:1" (a '_' prefix marking a
+ * static integer is accepted and ignored).  A tiler is one of:
+ *   "4:1"            one layout that divides the whole (1-D) layout,
+ *   "(16,16)"        one contiguous tile per leading mode (t means t:1),
+ *   "<4:1,(2,2):(1,4)>"  one tile layout per leading mode.
+ *
+ * All functions run on the host, allocate nothing the caller must free, are
+ * thread-safe, and return 0 (LA_OK) or a positive error code (la_error_string names
+ * it).  Output text goes to a caller-owned buffer `out` of `cap` bytes; when it does not
+ * fit, LA_ERR_BUFFER is returned and `out` holds an empty string.
+ *
+ * Definitions (page — section):
+ *   evaluation      "Day 84: CUTLASS and CuTe layouts" — "A layout is a shape and a
+ *                   stride"; flat indices unravel first mode fastest: "Layouts as
+ *                   Algebra" — "The formula gets a name".
+ *   size, cosize    "3.5 CUTLASS II — CuTe layouts and tensors", 3.5.5.
+ *   coalesce        "Layouts as Algebra" — "A shape is a tree".
+ *   composition     "Layouts as Algebra" — "Composition, worked by hand".
+ *   complement,     "Layouts as Algebra" — "Divide is tiling";
+ *   logical_divide  "3.5 CUTLASS II", 3.5.6.
+ *   zipped_divide   "Day 84" — "A layout is a shape and a stride".
+ *   local_tile,     "Layouts as Algebra" — "The kernel, in three lines";
+ *   local_partition "3.5 CUTLASS II", 3.5.6–3.5.7.
+ *   thread layouts  "Layouts as Algebra" — "The threads are a layout too".
+ */
+#ifndef LAYOUT_ALGEBRA_H
+#define LAYOUT_ALGEBRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  LA_OK = 0,
+  LA_ERR_PARSE = 1,          /* text is not Shape:Stride, or a tiler form above */
+  LA_ERR_INCONGRUENT = 2,    /* shape and stride trees differ */
+  LA_ERR_NOT_COMPOSABLE = 3, /* divisibility conditions of composition fail */
+  LA_ERR_NO_COMPLEMENT = 4,  /* the layout's modes overlap: no complement exists */
+  LA_ERR_RANGE = 5,          /* index/coordinate out of range, or integer overflow */
+  LA_ERR_BUFFER = 6,         /* output buffer too small */
+  LA_ERR_ARG = 7             /* NULL pointer, non-positive extent, bad rank */
+};
+
+const char* la_error_string(int code);
+
+/* size (number of coordinates) and cosize (largest offset + 1). */
+int la_size(const char* layout, int64_t* size);
+int la_cosize(const char* layout, int64_t* cosize);
+
+/* offsets[i] = layout(idx[i]) for n flat (colexicographic) indices. */
+int la_eval(const char* layout, const int64_t* idx, int64_t n, int64_t* offsets);
+
+/* offset of one natural coordinate given leaf by leaf (ncoord = number of leaves). */
+int la_eval_coord(const char* layout, const int64_t* coord, int ncoord, int64_t* offset);
+
+/* Algebra: results written as Shape:Stride text. */
+int la_coalesce(const char* layout, char* out, size_t cap);
+int la_composition(const char* a, const char* b, char* out, size_t cap);
+int la_complement(const char* layout, int64_t cotarget, char* out, size_t cap);
+int la_logical_divide(const char* layout, const char* tiler, char* out, size_t cap);
+int la_zipped_divide(const char* layout, const char* tiler, char* out, size_t cap);
+
+/* The tile of zipped_divide(layout, tiler) at grid coordinate `grid` (ngrid leaves):
+   tile layout in `out`, offset of its first element in *origin. */
+int la_local_tile(const char* layout, const char* tiler, const int64_t* grid, int ngrid,
+                  int64_t* origin, char* out, size_t cap);
+
+/* Thread `tid` of thread layout `thr`: its elements of `layout` (the rest layout in
+   `out`) and the offset of its first element in *origin. */
+int la_local_partition(const char* layout, const char* thr, int64_t tid, int64_t* origin,
+                       char* out, size_t cap);
+
+/* Offset grid of a rank-2 layout (rows = mode 0, columns = mode 1) as text. */
+int la_print_layout(const char* layout, char* out, size_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAYOUT_ALGEBRA_H */

@@ -1,0 +1,123 @@
+"""Python face of the GEMM C ABI (include/gb300_gemm.h): argument marshalling only.
+
+``gemm`` takes torch tensors holding the STORED operands (see include/gb300_gemm.h for
+the K-major / MN-major conventions) and calls gb_gemm_f16 / gb_gemm_bf16 on the current
+CUDA stream.  When the operands are host tensors the call stages them to the device with
+torch copies, runs the same C-ABI call, and copies D back into a host tensor: that is the
+end-to-end path a caller holding host buffers uses.
+"""
+import ctypes
+
+import torch
+
+from ._native import GemmPlan, lib
+
+K_MAJOR, MN_MAJOR = 0, 1
+F16, BF16 = 0, 1
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status, what="gemm"):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+def status_string(status):
+    return lib().gb_status_string(int(status)).decode()
+
+
+def major_code(m):
+    if m in (K_MAJOR, "K", "k"):
+        return K_MAJOR
+    if m in (MN_MAJOR, "MN", "mn", "M", "N"):
+        return MN_MAJOR
+    raise ValueError("major must be 'K' or 'MN'")
+
+
+def dtype_code(dt):
+    if dt in (torch.float16, "f16", "fp16"):
+        return F16
+    if dt in (torch.bfloat16, "bf16"):
+        return BF16
+    raise TypeError("operands must be float16 or bfloat16")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0, C=None,
+         D=None, stream=None):
+    """D = alpha * A @ B + beta * C.  Returns D (M*N elements, row-major).
+
+    A, B, C are flat (or any contiguous) tensors of one dtype.  Device tensors: D is
+    written in place (allocated if None).  Host tensors: operands are copied to the
+    device, and D (a host tensor, pinned if given so) receives the result.
+    """
+    dt = dtype_code(A.dtype)
+    if B.dtype != A.dtype or (C is not None and C.dtype != A.dtype):
+        raise TypeError("A, B and C must share one dtype")
+    host = not A.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        A_d = A.to(dev, non_blocking=True)
+        B_d = B.to(dev, non_blocking=True)
+        C_d = C.to(dev, non_blocking=True) if C is not None else None
+        D_d = torch.empty(M * N, dtype=A.dtype, device=dev)
+    else:
+        A_d, B_d, C_d = A, B, C
+        D_d = D if D is not None else torch.empty(M * N, dtype=A.dtype, device=A.device)
+    fn = lib().gb_gemm_bf16 if dt == BF16 else lib().gb_gemm_f16
+    st = fn(M, N, K, float(alpha), _ptr(A_d), lda, major_code(majorA), _ptr(B_d), ldb,
+            major_code(majorB), float(beta), _ptr(C_d), _ptr(D_d), _stream_handle(stream))
+    if st != 0:
+        raise GemmError(st)
+    if host:
+        if D is None:
+            D = torch.empty(M * N, dtype=A.dtype, pin_memory=True)
+        D.copy_(D_d, non_blocking=True)
+        return D
+    return D_d
+
+
+def raw_call(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta, C_ptr, D_ptr,
+             stream_handle):
+    """Direct C-ABI call with integer pointers; returns the status code."""
+    fn = lib().gb_gemm_bf16 if dtype_code(dtype) == BF16 else lib().gb_gemm_f16
+    return fn(M, N, K, float(alpha), A_ptr, lda, major_code(majorA), B_ptr, ldb,
+              major_code(majorB), float(beta), C_ptr, D_ptr, stream_handle)
+
+
+def plan(dtype, M, N, K, lda, majorA, ldb, majorB):
+    """Host-side plan (tile grid, copy geometry, instruction descriptor) as a dict."""
+    p = GemmPlan()
+    st = lib().gb_gemm_make_plan(dtype_code(dtype), M, N, K, lda, major_code(majorA), ldb,
+                                 major_code(majorB), ctypes.byref(p))
+    if st != 0:
+        raise GemmError(st, "plan")
+    out = {}
+    for name, _ in GemmPlan._fields_:
+        v = getattr(p, name)
+        out[name] = list(v) if hasattr(v, "__len__") else v
+    return out
+
+
+def last_device_status(stream=None):
+    """(status, detail) of the device status word; synchronises the stream."""
+    detail = ctypes.c_uint32()
+    st = lib().gb_last_device_status(_stream_handle(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def set_wait_timeout_ns(ns):
+    lib().gb_set_wait_timeout_ns(int(ns))
+
+
+def debug_skip_k_block(kb):
+    lib().gb_debug_skip_k_block(int(kb))

@@ -1,0 +1,877 @@
+// Persistent tiled GEMM for sm_103a:  D = alpha * A * B + beta * C.
+//
+// What the pages define ("CUTLASS, in depth" — "The problem CUTLASS solves", "Kernel
+// schedules", "Epilogue fusion"; "Layouts as Algebra" — "The kernel, in three lines"):
+// a CTA owns a BM x BN output tile, walks K in BK steps and stages the A and B slices in
+// shared memory; a producer fills a ring of stages and signals barriers, the consumer
+// multiplies and releases them; after the last K step the epilogue applies alpha and
+// beta and stores D.  Persistent CTAs loop over tiles in a grouped raster order.
+//
+// How it maps onto sm_103a:
+//   warp 0, one lane   tensor copies (TMA) of A/B k-blocks into a 4-stage ring of
+//                      128-byte-swizzled shared memory, counted on mbarriers;
+//   warp 1, one lane   tcgen05.mma (128 x 256 x 16, fp32 accumulate) into one of two
+//                      Tensor Memory accumulators (2 x 256 columns); tcgen05.commit
+//                      frees a stage when its MMAs retire and hands a finished
+//                      accumulator to the epilogue;  warp 1 also owns the TMEM allocation;
+//   warps 2-5          epilogue: tcgen05.ld of their 32-lane quarter, alpha*acc + beta*C
+//                      in fp32, round to fp16/bf16, 16-byte stores, rows/columns past
+//                      M/N predicated off.  The second accumulator lets the epilogue of
+//                      tile i overlap the main loop of tile i+1.
+// Tile origins and in-tile offsets of C/D are the evaluation of
+// zipped_divide((M,N):(N,1), (128,256)); the copy geometry of A and B comes from the
+// same divide of their layouts (host side, layout.cpp).
+//
+// Every wait is bounded: past the limit the waiting thread records a code in g_status,
+// raises an abort flag in shared memory, and all roles leave their loops; the copy
+// stage waits for its own copies in flight, the MMA stage for its own MMAs, and TMEM is
+// always released before the CTA exits.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gb300_gemm.h"
+#include "layout.hpp"
+#include "ptx.cuh"
+
+namespace gb {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
+constexpr int kStages = 4;
+constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
+constexpr int kSwz = 64;             // elements per 128-byte swizzle span
+constexpr int kAStage = kBM * kBK * 2;
+constexpr int kBStage = kBN * kBK * 2;
+constexpr int kStageBytes = kAStage + kBStage;
+constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kCtlBytes = 256;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
+static_assert(kTmemCols <= 512, "Tensor Memory holds 512 columns per SM");
+static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
+
+struct Params {
+  int32_t M, N, K;
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles, group_m;
+  int32_t majorA, majorB;     // 0: K-major, 1: MN-major
+  float alpha, beta;
+  const uint16_t* C;
+  uint16_t* D;
+  int64_t d_grid_m, d_grid_n; // D/C offset per tile step (grid mode of the divide)
+  int64_t d_row, d_col;       // D/C offset per element step (tile mode of the divide)
+  uint32_t idesc;
+  int32_t vec_ok, has_c;
+  uint64_t timeout_ns;
+  int64_t skip_kb;
+};
+
+struct Ctl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int32_t abort;
+};
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+
+enum : uint32_t {
+  kSiteEmpty = 1,     // copy stage waiting for a free ring slot
+  kSiteFull = 2,      // MMA waiting for a k-block to land
+  kSiteAccEmpty = 3,  // MMA waiting for the epilogue to free an accumulator
+  kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
+  kSiteDrain = 5,     // abort path: waiting for own operations in flight
+  kSiteTail = 6,      // copy stage waiting for the last releases before exit
+  kSiteDebug = 7,
+};
+
+__device__ uint32_t g_status;
+
+__device__ __forceinline__ void raise_status(Ctl* ctl, uint32_t site) {
+  atomicCAS(&g_status, 0u, site | (blockIdx.x << 8));
+  *reinterpret_cast<volatile int32_t*>(&ctl->abort) = 1;
+}
+
+__device__ __forceinline__ bool aborted(Ctl* ctl) {
+  return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0;
+}
+
+// Single-thread bounded wait; gives up on the abort flag or the time limit.
+__device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
+                                      uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 7) == 0) {
+      if (aborted(ctl)) return false;
+      if (global_timer_ns() - t0 > limit) {
+        raise_status(ctl, site);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain own work after an abort).
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit) {
+      atomicCAS(&g_status, 0u, kSiteDrain | (blockIdx.x << 8));
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-collective bounded wait with a warp-uniform outcome.
+__device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
+                                       uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((n & 7) == 7) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (aborted(ctl)) {
+          stop = 1;
+        } else if (global_timer_ns() - t0 > limit) {
+          raise_status(ctl, site);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+// Grouped raster order: runs of group_m M-tiles, walked down M first, then across N,
+// so that CTAs working at the same time share A rows and B columns in L2 ("CUTLASS, in
+// depth" — "Kernel schedules", rasterisation).
+__device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t& mt, int32_t& nt) {
+  const int32_t per_group = p.group_m * p.n_tiles;
+  const int32_t g = t / per_group;
+  const int32_t first_m = g * p.group_m;
+  const int32_t gm = min(p.m_tiles - first_m, p.group_m);
+  const int32_t local = t - g * per_group;
+  mt = first_m + local % gm;
+  nt = local / gm;
+}
+
+// C/D offset of in-tile element (r, c) of tile (mt, nt): the divided layout evaluated.
+__device__ __forceinline__ int64_t d_offset(const Params& p, int32_t mt, int32_t nt, int32_t r,
+                                            int32_t c) {
+  return mt * p.d_grid_m + nt * p.d_grid_n + r * p.d_row + c * p.d_col;
+}
+
+// Copies of one k-block.  K-major operand: one box of 64 (K) x rows.  MN-major operand:
+// rows/64 boxes of 64 (M or N) x 64 (K), each 8 KiB, placed one after another.
+__device__ __forceinline__ void issue_a(const Params& p, const void* tm, uint32_t dst,
+                                       uint32_t bar, int32_t mt, int32_t kb) {
+  if (p.majorA == 0) {
+    tma_load_2d(dst, tm, bar, kb * kBK, mt * kBM);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kBM / kSwz; ++j)
+      tma_load_2d(dst + j * kChunkBytes, tm, bar, mt * kBM + j * kSwz, kb * kBK);
+  }
+}
+
+__device__ __forceinline__ void issue_b(const Params& p, const void* tm, uint32_t dst,
+                                       uint32_t bar, int32_t nt, int32_t kb) {
+  if (p.majorB == 0) {
+    tma_load_2d(dst, tm, bar, kb * kBK, nt * kBN);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kBN / kSwz; ++j)
+      tma_load_2d(dst + j * kChunkBytes, tm, bar, nt * kBN + j * kSwz, kb * kBK);
+  }
+}
+
+// Shared-memory descriptor of the k-th K=16 slice of a stage operand.
+//  K-major, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (stride offset);
+//    the leading offset is unused; the k-th slice starts 32 B further along the row.
+//  MN-major, 128-byte swizzle: 64-element MN chunks one box (8 KiB) apart (leading
+//    offset), 8-row K groups 1024 B apart (stride offset); the k-th slice starts 16 rows
+//    (2 KiB) further down.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k) {
+  if (major == 0) return smem_desc_sw128(base + k * (kUmmaK * 2), 16, 1024);
+  return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
+}
+
+__device__ void run_producer(const Params& p, const void* tmA, const void* tmB, uint8_t* smem,
+                             Ctl* ctl) {
+  int stage = 0;
+  uint32_t phase = 0;
+  int64_t gkb = 0;
+  uint32_t issued = 0, issued_parity = 0;
+  bool ok = true;
+  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    int32_t mt, nt;
+    tile_coords(p, t, mt, nt);
+    for (int32_t kb = 0; kb < p.k_blocks; ++kb, ++gkb) {
+      if (!wait_one(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
+        ok = false;
+        break;
+      }
+      if (gkb != p.skip_kb) {
+        const uint32_t full = smem_addr(&ctl->full[stage]);
+        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
+        mbar_arrive_expect_tx(full, kStageBytes);
+        issue_a(p, tmA, sa, full, mt, kb);
+        issue_b(p, tmB, sa + kAStage, full, nt, kb);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      } else {
+        issued &= ~(1u << stage);
+      }
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (ok) {
+    // The consumer releases stages through asynchronous arrivals; wait for the last
+    // kStages releases so that none lands after this CTA's shared memory is gone.
+    for (int i = 0; i < kStages; ++i) {
+      if (!wait_one(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteTail)) break;
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else {
+    for (int s = 0; s < kStages; ++s)
+      if (issued & (1u << s))
+        wait_drain(smem_addr(&ctl->full[s]), (issued_parity >> s) & 1u, p.timeout_ns);
+  }
+}
+
+__device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base) {
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true, issued_any = false;
+  int32_t it = 0;
+  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+    const int buf = it & 1;
+    const uint32_t use = (it >> 1) & 1;
+    if (!wait_one(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns, kSiteAccEmpty)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t d_tmem = tmem_base + buf * kBN;
+    for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+      if (!wait_one(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sa = smem_addr(smem + stage * kStageBytes);
+      const uint32_t sb = sa + kAStage;
+#pragma unroll
+      for (int k = 0; k < kBK / kUmmaK; ++k)
+        tc_mma_f16(d_tmem, operand_desc(sa, p.majorA, k), operand_desc(sb, p.majorB, k), p.idesc,
+                   (kb | k) != 0 ? 1u : 0u);
+      issued_any = true;
+      tc_commit(smem_addr(&ctl->empty[stage]));
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    if (p.k_blocks == 0)
+      mbar_arrive(smem_addr(&ctl->acc_full[buf]));
+    else
+      tc_commit(smem_addr(&ctl->acc_full[buf]));
+  }
+  if (!ok && issued_any) {
+    tc_commit(smem_addr(&ctl->drain));
+    wait_drain(smem_addr(&ctl->drain), 0u, p.timeout_ns);
+    __nanosleep(20000);   // let the arrivals of earlier commits land
+  }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ float to_f32(uint16_t b) {
+  if constexpr (kBF16)
+    return __bfloat162float(__ushort_as_bfloat16(b));
+  else
+    return __half2float(__ushort_as_half(b));
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint16_t from_f32(float v) {
+  if constexpr (kBF16)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return static_cast<uint32_t>(from_f32<kBF16>(lo)) |
+         (static_cast<uint32_t>(from_f32<kBF16>(hi)) << 16);
+}
+
+// 32 consecutive outputs of one row: v = alpha*acc (+ beta*c), rounded and stored.
+template <bool kBF16>
+__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint32_t (&acc)[32],
+                                          int valid) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
+  const bool vec = p.vec_ok && valid == 32;
+  if (p.has_c) {
+    if (vec) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.C + off);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 u = __ldg(src + j);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
+                                  v[8 * j + 2 * e]);
+          v[8 * j + 2 * e + 1] =
+              fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[off + i * p.d_col]), v[i]);
+    }
+  }
+  if (vec) {
+    uint4* dst = reinterpret_cast<uint4*>(p.D + off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 u;
+      u.x = pack2<kBF16>(v[8 * j + 0], v[8 * j + 1]);
+      u.y = pack2<kBF16>(v[8 * j + 2], v[8 * j + 3]);
+      u.z = pack2<kBF16>(v[8 * j + 4], v[8 * j + 5]);
+      u.w = pack2<kBF16>(v[8 * j + 6], v[8 * j + 7]);
+      dst[j] = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) p.D[off + i * p.d_col] = from_f32<kBF16>(v[i]);
+  }
+}
+
+template <bool kBF16>
+__device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane) {
+  const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
+  const int r = q * 32 + lane;       // accumulator row = TMEM lane
+  int32_t it = 0;
+  for (int32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    int32_t mt, nt;
+    tile_coords(p, t, mt, nt);
+    const int buf = it & 1;
+    const uint32_t use = (it >> 1) & 1;
+    if (!wait_warp(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
+    tc_fence_after_sync();
+    const bool row_ok = static_cast<int64_t>(mt) * kBM + r < p.M;
+    const int32_t cols_left = p.N - nt * kBN;
+    const int64_t base = d_offset(p, mt, nt, r, 0);
+    for (int c0 = 0; c0 < kBN && c0 < cols_left; c0 += 32) {
+      uint32_t acc[32];
+      if (p.k_blocks > 0) {
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + c0, acc);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0u;
+      }
+      if (row_ok) store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0));
+    }
+    tc_fence_before_sync();
+    mbar_arrive(smem_addr(&ctl->acc_empty[buf]));
+  }
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&ctl->acc_full[b]), 1);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiThreads);
+    }
+    mbar_init(smem_addr(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+    if (p.k_blocks > 0) {
+      prefetch_tensormap(&tmA);
+      prefetch_tensormap(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer(p, &tmA, &tmB, smem, ctl);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) run_mma(p, smem, ctl, tmem_base);
+    __syncwarp();
+  } else {
+    run_epilogue<kBF16>(p, ctl, tmem_base, warp, lane);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ test kernels
+__global__ void epilogue_map_kernel(const Params p, int32_t mt, int32_t nt, int64_t* out) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= kBM * kBN) return;
+  const int r = idx / kBN, c = idx % kBN;
+  const int64_t row = static_cast<int64_t>(mt) * kBM + r;
+  const int64_t col = static_cast<int64_t>(nt) * kBN + c;
+  out[idx] = (row < p.M && col < p.N) ? d_offset(p, mt, nt, r, c) : -1;
+}
+
+// One CTA of 32 threads: copy one stage of A (which == 0) or B (which == 1) exactly as the
+// producer does, then dump the raw shared-memory bytes.
+__global__ void __launch_bounds__(32, 1)
+    stage_bytes_kernel(const __grid_constant__ CUtensorMap tm, const Params p, int which,
+                       int32_t tile, int32_t kb, uint4* out) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStageBytes);
+  const int bytes = which == 0 ? kAStage : kBStage;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&ctl->full[0]), 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t full = smem_addr(&ctl->full[0]);
+    mbar_arrive_expect_tx(full, bytes);
+    if (which == 0)
+      issue_a(p, &tm, smem_addr(smem), full, tile, kb);
+    else
+      issue_b(p, &tm, smem_addr(smem), full, tile, kb);
+    wait_drain(full, 0u, p.timeout_ns);
+  }
+  __syncthreads();
+  const uint4* src = reinterpret_cast<const uint4*>(smem);
+  for (int i = threadIdx.x; i < bytes / 16; i += 32) out[i] = src[i];
+}
+
+}  // namespace gb
+
+// ====================================================================== host side
+namespace {
+
+using gb::Params;
+
+std::mutex g_mu;
+uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
+int64_t g_skip_kb = -1;
+
+struct DeviceState {
+  bool probed = false;
+  int major = 0, minor = 0, sms = 0;
+  bool smem_attr[2] = {false, false};
+  bool dbg_attr = false;
+};
+DeviceState g_dev[128];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Copy geometry of one operand, read off its layout: the stride-1 mode is the copy's
+// inner dimension; the other mode's stride is the row pitch.
+struct OperandPlan {
+  int64_t dim[2], row_bytes, box[2], boxes;
+  int64_t grid_rows, k_blocks;
+};
+
+gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t tile_rows,
+                       OperandPlan* o) {
+  // (rows, K) layout of the stored operand
+  la::Layout m = major == GB_K_MAJOR ? la::make_layout({rows, K}, {ld, 1}) : la::make_layout({rows, K}, {1, ld});
+  la::Layout z = la::zipped_divide(m, la::tiler_of({tile_rows, gb::kBK}));
+  // grid mode: (row tiles, k-blocks)
+  auto grid = la::flatten(z.mode(1).shape);
+  o->grid_rows = grid[0];
+  o->k_blocks = grid[1];
+  auto modes = la::flat_modes(m);
+  const int64_t s_rows = modes[0].second, s_k = modes[1].second;
+  if (s_k == 1 && major == GB_K_MAJOR) {
+    o->dim[0] = K;
+    o->dim[1] = rows;
+    o->row_bytes = s_rows * 2;
+    o->box[0] = gb::kSwz;
+    o->box[1] = tile_rows;
+    o->boxes = 1;
+  } else if (s_rows == 1) {
+    o->dim[0] = rows;
+    o->dim[1] = K;
+    o->row_bytes = s_k * 2;
+    o->box[0] = gb::kSwz;
+    o->box[1] = gb::kBK;
+    o->boxes = tile_rows / gb::kSwz;
+  } else {
+    return GB_ERR_INVALID_ARG;
+  }
+  return GB_OK;
+}
+
+gb_status validate_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
+                         int majorB) {
+  if (M < 0 || N < 0 || K < 0) return GB_ERR_INVALID_ARG;
+  if (majorA != GB_K_MAJOR && majorA != GB_MN_MAJOR) return GB_ERR_INVALID_ARG;
+  if (majorB != GB_K_MAJOR && majorB != GB_MN_MAJOR) return GB_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t(1) << 31) - 1;
+  if (M > lim || N > lim || K > lim) return GB_ERR_INVALID_ARG;
+  if (K > 0 && M > 0 && N > 0) {
+    if (lda < (majorA == GB_K_MAJOR ? K : M)) return GB_ERR_INVALID_ARG;
+    if (ldb < (majorB == GB_K_MAJOR ? K : N)) return GB_ERR_INVALID_ARG;
+    if ((lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0) return GB_ERR_MISALIGNED;
+    if (lda * 2 >= (int64_t(1) << 40) || ldb * 2 >= (int64_t(1) << 40)) return GB_ERR_INVALID_ARG;
+  }
+  return GB_OK;
+}
+
+uint32_t make_idesc(int dtype, int majorA, int majorB) {
+  uint32_t d = 0;
+  d |= 1u << 4;                                     // accumulator format: fp32
+  d |= static_cast<uint32_t>(dtype == GB_BF16) << 7;   // A format: 0 fp16, 1 bf16
+  d |= static_cast<uint32_t>(dtype == GB_BF16) << 10;  // B format
+  d |= static_cast<uint32_t>(majorA) << 15;         // A: 0 K-major, 1 MN-major
+  d |= static_cast<uint32_t>(majorB) << 16;         // B: 0 K-major, 1 MN-major
+  d |= static_cast<uint32_t>(gb::kBN >> 3) << 17;   // N / 8
+  d |= static_cast<uint32_t>(gb::kBM >> 4) << 24;   // M / 16
+  return d;
+}
+
+gb_status make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
+                    int majorB, gb_gemm_plan* pl) {
+  gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB);
+  if (st != GB_OK) return st;
+  if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  std::memset(pl, 0, sizeof(*pl));
+  pl->tile_m = gb::kBM;
+  pl->tile_n = gb::kBN;
+  pl->tile_k = gb::kBK;
+  if (M == 0 || N == 0) return GB_OK;
+  try {
+    // D (and C): (M,N):(N,1) divided into (128,256) tiles -> ((tile),(grid))
+    la::Layout mD = la::make_layout({M, N}, {N, 1});
+    la::Layout zD = la::zipped_divide(mD, la::tiler_of({gb::kBM, gb::kBN}));
+    auto grid_shape = la::flatten(zD.mode(1).shape);
+    auto grid_stride = la::flatten(zD.mode(1).stride);
+    auto elem_stride = la::flatten(mD.stride);
+    pl->m_tiles = grid_shape[0];
+    pl->n_tiles = grid_shape[1];
+    pl->d_grid_stride[0] = grid_stride[0];
+    pl->d_grid_stride[1] = grid_stride[1];
+    pl->d_elem_stride[0] = elem_stride[0];
+    pl->d_elem_stride[1] = elem_stride[1];
+    pl->vector_epilogue = (pl->d_elem_stride[1] == 1 && N % 8 == 0) ? 1 : 0;
+    if (K > 0) {
+      OperandPlan a, b;
+      if ((st = plan_operand(M, K, lda, majorA, gb::kBM, &a)) != GB_OK) return st;
+      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, &b)) != GB_OK) return st;
+      if (a.grid_rows != pl->m_tiles || b.grid_rows != pl->n_tiles || a.k_blocks != b.k_blocks)
+        return GB_ERR_INVALID_ARG;
+      pl->k_blocks = a.k_blocks;
+      for (int i = 0; i < 2; ++i) {
+        pl->a_dim[i] = a.dim[i];
+        pl->a_box[i] = a.box[i];
+        pl->b_dim[i] = b.dim[i];
+        pl->b_box[i] = b.box[i];
+      }
+      pl->a_row_bytes = a.row_bytes;
+      pl->a_boxes = a.boxes;
+      pl->b_row_bytes = b.row_bytes;
+      pl->b_boxes = b.boxes;
+    }
+    const int64_t tiles = pl->m_tiles * pl->n_tiles;
+    if (tiles > (int64_t(1) << 31) - 1) return GB_ERR_INVALID_ARG;
+  } catch (const la::Error&) {
+    return GB_ERR_INVALID_ARG;
+  }
+  pl->instr_desc = make_idesc(dtype, majorA, majorB);
+  return GB_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
+                     const int64_t box[2], int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return GB_ERR_LAUNCH;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(dim[0]), static_cast<cuuint64_t>(dim[1])};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t bdim[2] = {static_cast<cuuint32_t>(box[0]), static_cast<cuuint32_t>(box[1])};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(map, dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  2, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
+}
+
+gb_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
+  if (dev < 0 || dev >= 128) return GB_ERR_UNSUPPORTED_ARCH;
+  DeviceState& d = g_dev[dev];
+  if (!d.probed) {
+    if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GB_ERR_UNSUPPORTED_ARCH;
+    d.probed = true;
+  }
+  if (d.major != 10 || d.minor != 3) return GB_ERR_UNSUPPORTED_ARCH;
+  *out = &d;
+  return GB_OK;
+}
+
+gb_status fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float alpha, int majorA,
+                      int majorB, float beta, const void* C, void* D, Params* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->M = static_cast<int32_t>(M);
+  p->N = static_cast<int32_t>(N);
+  p->K = static_cast<int32_t>(K);
+  p->m_tiles = static_cast<int32_t>(pl.m_tiles);
+  p->n_tiles = static_cast<int32_t>(pl.n_tiles);
+  p->k_blocks = static_cast<int32_t>(pl.k_blocks);
+  p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);
+  p->group_m = 16;
+  p->majorA = majorA;
+  p->majorB = majorB;
+  p->alpha = alpha;
+  p->beta = beta;
+  p->C = static_cast<const uint16_t*>(C);
+  p->D = static_cast<uint16_t*>(D);
+  p->d_grid_m = pl.d_grid_stride[0];
+  p->d_grid_n = pl.d_grid_stride[1];
+  p->d_row = pl.d_elem_stride[0];
+  p->d_col = pl.d_elem_stride[1];
+  p->idesc = pl.instr_desc;
+  p->vec_ok = pl.vector_epilogue;
+  p->has_c = beta != 0.0f ? 1 : 0;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    p->timeout_ns = g_timeout_ns;
+    p->skip_kb = g_skip_kb;
+  }
+  return GB_OK;
+}
+
+gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                     int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                     void* stream) {
+  gb_gemm_plan pl;
+  gb_status st = make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, &pl);
+  if (st != GB_OK) return st;
+  if (M == 0 || N == 0) return GB_OK;
+  if (D == nullptr) return GB_ERR_INVALID_ARG;
+  if (beta != 0.0f && C == nullptr) return GB_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B == nullptr)) return GB_ERR_INVALID_ARG;
+  if (!aligned16(D) || (C && !aligned16(C))) return GB_ERR_MISALIGNED;
+  if (K > 0 && (!aligned16(A) || !aligned16(B))) return GB_ERR_MISALIGNED;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != GB_OK) return st;
+
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (K > 0) {
+    if ((st = encode_map(&tmA, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype)) != GB_OK) return st;
+    if ((st = encode_map(&tmB, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype)) != GB_OK) return st;
+  }
+  Params p;
+  fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
+  const int grid = static_cast<int>(std::min<int64_t>(p.num_tiles, dev->sms));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == GB_BF16) {
+    if (!dev->smem_attr[1]) {
+      if (cudaFuncSetAttribute(gb::gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               gb::kSmemBytes) != cudaSuccess)
+        return GB_ERR_LAUNCH;
+      dev->smem_attr[1] = true;
+    }
+    gb::gemm_kernel<true><<<grid, gb::kThreads, gb::kSmemBytes, s>>>(tmA, tmB, p);
+  } else {
+    if (!dev->smem_attr[0]) {
+      if (cudaFuncSetAttribute(gb::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               gb::kSmemBytes) != cudaSuccess)
+        return GB_ERR_LAUNCH;
+      dev->smem_attr[0] = true;
+    }
+    gb::gemm_kernel<false><<<grid, gb::kThreads, gb::kSmemBytes, s>>>(tmA, tmB, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+gb_status gb_gemm_f16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
+                      const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                      void* stream) {
+  return gemm_entry(GB_F16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, stream);
+}
+
+gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
+                       const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                       void* stream) {
+  return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, stream);
+}
+
+gb_status gb_last_device_status(void* stream, uint32_t* detail) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GB_ERR_CUDA;
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, gb::g_status, sizeof(v)) != cudaSuccess) return GB_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(gb::g_status, &zero, sizeof(zero)) != cudaSuccess) return GB_ERR_CUDA;
+  if (detail) *detail = v;
+  return v == 0 ? GB_OK : GB_ERR_TIMEOUT;
+}
+
+const char* gb_status_string(int status) {
+  switch (status) {
+    case GB_OK: return "ok";
+    case GB_ERR_INVALID_ARG: return "invalid argument";
+    case GB_ERR_MISALIGNED: return "misaligned operand";
+    case GB_ERR_UNSUPPORTED_ARCH: return "unsupported architecture (needs compute capability 10.3)";
+    case GB_ERR_LAUNCH: return "launch failed";
+    case GB_ERR_TIMEOUT: return "device wait timed out";
+    case GB_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
+                            int majorB, gb_gemm_plan* plan) {
+  if (!plan) return GB_ERR_INVALID_ARG;
+  return make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, plan);
+}
+
+gb_status gb_set_wait_timeout_ns(uint64_t ns) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timeout_ns = ns == 0 ? gb::kDefaultTimeoutNs : ns;
+  return GB_OK;
+}
+
+gb_status gb_debug_skip_k_block(int64_t k_block) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_skip_kb = k_block < 0 ? -1 : k_block;
+  return GB_OK;
+}
+
+gb_status gb_debug_epilogue_map(int64_t M, int64_t N, int64_t m_tile, int64_t n_tile, int64_t* out,
+                                void* stream) {
+  gb_gemm_plan pl;
+  gb_status st = make_plan(GB_F16, M, N, 0, 0, GB_K_MAJOR, 0, GB_K_MAJOR, &pl);
+  if (st != GB_OK) return st;
+  if (M == 0 || N == 0 || !out || m_tile < 0 || n_tile < 0 || m_tile >= pl.m_tiles || n_tile >= pl.n_tiles)
+    return GB_ERR_INVALID_ARG;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != GB_OK) return st;
+  Params p;
+  fill_params(pl, M, N, 0, 1.0f, 0, 0, 0.0f, nullptr, nullptr, &p);
+  gb::epilogue_map_kernel<<<(gb::kBM * gb::kBN) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      p, static_cast<int32_t>(m_tile), static_cast<int32_t>(n_tile), out);
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64_t K, const void* A,
+                               int64_t lda, int majorA, const void* B, int64_t ldb, int majorB, int64_t tile,
+                               int64_t k_block, void* out, void* stream) {
+  gb_gemm_plan pl;
+  gb_status st = make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, &pl);
+  if (st != GB_OK) return st;
+  if (M == 0 || N == 0 || K == 0 || !out || (which != 0 && which != 1)) return GB_ERR_INVALID_ARG;
+  const void* base = which == 0 ? A : B;
+  if (!base || !aligned16(base) || !aligned16(out)) return GB_ERR_MISALIGNED;
+  const int64_t ntiles = which == 0 ? pl.m_tiles : pl.n_tiles;
+  if (tile < 0 || tile >= ntiles || k_block < 0 || k_block >= pl.k_blocks) return GB_ERR_INVALID_ARG;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != GB_OK) return st;
+  CUtensorMap tm;
+  st = which == 0 ? encode_map(&tm, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype)
+                  : encode_map(&tm, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype);
+  if (st != GB_OK) return st;
+  Params p;
+  fill_params(pl, M, N, K, 1.0f, majorA, majorB, 0.0f, nullptr, nullptr, &p);
+  const int smem = 1024 + gb::kStageBytes + gb::kCtlBytes;
+  if (!dev->dbg_attr) {
+    if (cudaFuncSetAttribute(gb::stage_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return GB_ERR_LAUNCH;
+    dev->dbg_attr = true;
+  }
+  gb::stage_bytes_kernel<<<1, 32, smem, static_cast<cudaStream_t>(stream)>>>(
+      tm, p, which, static_cast<int32_t>(tile), static_cast<int32_t>(k_block), static_cast<uint4*>(out));
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -138,13 +138,15 @@ def compose_table(a, b):
 
 
 def complement_by_search(b, m):
-    """Offsets at which translated copies of B's image tile an interval [0, M').
+    """Offsets at which translated copies of B's image tile a prefix [0, N), N >= m.
 
     Definition restated: the complement lists, in increasing order, where the copies of
-    "everything B touches" must start so that together with B they cover every offset
-    exactly once.  Found greedily: the next start is the smallest offset not yet covered.
-    Stops once [0, m) is covered.  Returns the list of starts, or None when B's image
-    cannot be tiled this way (then no complement exists).
+    "everything B touches" must start so that together with B they cover every offset of
+    a contiguous prefix [0, N) exactly once, with N at least the target m.  Found
+    greedily: the next start is always the smallest offset not yet covered; the search
+    stops at the first point where the target is reached and the covered set has no
+    holes.  Returns the list of starts, or None when B's image cannot be tiled this way
+    (then no complement exists).
     """
     image = table(b)
     if len(set(image)) != len(image):
@@ -153,7 +155,7 @@ def complement_by_search(b, m):
     covered = set()
     starts = []
     nxt = 0
-    while nxt < m:
+    while nxt < m or len(covered) != max(covered) + 1:
         for v in image:
             if nxt + v in covered:
                 return None
@@ -163,7 +165,7 @@ def complement_by_search(b, m):
         nxt = 0
         while nxt in covered:
             nxt += 1
-        if nxt > m + span:
+        if nxt > (m + span) * (span + 1):
             return None
     return starts
 

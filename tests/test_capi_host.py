@@ -1,0 +1,118 @@
+"""C ABI: every declared symbol is exported, and the host-side planning and validation
+(no GPU needed) behave as include/gb300_gemm.h states."""
+import os
+import re
+
+import pytest
+
+from layout_algebra_gb300 import _native, binding as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b((?:gb|la)_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = _native.lib()
+    decl = declared_functions()
+    assert len(decl) >= 20
+    missing = [n for n in decl if not hasattr(lib, n)]
+    assert not missing
+    assert set(decl) >= set(_native.GEMM_SYMBOLS) | set(_native.LAYOUT_SYMBOLS)
+
+
+def test_status_strings():
+    assert G.status_string(0) == "ok"
+    assert "misaligned" in G.status_string(2)
+    assert "10.3" in G.status_string(3)
+
+
+@pytest.mark.parametrize("name,M,N,K,majors,grid", [
+    ("gemm256_int_f16", 256, 256, 256, ("K", "K"), (2, 1, 4)),
+    ("gemm4096_f16", 4096, 4096, 4096, ("K", "K"), (32, 16, 64)),
+    ("gemm8192_bf16_c", 8192, 8192, 8192, ("K", "K"), (64, 32, 128)),
+    ("gemm16384x1024x4096_mnmajor_f16", 16384, 1024, 4096, ("MN", "MN"), (128, 4, 64)),
+    ("gemm5000x3000x4104_ragged_f16", 5000, 3000, 4104, ("K", "K"), (40, 12, 65)),
+])
+def test_plans_of_the_workloads(name, M, N, K, majors, grid):
+    lda = K if majors[0] == "K" else M
+    ldb = K if majors[1] == "K" else N
+    p = G.plan("f16", M, N, K, lda, majors[0], ldb, majors[1])
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
+    # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
+    for i, (ext, want) in enumerate(zip(grid[:2], [128 * N, 256])):
+        if ext > 1:
+            assert p["d_grid_stride"][i] == want
+    assert p["d_elem_stride"] == [N, 1]
+    if majors[0] == "K":
+        assert p["a_dim"] == [K, M] and p["a_box"] == [64, 128] and p["a_boxes"] == 1
+        assert p["a_row_bytes"] == 2 * lda
+    else:
+        assert p["a_dim"] == [M, K] and p["a_box"] == [64, 64] and p["a_boxes"] == 2
+    if majors[1] == "K":
+        assert p["b_dim"] == [K, N] and p["b_box"] == [64, 256] and p["b_boxes"] == 1
+    else:
+        assert p["b_dim"] == [N, K] and p["b_box"] == [64, 64] and p["b_boxes"] == 4
+    # instruction descriptor: fp32 accumulate, fp16 inputs, majors, N/8, M/16
+    d = p["instr_desc"]
+    assert (d >> 4) & 3 == 1 and (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0
+    assert (d >> 15) & 1 == (majors[0] == "MN") and (d >> 16) & 1 == (majors[1] == "MN")
+    assert (d >> 17) & 63 == 256 >> 3 and (d >> 24) & 31 == 128 >> 4
+    assert p["vector_epilogue"] == 1
+
+
+def test_plan_bf16_descriptor_and_scalar_epilogue():
+    p = G.plan("bf16", 129, 77, 40, 40, "K", 40, "K")
+    assert (p["instr_desc"] >> 7) & 7 == 1 and (p["instr_desc"] >> 10) & 7 == 1
+    assert p["vector_epilogue"] == 0          # rows of 77 elements are not 16-byte aligned
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (2, 1, 1)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((-1, 8, 8, 8, "K", 8, "K"), 1),
+    ((8, 8, 8, 4, "K", 8, "K"), 1),           # lda < K
+    ((8, 8, 8, 8, "MN", 8, "K"), 0),
+    ((8, 8, 12, 12, "K", 16, "K"), 2),        # lda*2 = 24 bytes: not a multiple of 16
+    ((8, 8, 8, 8, "K", 20, "K"), 2),
+    ((8, 8, 8, 8, "K", 8, 7), 1),             # bad major
+    ((1 << 31, 8, 8, 1 << 31, "MN", 8, "K"), 1),
+])
+def test_plan_validation(args, status):
+    M, N, K, lda, ma, ldb, mb = args
+    if isinstance(mb, int) and mb not in (0, 1):
+        rc = _native.lib().gb_gemm_make_plan(0, M, N, K, lda, 0, ldb, mb,
+                                             __import__("ctypes").byref(_native.GemmPlan()))
+        assert rc == status
+        return
+    if status == 0:
+        G.plan("f16", M, N, K, lda, ma, ldb, mb)
+    else:
+        with pytest.raises(G.GemmError) as e:
+            G.plan("f16", M, N, K, lda, ma, ldb, mb)
+        assert e.value.status == status
+
+
+def test_gemm_call_validation_without_gpu():
+    """Argument errors come back before any device is touched."""
+    lib = _native.lib()
+    # negative size
+    assert lib.gb_gemm_f16(-1, 8, 8, 1.0, 16, 8, 0, 16, 8, 0, 0.0, None, 16, None) == 1
+    # empty problem: nothing to do
+    assert lib.gb_gemm_f16(0, 8, 8, 1.0, None, 8, 0, None, 8, 0, 0.0, None, None, None) == 0
+    # beta != 0 needs C
+    assert lib.gb_gemm_f16(8, 8, 8, 1.0, 16, 8, 0, 16, 8, 0, 1.0, None, 16, None) == 1
+    # D missing
+    assert lib.gb_gemm_f16(8, 8, 8, 1.0, 16, 8, 0, 16, 8, 0, 0.0, None, None, None) == 1
+    # misaligned pointers
+    assert lib.gb_gemm_bf16(8, 8, 8, 1.0, 18, 8, 0, 16, 8, 0, 0.0, None, 16, None) == 2
+    assert lib.gb_gemm_bf16(8, 8, 8, 1.0, 16, 8, 0, 16, 8, 0, 0.0, None, 24, None) == 2
