@@ -1,0 +1,398 @@
+"""Throughput of the sm_103a GEMM D = alpha*A*B + beta*C on synthetic operands.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one GEMM over the workload (default: 8192^3 bf16 with C, alpha 1.25,
+beta 0.5).  Operands are generated on the host from fixed seeds, copied to the device
+once, and stay resident; the timed region holds K back-to-back launches through the C
+ABI, bracketed by a barrier and a device synchronise, timed with CUDA events on the
+launching stream.  The working set (A, B, C, D) is larger than L2, so no flush is needed
+between steps.  Under torchrun every rank runs its own replica (there is no exchange
+step in a GEMM), and the slowest rank's time sets the aggregate.
+
+The JSON line carries: value (TFLOP/s, all ranks), e2e (same metric through the public
+API with pinned host buffers, copies inside the timed region), roofline (the kernel's
+average launch time against the measured tensor peak), clocks sampled during the timed
+region, and cpu_baseline (the CPU checker timed on a bounded sample of the same problem).
+--impl reference times that CPU checker alone, on rank 0.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNK/s) at 8192^3 fp16->fp32 acc; % of GB300 dense FP16 peak"
+DEFAULT_WORKLOAD = "gemm8192_bf16_c"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/ptx.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="CPU time budget of the whole reference run")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_source_hash():
+        return None
+    w = d.get("workloads", {}).get(workload)
+    return None if w is None else w.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(elapsed_s, units, world, device=None):
+    """(max elapsed over ranks, sum of units over ranks); plain values when world == 1."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), u.item()
+
+
+def barrier(world, local):
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[local])
+        else:
+            dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples, each stamped with its arrival time."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            inside = [p for _, p in self.samples]
+            window = "whole run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[5:9]) if v.lower() == "active"})
+        power = [num(p[3]) for p in inside if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+def oracle_sample(problem, data, seconds, max_rows=None):
+    """Time the CPU checker on whole rows of D until `seconds` elapse (at least one row)."""
+    import numpy as np
+    from layout_algebra_gb300 import workloads as W
+    from oracle import gemm_ref as O
+    p = problem
+    A, B = W.bits(data["A"]), W.bits(data["B"])
+    C = W.bits(data["C"]) if data["C"] is not None else None
+    code = O.dtype_code(p.dtype)
+    ma = 0 if p.majorA == "K" else 1
+    mb = 0 if p.majorB == "K" else 1
+    threads = O.max_threads()
+    cols_all = np.arange(p.N, dtype=np.int64)
+
+    def run_rows(r0, nrows, ncols):
+        rows = np.repeat(np.arange(r0, r0 + nrows, dtype=np.int64), ncols)
+        cols = np.tile(cols_all[:ncols], nrows)
+        t = time.perf_counter()
+        O.gemm(p.M, p.N, p.K, p.alpha, A, data["lda"], ma, B, data["ldb"], mb, p.beta, C, p.N,
+               code, rows, cols, threads=threads)
+        return time.perf_counter() - t
+
+    # probe with a slice of one row, then size the sample to the time budget
+    probe_cols = min(p.N, 1024)
+    tp = run_rows(0, 1, probe_cols)
+    per_entry = max(tp / probe_cols, 1e-9)
+    entries = int(seconds / per_entry)
+    rows = max(1, min(entries // p.N, p.M if max_rows is None else max_rows))
+    if entries < p.N:
+        ncols = max(1, min(p.N, entries))
+        rows = 1
+    else:
+        ncols = p.N
+    t = run_rows(0, rows, ncols)
+    n_out = rows * ncols
+    return {"seconds": t, "outputs": n_out, "rows": rows, "cols": ncols, "threads": threads,
+            "flops": 2.0 * n_out * p.K}
+
+
+# ----------------------------------------------------------------------------- arms
+
+
+def run_reference(args):
+    """The CPU checker as it stands, on host cores, over bounded samples of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from layout_algebra_gb300 import workloads as W
+    p = W.WORKLOADS[args.workload]
+    data = W.make(p)
+    total_budget = args.ref_seconds
+    per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(p, data, per_step)
+    flops = secs = 0.0
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(p, data, per_step)
+        flops += last["flops"]
+        secs += last["seconds"]
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(p),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": last["threads"], "kind": "oracle",
+                         "sample": "each step: %d row(s) x %d column(s) of D of the %s problem "
+                                   "(fp64 triple loop, OpenMP over outputs)"
+                                   % (last["rows"], last["cols"], p.name)},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(p):
+    return {"workload": p.name, "M": p.M, "N": p.N, "K": p.K, "operand_dtype": p.dtype,
+            "majorA": p.majorA, "majorB": p.majorB, "alpha": p.alpha, "beta": p.beta,
+            "has_C": p.has_c, "values": p.dist, "seed": p.seed,
+            "l2": "inputs larger than L2 (no flush between steps)"
+            if p.algorithmic_bytes > 256 * 2**20 else "working set may fit in L2",
+            "parallelism": "replicas"}
+
+
+def run_gb300(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from layout_algebra_gb300 import binding as G
+    from layout_algebra_gb300 import workloads as W
+    p = W.WORKLOADS[args.workload]
+    data = W.make(p)
+    A, B = data["A"].to(dev), data["B"].to(dev)
+    C = data["C"].to(dev) if data["C"] is not None else None
+    D = torch.empty(p.M * p.N, dtype=A.dtype, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    lda, ldb = data["lda"], data["ldb"]
+    cptr = C.data_ptr() if C is not None else None
+
+    def launch():
+        st = G.raw_call(A.dtype, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda, p.majorA, B.data_ptr(), ldb,
+                        p.majorB, p.beta, cptr, D.data_ptr(), sh)
+        if st != 0:
+            raise G.GemmError(st)
+
+    for _ in range(max(3, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    st, detail = G.last_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d (%#x) during warm-up" % (st, detail))
+
+    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    sampler = ClockSampler(phys)
+    time.sleep(0.3)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world, local)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world, local)
+    time.sleep(0.15)
+    sampler.stop()
+    st, detail = G.last_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d (%#x) in the timed region" % (st, detail))
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    elapsed_s, total_flops = aggregate(total_ms / 1e3, float(p.flops) * args.steps, world, dev)
+    value = total_flops / elapsed_s / 1e12
+    clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
+
+    # end to end through the public API with pinned host buffers
+    A_h, B_h = data["A"].pin_memory(), data["B"].pin_memory()
+    C_h = data["C"].pin_memory() if data["C"] is not None else None
+    D_h = torch.empty(p.M * p.N, dtype=A.dtype, pin_memory=True)
+    for _ in range(2):
+        G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
+               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h)
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    barrier(world, local)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
+               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world, local)
+    e2e_s, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, float(p.flops) * e2e_steps, world, dev)
+    h2d = (data["A"].numel() + data["B"].numel() + (data["C"].numel() if data["C"] is not None else 0)) * 2
+    d2h = p.M * p.N * 2
+    st, detail = G.last_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d (%#x) in the end-to-end region" % (st, detail))
+
+    peaks, peak_src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = p.flops / (kernel_ms / 1e3) / 1e12
+    traffic = load_traffic(p.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+                "frac": achieved / burst, "traffic": traffic,
+                "peak_source": "%s burst (MEASURED_PEAKS.json bf16_tflops); fp16 and bf16 share the rate"
+                               % peak_src,
+                "frac_of_sustained": achieved / sustained, "frac_of_nominal_2250": achieved / 2250.0,
+                "kernel": "gb::gemm_kernel", "kernel_ms": kernel_ms,
+                "algorithmic_flops_per_launch": p.flops,
+                "algorithmic_bytes_per_launch": p.algorithmic_bytes}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
+        "config": workload_config(p),
+        "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "roofline": roofline, "clocks": clocks, "gpu_launches": args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample(p, data, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": s["flops"] / s["seconds"] / 1e12, "unit": "TFLOP/s", "cores": s["threads"],
+            "kind": "oracle",
+            "sample": "%d row(s) x %d column(s) of D of the %s problem, fp64 triple loop with "
+                      "OpenMP over outputs, %.1f s" % (s["rows"], s["cols"], p.name, s["seconds"])}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
