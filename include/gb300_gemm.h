@@ -5,10 +5,12 @@
  * K x N, C and D are M x N; 16-bit inputs (fp16 or bf16, named by the symbol), products
  * accumulated in fp32, alpha/beta applied in fp32, D rounded to nearest even.
  *
- * A CTA owns a 128 x 256 output tile and walks K in steps of 64 with A/B slices staged
- * in shared memory ("CUTLASS, in depth" — "The problem CUTLASS solves", tiling); tile
- * and element addressing come from shape:stride layouts divided into (tile, grid) modes
- * ("Day 84: CUTLASS and CuTe layouts" — "A layout is a shape and a stride").
+ * A CTA (or a pair of CTAs on two SMs) owns an output tile (128 x 256, or 256 x 256 for
+ * a pair) and walks K in steps of 64 with A/B slices staged in shared memory ("CUTLASS,
+ * in depth" — "The problem CUTLASS solves", tiling); tile and element addressing come
+ * from shape:stride layouts divided into (tile, grid) modes ("Day 84: CUTLASS and CuTe
+ * layouts" — "A layout is a shape and a stride").  The pair variant is used when
+ * M > 128, the single-CTA variant otherwise (gb_set_kernel_variant overrides this).
  *
  * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
  * "One notation, and no more transposes"):
@@ -84,16 +86,17 @@ const char* gb_status_string(int status);
    Pure host computation (no GPU needed), same validation as the GEMM call except the
    pointer and device checks. */
 typedef struct {
-  int64_t m_tiles, n_tiles, k_blocks;   /* grid of 128 x 256 output tiles, K steps of 64 */
-  int64_t tile_m, tile_n, tile_k;       /* 128, 256, 64 */
+  int64_t m_tiles, n_tiles, k_blocks;   /* grid of tile_m x 256 output tiles, K steps of 64 */
+  int64_t tile_m, tile_n, tile_k;       /* 128 (single) or 256 (pair), 256, 64 */
   int64_t a_dim[2], a_row_bytes;        /* A copy: extents (inner first), row pitch */
-  int64_t a_box[2], a_boxes;            /* box extents (inner first) and boxes per stage */
+  int64_t a_box[2], a_boxes;            /* box extents (inner first), boxes per stage per CTA */
   int64_t b_dim[2], b_row_bytes;
   int64_t b_box[2], b_boxes;
   int64_t d_grid_stride[2];             /* D offset step per tile along M and along N */
   int64_t d_elem_stride[2];             /* D offset step per row and per column */
   uint32_t instr_desc;                  /* tensor-core instruction descriptor */
   int32_t vector_epilogue;              /* 1 when 16-byte C/D accesses are legal */
+  int32_t variant;                      /* 1: single CTA, 2: CTA pair */
 } gb_gemm_plan;
 
 gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
@@ -107,17 +110,23 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
 gb_status gb_set_wait_timeout_ns(uint64_t ns);
 gb_status gb_debug_skip_k_block(int64_t k_block);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue uses for tile
-   (m_tile, n_tile) of an M x N problem: out[r*256 + c] = offset of in-tile element
-   (r, c) (r < 128, c < 256), or -1 when the element lies outside M x N.  out is a device
-   buffer of 32768 int64.  Asynchronous on stream. */
-gb_status gb_debug_epilogue_map(int64_t M, int64_t N, int64_t m_tile, int64_t n_tile,
-                                int64_t* out, void* stream);
+/* Kernel variant for later calls (process-wide): 0 chooses by shape (the default), 1 the
+   single-CTA 128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel.  GB_ERR_INVALID_ARG for
+   other values. */
+gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: copy one pipeline stage of operand A (which = 0) or B (which = 1) for
-   (tile, k_block) into shared memory exactly as the GEMM's copy stage does, then write
-   the raw shared-memory bytes to `out` (a device buffer of 16384 bytes for A, 32768 for
-   B).  Checks the tensor-copy geometry and the 128-byte swizzle. */
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1 or 2)
+   uses for tile (m_tile, n_tile) of an M x N problem: out[r*256 + c] = offset of in-tile
+   element (r, c) (r < tile_m, c < 256), or -1 when the element lies outside M x N.  out is
+   a device buffer of tile_m * 256 int64.  Asynchronous on stream. */
+gb_status gb_debug_epilogue_map(int variant, int64_t M, int64_t N, int64_t m_tile,
+                                int64_t n_tile, int64_t* out, void* stream);
+
+/* Test hook: copy one pipeline stage of operand A (which = 0) or B (which = 1) of the
+   single-CTA kernel for (tile, k_block) into shared memory exactly as its copy stage
+   does, then write the raw shared-memory bytes to `out` (a device buffer of 16384 bytes
+   for A, 32768 for B); `tile` is the M-tile for A and the N-tile for B.  Checks the
+   tensor-copy geometry and the 128-byte swizzle. */
 gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, int majorA,
                                const void* B, int64_t ldb, int majorB,

@@ -12,7 +12,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgb300gem
 GEMM_SYMBOLS = [
     "gb_gemm_f16", "gb_gemm_bf16", "gb_last_device_status", "gb_status_string",
     "gb_gemm_make_plan", "gb_set_wait_timeout_ns", "gb_debug_skip_k_block",
-    "gb_debug_epilogue_map", "gb_debug_stage_bytes",
+    "gb_debug_epilogue_map", "gb_debug_stage_bytes", "gb_set_kernel_variant",
 ]
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
@@ -35,6 +35,7 @@ class GemmPlan(ctypes.Structure):
         ("b_box", ctypes.c_int64 * 2), ("b_boxes", ctypes.c_int64),
         ("d_grid_stride", ctypes.c_int64 * 2), ("d_elem_stride", ctypes.c_int64 * 2),
         ("instr_desc", ctypes.c_uint32), ("vector_epilogue", ctypes.c_int32),
+        ("variant", ctypes.c_int32),
     ]
 
 
@@ -66,7 +67,9 @@ def lib():
     L.gb_debug_skip_k_block.restype = ci
     L.gb_debug_skip_k_block.argtypes = [i64]
     L.gb_debug_epilogue_map.restype = ci
-    L.gb_debug_epilogue_map.argtypes = [i64, i64, i64, i64, vp, vp]
+    L.gb_debug_epilogue_map.argtypes = [ci, i64, i64, i64, i64, vp, vp]
+    L.gb_set_kernel_variant.restype = ci
+    L.gb_set_kernel_variant.argtypes = [ci]
     L.gb_debug_stage_bytes.restype = ci
     L.gb_debug_stage_bytes.argtypes = [ci, ci, i64, i64, i64, vp, i64, ci, vp, i64, ci, i64,
                                        i64, vp, vp]

@@ -121,3 +121,10 @@ def set_wait_timeout_ns(ns):
 
 def debug_skip_k_block(kb):
     lib().gb_debug_skip_k_block(int(kb))
+
+
+def set_kernel_variant(variant):
+    """0: choose by shape; 1: single-CTA 128x256 kernel; 2: CTA-pair 256x256 kernel."""
+    st = lib().gb_set_kernel_variant(int(variant))
+    if st != 0:
+        raise GemmError(st, "set_kernel_variant")

@@ -44,23 +44,38 @@
 
 namespace gb {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBN = 256;             // output tile columns (one MMA's N)
 constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
-constexpr int kStages = 4;
+constexpr int kRowsA = 128;          // A rows staged per CTA (one MMA's M per SM)
 constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
 constexpr int kSwz = 64;             // elements per 128-byte swizzle span
-constexpr int kAStage = kBM * kBK * 2;
-constexpr int kBStage = kBN * kBK * 2;
-constexpr int kStageBytes = kAStage + kBStage;
 constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
 constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kCtlBytes = 256;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+constexpr int kMaxStages = 6;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
-static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
+
+// Two variants share all code:
+//  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64;
+//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x 256 tile; each CTA
+//         stages its own 128 A rows and 128 of the 256 B rows (6 stages of 32 KiB), the even
+//         CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory,
+//         and each CTA's TMEM holds its own 128 rows of the accumulator.
+template <bool kPair>
+struct Cfg {
+  static constexpr int kTileM = kPair ? 256 : 128;
+  static constexpr int kRowsB = kPair ? 128 : 256;
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kAStage = kRowsA * kBK * 2;
+  static constexpr int kBStage = kRowsB * kBK * 2;
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr uint32_t kTxBytes = kStageBytes * (kPair ? 2 : 1);   // bytes per full barrier
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+  static constexpr uint32_t kAccEmptyArrivals = 4 * (kPair ? 2 : 1);   // epilogue warps
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
+  static_assert(kStages <= kMaxStages, "control block");
+};
 static_assert(kTmemCols <= 512, "Tensor Memory holds 512 columns per SM");
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -80,8 +95,8 @@ struct Params {
 };
 
 struct Ctl {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -97,31 +112,42 @@ enum : uint32_t {
   kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
   kSiteDrain = 5,     // abort path: waiting for own operations in flight
   kSiteTail = 6,      // copy stage waiting for the last releases before exit
-  kSiteDebug = 7,
 };
 
 __device__ uint32_t g_status;
 
+// Record the first failing wait, and stop this CTA (and its peer, in a pair).
+template <bool kPair>
 __device__ __forceinline__ void raise_status(Ctl* ctl, uint32_t site) {
   atomicCAS(&g_status, 0u, site | (blockIdx.x << 8));
   *reinterpret_cast<volatile int32_t*>(&ctl->abort) = 1;
+  if constexpr (kPair) st_cluster_u32(map_to_cta(smem_addr(&ctl->abort), cluster_ctarank() ^ 1u), 1u);
 }
 
 __device__ __forceinline__ bool aborted(Ctl* ctl) {
   return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0;
 }
 
+template <bool kCluster>
+__device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) {
+  if constexpr (kCluster)
+    return mbar_try_wait_cluster(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
+
 // Single-thread bounded wait; gives up on the abort flag or the time limit.
+template <bool kPair>
 __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
                                       uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (probe<kPair>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe<kPair>(bar, parity)) return true;
     if ((n & 7) == 0) {
       if (aborted(ctl)) return false;
       if (global_timer_ns() - t0 > limit) {
-        raise_status(ctl, site);
+        raise_status<kPair>(ctl, site);
         return false;
       }
     }
@@ -141,11 +167,12 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 }
 
 // Warp-collective bounded wait with a warp-uniform outcome.
+template <bool kPair>
 __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
                                        uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 0;; ++n) {
-    const bool ok = mbar_try_wait(bar, parity);
+    const bool ok = probe<kPair>(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
     if ((n & 7) == 7) {
       int stop = 0;
@@ -153,7 +180,7 @@ __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, 
         if (aborted(ctl)) {
           stop = 1;
         } else if (global_timer_ns() - t0 > limit) {
-          raise_status(ctl, site);
+          raise_status<kPair>(ctl, site);
           stop = 1;
         }
       }
@@ -181,27 +208,23 @@ __device__ __forceinline__ int64_t d_offset(const Params& p, int32_t mt, int32_t
   return mt * p.d_grid_m + nt * p.d_grid_n + r * p.d_row + c * p.d_col;
 }
 
-// Copies of one k-block.  K-major operand: one box of 64 (K) x rows.  MN-major operand:
-// rows/64 boxes of 64 (M or N) x 64 (K), each 8 KiB, placed one after another.
-__device__ __forceinline__ void issue_a(const Params& p, const void* tm, uint32_t dst,
-                                       uint32_t bar, int32_t mt, int32_t kb) {
-  if (p.majorA == 0) {
-    tma_load_2d(dst, tm, bar, kb * kBK, mt * kBM);
+// Copies of one k-block of one operand, `rows` rows starting at row0.  K-major: one box of
+// 64 (K) x rows.  MN-major: rows/64 boxes of 64 (M or N) x 64 (K), 8 KiB each, back to back.
+template <bool kPair>
+__device__ __forceinline__ void issue_operand(int major, const void* tm, uint32_t dst, uint32_t bar,
+                                              int32_t row0, int rows, int32_t kb) {
+  if (major == 0) {
+    if constexpr (kPair)
+      tma_load_2d_pair(dst, tm, bar, kb * kBK, row0);
+    else
+      tma_load_2d(dst, tm, bar, kb * kBK, row0);
   } else {
-#pragma unroll
-    for (int j = 0; j < kBM / kSwz; ++j)
-      tma_load_2d(dst + j * kChunkBytes, tm, bar, mt * kBM + j * kSwz, kb * kBK);
-  }
-}
-
-__device__ __forceinline__ void issue_b(const Params& p, const void* tm, uint32_t dst,
-                                       uint32_t bar, int32_t nt, int32_t kb) {
-  if (p.majorB == 0) {
-    tma_load_2d(dst, tm, bar, kb * kBK, nt * kBN);
-  } else {
-#pragma unroll
-    for (int j = 0; j < kBN / kSwz; ++j)
-      tma_load_2d(dst + j * kChunkBytes, tm, bar, nt * kBN + j * kSwz, kb * kBK);
+    for (int j = 0; j < rows / kSwz; ++j) {
+      if constexpr (kPair)
+        tma_load_2d_pair(dst + j * kChunkBytes, tm, bar, row0 + j * kSwz, kb * kBK);
+      else
+        tma_load_2d(dst + j * kChunkBytes, tm, bar, row0 + j * kSwz, kb * kBK);
+    }
   }
 }
 
@@ -216,33 +239,39 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k
   return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
 }
 
+template <bool kPair>
 __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, uint8_t* smem,
-                             Ctl* ctl) {
+                             Ctl* ctl, uint32_t rank, uint32_t cluster, uint32_t nclusters) {
+  using C = Cfg<kPair>;
   int stage = 0;
   uint32_t phase = 0;
   int64_t gkb = 0;
   uint32_t issued = 0, issued_parity = 0;
   bool ok = true;
-  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+  for (int32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
     int32_t mt, nt;
     tile_coords(p, t, mt, nt);
+    const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(rank) * kRowsA;
+    const int32_t b_row0 = nt * kBN + static_cast<int32_t>(rank) * C::kRowsB;
     for (int32_t kb = 0; kb < p.k_blocks; ++kb, ++gkb) {
-      if (!wait_one(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
+      if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
         ok = false;
         break;
       }
       if (gkb != p.skip_kb) {
         const uint32_t full = smem_addr(&ctl->full[stage]);
-        const uint32_t sa = smem_addr(smem + stage * kStageBytes);
-        mbar_arrive_expect_tx(full, kStageBytes);
-        issue_a(p, tmA, sa, full, mt, kb);
-        issue_b(p, tmB, sa + kAStage, full, nt, kb);
+        // in a pair both CTAs' copies are counted on the even CTA's barrier
+        const uint32_t full_tgt = kPair ? map_to_cta(full, 0) : full;
+        const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
+        if (!kPair || rank == 0) mbar_arrive_expect_tx(full, C::kTxBytes);
+        issue_operand<kPair>(p.majorA, tmA, sa, full_tgt, a_row0, kRowsA, kb);
+        issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage, full_tgt, b_row0, C::kRowsB, kb);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       } else {
         issued &= ~(1u << stage);
       }
-      if (++stage == kStages) {
+      if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -251,61 +280,86 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   if (ok) {
     // The consumer releases stages through asynchronous arrivals; wait for the last
     // kStages releases so that none lands after this CTA's shared memory is gone.
-    for (int i = 0; i < kStages; ++i) {
-      if (!wait_one(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteTail)) break;
-      if (++stage == kStages) {
+    for (int i = 0; i < C::kStages; ++i) {
+      if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteTail)) break;
+      if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-  } else {
-    for (int s = 0; s < kStages; ++s)
+  } else if (!kPair || rank == 0) {
+    for (int s = 0; s < C::kStages; ++s)
       if (issued & (1u << s))
         wait_drain(smem_addr(&ctl->full[s]), (issued_parity >> s) & 1u, p.timeout_ns);
+  } else {
+    // the odd CTA's copies complete on the even CTA's barrier, which it cannot observe;
+    // a copy of 32 KiB lands in microseconds
+    __nanosleep(200000);
   }
 }
 
-__device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base) {
+template <bool kPair>
+__device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
+                        uint32_t cluster, uint32_t nclusters) {
+  using C = Cfg<kPair>;
+  if (kPair && rank != 0) return;          // the even CTA issues for the pair
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true, issued_any = false;
   int32_t it = 0;
-  for (int32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+  for (int32_t t = cluster; ok && t < p.num_tiles; t += nclusters, ++it) {
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
-    if (!wait_one(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns, kSiteAccEmpty)) {
+    if (!wait_one<kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns, kSiteAccEmpty)) {
       ok = false;
       break;
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + buf * kBN;
     for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
-      if (!wait_one(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
+      if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const uint32_t sa = smem_addr(smem + stage * kStageBytes);
-      const uint32_t sb = sa + kAStage;
+      const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
+      const uint32_t sb = sa + C::kAStage;
 #pragma unroll
-      for (int k = 0; k < kBK / kUmmaK; ++k)
-        tc_mma_f16(d_tmem, operand_desc(sa, p.majorA, k), operand_desc(sb, p.majorB, k), p.idesc,
-                   (kb | k) != 0 ? 1u : 0u);
+      for (int k = 0; k < kBK / kUmmaK; ++k) {
+        const uint64_t da = operand_desc(sa, p.majorA, k), db = operand_desc(sb, p.majorB, k);
+        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+        if constexpr (kPair)
+          tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
+        else
+          tc_mma_f16(d_tmem, da, db, p.idesc, acc);
+      }
       issued_any = true;
-      tc_commit(smem_addr(&ctl->empty[stage]));
-      if (++stage == kStages) {
+      if constexpr (kPair)
+        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
+      else
+        tc_commit(smem_addr(&ctl->empty[stage]));
+      if (++stage == C::kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    if (p.k_blocks == 0)
-      mbar_arrive(smem_addr(&ctl->acc_full[buf]));
-    else
-      tc_commit(smem_addr(&ctl->acc_full[buf]));
+    const uint32_t af = smem_addr(&ctl->acc_full[buf]);
+    if (p.k_blocks == 0) {
+      mbar_arrive(af);
+      if constexpr (kPair) mbar_arrive_cluster(map_to_cta(af, 1));
+    } else {
+      if constexpr (kPair)
+        tc_commit_pair_mc(af, 0x3);
+      else
+        tc_commit(af);
+    }
   }
   if (!ok && issued_any) {
-    tc_commit(smem_addr(&ctl->drain));
+    if constexpr (kPair)
+      tc_commit_pair(smem_addr(&ctl->drain));
+    else
+      tc_commit(smem_addr(&ctl->drain));
     wait_drain(smem_addr(&ctl->drain), 0u, p.timeout_ns);
     __nanosleep(20000);   // let the arrivals of earlier commits land
   }
@@ -380,19 +434,21 @@ __device__ __forceinline__ void store_run(const Params& p, int64_t off, const ui
   }
 }
 
-template <bool kBF16>
-__device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane) {
+template <bool kBF16, bool kPair>
+__device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
+                             uint32_t rank, uint32_t cluster, uint32_t nclusters) {
+  using C = Cfg<kPair>;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
-  const int r = q * 32 + lane;       // accumulator row = TMEM lane
+  const int r = static_cast<int>(rank) * kRowsA + q * 32 + lane;   // row within the tile
   int32_t it = 0;
-  for (int32_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+  for (int32_t t = cluster; t < p.num_tiles; t += nclusters, ++it) {
     int32_t mt, nt;
     tile_coords(p, t, mt, nt);
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
-    if (!wait_warp(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
+    if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
     tc_fence_after_sync();
-    const bool row_ok = static_cast<int64_t>(mt) * kBM + r < p.M;
+    const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
     const int32_t cols_left = p.N - nt * kBN;
     const int64_t base = d_offset(p, mt, nt, r, 0);
     for (int c0 = 0; c0 < kBN && c0 < cols_left; c0 += 32) {
@@ -407,7 +463,14 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       if (row_ok) store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0));
     }
     tc_fence_before_sync();
-    mbar_arrive(smem_addr(&ctl->acc_empty[buf]));
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
+      if constexpr (kPair)
+        mbar_arrive_cluster(map_to_cta(ae, 0));
+      else
+        mbar_arrive(ae);
+    }
   }
 }
 
@@ -415,24 +478,28 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
+  using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStages * C::kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t cluster = kPair ? cluster_id_x() : blockIdx.x;
+  const uint32_t nclusters = kPair ? cluster_count_x() : gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
       mbar_init(smem_addr(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
-      mbar_init(smem_addr(&ctl->acc_empty[b]), kEpiThreads);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), C::kAccEmptyArrivals);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
@@ -443,51 +510,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // peer barriers initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer(p, &tmA, &tmB, smem, ctl);
+    if (lane == 0) run_producer<kPair>(p, &tmA, &tmB, smem, ctl, rank, cluster, nclusters);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma(p, smem, ctl, tmem_base);
+    if (lane == 0) run_mma<kPair>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
-    run_epilogue<kBF16>(p, ctl, tmem_base, warp, lane);
+    run_epilogue<kBF16, kPair>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
   }
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // no remote arrival or MMA targets a CTA that left
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 // ------------------------------------------------------------------ test kernels
-__global__ void epilogue_map_kernel(const Params p, int32_t mt, int32_t nt, int64_t* out) {
+__global__ void epilogue_map_kernel(const Params p, int32_t tile_m, int32_t mt, int32_t nt,
+                                    int64_t* out) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= kBM * kBN) return;
+  if (idx >= tile_m * kBN) return;
   const int r = idx / kBN, c = idx % kBN;
-  const int64_t row = static_cast<int64_t>(mt) * kBM + r;
+  const int64_t row = static_cast<int64_t>(mt) * tile_m + r;
   const int64_t col = static_cast<int64_t>(nt) * kBN + c;
   out[idx] = (row < p.M && col < p.N) ? d_offset(p, mt, nt, r, c) : -1;
 }
 
-// One CTA of 32 threads: copy one stage of A (which == 0) or B (which == 1) exactly as the
-// producer does, then dump the raw shared-memory bytes.
+// One CTA of 32 threads: copy one stage of A (which == 0) or B (which == 1) of the single
+// variant exactly as its producer does, then dump the raw shared-memory bytes.
 __global__ void __launch_bounds__(32, 1)
     stage_bytes_kernel(const __grid_constant__ CUtensorMap tm, const Params p, int which,
                        int32_t tile, int32_t kb, uint4* out) {
+  using C = Cfg<false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStageBytes);
-  const int bytes = which == 0 ? kAStage : kBStage;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStageBytes);
+  const int rows = which == 0 ? kRowsA : C::kRowsB;
+  const int bytes = rows * kBK * 2;
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&ctl->full[0]), 1);
     ctl->abort = 0;
@@ -497,10 +577,8 @@ __global__ void __launch_bounds__(32, 1)
   if (threadIdx.x == 0) {
     const uint32_t full = smem_addr(&ctl->full[0]);
     mbar_arrive_expect_tx(full, bytes);
-    if (which == 0)
-      issue_a(p, &tm, smem_addr(smem), full, tile, kb);
-    else
-      issue_b(p, &tm, smem_addr(smem), full, tile, kb);
+    issue_operand<false>(which == 0 ? p.majorA : p.majorB, &tm, smem_addr(smem), full, tile * rows,
+                         rows, kb);
     wait_drain(full, 0u, p.timeout_ns);
   }
   __syncthreads();
@@ -518,44 +596,48 @@ using gb::Params;
 std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
+int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair
+
+constexpr int kVariantSingle = 1;
+constexpr int kVariantPair = 2;
 
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
-  bool smem_attr[2] = {false, false};
+  bool attr_single[2] = {false, false};
+  bool attr_pair[2] = {false, false};
+  int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
   bool dbg_attr = false;
 };
 DeviceState g_dev[128];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  });
   return fn;
 }
 
 // Copy geometry of one operand, read off its layout: the stride-1 mode is the copy's
-// inner dimension; the other mode's stride is the row pitch.
+// inner dimension; the other mode's stride is the row pitch.  `tile_rows` is the tile
+// extent along the operand's rows (for the grid), `cta_rows` the rows one CTA stages.
 struct OperandPlan {
   int64_t dim[2], row_bytes, box[2], boxes;
   int64_t grid_rows, k_blocks;
 };
 
 gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t tile_rows,
-                       OperandPlan* o) {
-  // (rows, K) layout of the stored operand
+                       int64_t cta_rows, OperandPlan* o) {
   la::Layout m = major == GB_K_MAJOR ? la::make_layout({rows, K}, {ld, 1}) : la::make_layout({rows, K}, {1, ld});
   la::Layout z = la::zipped_divide(m, la::tiler_of({tile_rows, gb::kBK}));
-  // grid mode: (row tiles, k-blocks)
-  auto grid = la::flatten(z.mode(1).shape);
+  auto grid = la::flatten(z.mode(1).shape);   // (row tiles, k-blocks)
   o->grid_rows = grid[0];
   o->k_blocks = grid[1];
   auto modes = la::flat_modes(m);
@@ -565,7 +647,7 @@ gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t t
     o->dim[1] = rows;
     o->row_bytes = s_rows * 2;
     o->box[0] = gb::kSwz;
-    o->box[1] = tile_rows;
+    o->box[1] = cta_rows;
     o->boxes = 1;
   } else if (s_rows == 1) {
     o->dim[0] = rows;
@@ -573,7 +655,7 @@ gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t t
     o->row_bytes = s_k * 2;
     o->box[0] = gb::kSwz;
     o->box[1] = gb::kBK;
-    o->boxes = tile_rows / gb::kSwz;
+    o->boxes = cta_rows / gb::kSwz;
   } else {
     return GB_ERR_INVALID_ARG;
   }
@@ -596,32 +678,47 @@ gb_status validate_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int major
   return GB_OK;
 }
 
-uint32_t make_idesc(int dtype, int majorA, int majorB) {
+uint32_t make_idesc(int dtype, int majorA, int majorB, int tile_m) {
   uint32_t d = 0;
-  d |= 1u << 4;                                     // accumulator format: fp32
+  d |= 1u << 4;                                        // accumulator format: fp32
   d |= static_cast<uint32_t>(dtype == GB_BF16) << 7;   // A format: 0 fp16, 1 bf16
   d |= static_cast<uint32_t>(dtype == GB_BF16) << 10;  // B format
-  d |= static_cast<uint32_t>(majorA) << 15;         // A: 0 K-major, 1 MN-major
-  d |= static_cast<uint32_t>(majorB) << 16;         // B: 0 K-major, 1 MN-major
-  d |= static_cast<uint32_t>(gb::kBN >> 3) << 17;   // N / 8
-  d |= static_cast<uint32_t>(gb::kBM >> 4) << 24;   // M / 16
+  d |= static_cast<uint32_t>(majorA) << 15;            // A: 0 K-major, 1 MN-major
+  d |= static_cast<uint32_t>(majorB) << 16;            // B: 0 K-major, 1 MN-major
+  d |= static_cast<uint32_t>(gb::kBN >> 3) << 17;      // N / 8
+  d |= static_cast<uint32_t>(tile_m >> 4) << 24;       // M / 16 (256 for a CTA pair)
   return d;
 }
 
-gb_status make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
-                    int majorB, gb_gemm_plan* pl) {
+int choose_variant(int64_t M) {
+  int forced;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    forced = g_force_variant;
+  }
+  if (forced == kVariantSingle || forced == kVariantPair) return forced;
+  return M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+}
+
+gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
+                    int64_t ldb, int majorB, gb_gemm_plan* pl) {
   gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB);
   if (st != GB_OK) return st;
   if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  if (variant != kVariantSingle && variant != kVariantPair) return GB_ERR_INVALID_ARG;
+  const bool pair = variant == kVariantPair;
+  const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
+  const int64_t rows_b = pair ? gb::Cfg<true>::kRowsB : gb::Cfg<false>::kRowsB;
   std::memset(pl, 0, sizeof(*pl));
-  pl->tile_m = gb::kBM;
+  pl->variant = variant;
+  pl->tile_m = tile_m;
   pl->tile_n = gb::kBN;
   pl->tile_k = gb::kBK;
   if (M == 0 || N == 0) return GB_OK;
   try {
-    // D (and C): (M,N):(N,1) divided into (128,256) tiles -> ((tile),(grid))
+    // D (and C): (M,N):(N,1) divided into (tile_m, 256) tiles -> ((tile),(grid))
     la::Layout mD = la::make_layout({M, N}, {N, 1});
-    la::Layout zD = la::zipped_divide(mD, la::tiler_of({gb::kBM, gb::kBN}));
+    la::Layout zD = la::zipped_divide(mD, la::tiler_of({tile_m, gb::kBN}));
     auto grid_shape = la::flatten(zD.mode(1).shape);
     auto grid_stride = la::flatten(zD.mode(1).stride);
     auto elem_stride = la::flatten(mD.stride);
@@ -634,8 +731,8 @@ gb_status make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int
     pl->vector_epilogue = (pl->d_elem_stride[1] == 1 && N % 8 == 0) ? 1 : 0;
     if (K > 0) {
       OperandPlan a, b;
-      if ((st = plan_operand(M, K, lda, majorA, gb::kBM, &a)) != GB_OK) return st;
-      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, &b)) != GB_OK) return st;
+      if ((st = plan_operand(M, K, lda, majorA, tile_m, gb::kRowsA, &a)) != GB_OK) return st;
+      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, rows_b, &b)) != GB_OK) return st;
       if (a.grid_rows != pl->m_tiles || b.grid_rows != pl->n_tiles || a.k_blocks != b.k_blocks)
         return GB_ERR_INVALID_ARG;
       pl->k_blocks = a.k_blocks;
@@ -655,7 +752,7 @@ gb_status make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int
   } catch (const la::Error&) {
     return GB_ERR_INVALID_ARG;
   }
-  pl->instr_desc = make_idesc(dtype, majorA, majorB);
+  pl->instr_desc = make_idesc(dtype, majorA, majorB, static_cast<int>(tile_m));
   return GB_OK;
 }
 
@@ -693,8 +790,8 @@ gb_status device_state(DeviceState** out) {
   return GB_OK;
 }
 
-gb_status fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float alpha, int majorA,
-                      int majorB, float beta, const void* C, void* D, Params* p) {
+void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float alpha, int majorA,
+                 int majorB, float beta, const void* C, void* D, Params* p) {
   std::memset(p, 0, sizeof(*p));
   p->M = static_cast<int32_t>(M);
   p->N = static_cast<int32_t>(N);
@@ -703,7 +800,7 @@ gb_status fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, f
   p->n_tiles = static_cast<int32_t>(pl.n_tiles);
   p->k_blocks = static_cast<int32_t>(pl.k_blocks);
   p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);
-  p->group_m = 16;
+  p->group_m = pl.variant == kVariantPair ? 8 : 16;
   p->majorA = majorA;
   p->majorB = majorB;
   p->alpha = alpha;
@@ -717,19 +814,66 @@ gb_status fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, f
   p->idesc = pl.instr_desc;
   p->vec_ok = pl.vector_epilogue;
   p->has_c = beta != 0.0f ? 1 : 0;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    p->timeout_ns = g_timeout_ns;
-    p->skip_kb = g_skip_kb;
+  std::lock_guard<std::mutex> lk(g_mu);
+  p->timeout_ns = g_timeout_ns;
+  p->skip_kb = g_skip_kb;
+}
+
+template <bool kBF16>
+gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+                        cudaStream_t s) {
+  using C = gb::Cfg<false>;
+  if (!dev->attr_single[kBF16]) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return GB_ERR_LAUNCH;
+    dev->attr_single[kBF16] = true;
   }
-  return GB_OK;
+  const int grid = std::min(p.num_tiles, dev->sms);
+  gb::gemm_kernel<kBF16, false><<<grid, gb::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+template <bool kBF16>
+gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+                      cudaStream_t s) {
+  using C = gb::Cfg<true>;
+  if (!dev->attr_pair[kBF16]) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return GB_ERR_LAUNCH;
+    dev->attr_pair[kBF16] = true;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(gb::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (dev->pair_clusters == 0) {
+    // a persistent grid must fit at once: ask how many pairs can be resident together
+    int n = 0;
+    cfg.gridDim = dim3(2 * (dev->sms / 2), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true>, &cfg) != cudaSuccess || n <= 0)
+      n = dev->sms / 2;
+    dev->pair_clusters = std::min(n, dev->sms / 2);
+  }
+  const int clusters = std::min(p.num_tiles, dev->pair_clusters);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true>, tmA, tmB, p) != cudaSuccess) return GB_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
                      void* stream) {
   gb_gemm_plan pl;
-  gb_status st = make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, &pl);
+  gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl);
   if (st != GB_OK) return st;
   if (M == 0 || N == 0) return GB_OK;
   if (D == nullptr) return GB_ERR_INVALID_ARG;
@@ -749,26 +893,10 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
-  const int grid = static_cast<int>(std::min<int64_t>(p.num_tiles, dev->sms));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == GB_BF16) {
-    if (!dev->smem_attr[1]) {
-      if (cudaFuncSetAttribute(gb::gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               gb::kSmemBytes) != cudaSuccess)
-        return GB_ERR_LAUNCH;
-      dev->smem_attr[1] = true;
-    }
-    gb::gemm_kernel<true><<<grid, gb::kThreads, gb::kSmemBytes, s>>>(tmA, tmB, p);
-  } else {
-    if (!dev->smem_attr[0]) {
-      if (cudaFuncSetAttribute(gb::gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               gb::kSmemBytes) != cudaSuccess)
-        return GB_ERR_LAUNCH;
-      dev->smem_attr[0] = true;
-    }
-    gb::gemm_kernel<false><<<grid, gb::kThreads, gb::kSmemBytes, s>>>(tmA, tmB, p);
-  }
-  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+  if (pl.variant == kVariantPair)
+    return dtype == GB_BF16 ? launch_pair<true>(dev, tmA, tmB, p, s) : launch_pair<false>(dev, tmA, tmB, p, s);
+  return dtype == GB_BF16 ? launch_single<true>(dev, tmA, tmB, p, s) : launch_single<false>(dev, tmA, tmB, p, s);
 }
 
 }  // namespace
@@ -812,7 +940,8 @@ const char* gb_status_string(int status) {
 gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
                             int majorB, gb_gemm_plan* plan) {
   if (!plan) return GB_ERR_INVALID_ARG;
-  return make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, plan);
+  if (M < 0) return GB_ERR_INVALID_ARG;
+  return make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, plan);
 }
 
 gb_status gb_set_wait_timeout_ns(uint64_t ns) {
@@ -827,10 +956,17 @@ gb_status gb_debug_skip_k_block(int64_t k_block) {
   return GB_OK;
 }
 
-gb_status gb_debug_epilogue_map(int64_t M, int64_t N, int64_t m_tile, int64_t n_tile, int64_t* out,
+gb_status gb_set_kernel_variant(int variant) {
+  if (variant != 0 && variant != kVariantSingle && variant != kVariantPair) return GB_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_force_variant = variant;
+  return GB_OK;
+}
+
+gb_status gb_debug_epilogue_map(int variant, int64_t M, int64_t N, int64_t m_tile, int64_t n_tile, int64_t* out,
                                 void* stream) {
   gb_gemm_plan pl;
-  gb_status st = make_plan(GB_F16, M, N, 0, 0, GB_K_MAJOR, 0, GB_K_MAJOR, &pl);
+  gb_status st = make_plan(GB_F16, variant, M, N, 0, 0, GB_K_MAJOR, 0, GB_K_MAJOR, &pl);
   if (st != GB_OK) return st;
   if (M == 0 || N == 0 || !out || m_tile < 0 || n_tile < 0 || m_tile >= pl.m_tiles || n_tile >= pl.n_tiles)
     return GB_ERR_INVALID_ARG;
@@ -838,8 +974,9 @@ gb_status gb_debug_epilogue_map(int64_t M, int64_t N, int64_t m_tile, int64_t n_
   if ((st = device_state(&dev)) != GB_OK) return st;
   Params p;
   fill_params(pl, M, N, 0, 1.0f, 0, 0, 0.0f, nullptr, nullptr, &p);
-  gb::epilogue_map_kernel<<<(gb::kBM * gb::kBN) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      p, static_cast<int32_t>(m_tile), static_cast<int32_t>(n_tile), out);
+  const int n = static_cast<int>(pl.tile_m) * gb::kBN;
+  gb::epilogue_map_kernel<<<n / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      p, static_cast<int32_t>(pl.tile_m), static_cast<int32_t>(m_tile), static_cast<int32_t>(n_tile), out);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
@@ -847,7 +984,7 @@ gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64
                                int64_t lda, int majorA, const void* B, int64_t ldb, int majorB, int64_t tile,
                                int64_t k_block, void* out, void* stream) {
   gb_gemm_plan pl;
-  gb_status st = make_plan(dtype, M, N, K, lda, majorA, ldb, majorB, &pl);
+  gb_status st = make_plan(dtype, kVariantSingle, M, N, K, lda, majorA, ldb, majorB, &pl);
   if (st != GB_OK) return st;
   if (M == 0 || N == 0 || K == 0 || !out || (which != 0 && which != 1)) return GB_ERR_INVALID_ARG;
   const void* base = which == 0 ? A : B;
@@ -862,7 +999,7 @@ gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64
   if (st != GB_OK) return st;
   Params p;
   fill_params(pl, M, N, K, 1.0f, majorA, majorB, 0.0f, nullptr, nullptr, &p);
-  const int smem = 1024 + gb::kStageBytes + gb::kCtlBytes;
+  const int smem = 1024 + gb::Cfg<false>::kStageBytes + gb::kCtlBytes;
   if (!dev->dbg_attr) {
     if (cudaFuncSetAttribute(gb::stage_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)

@@ -37,20 +37,31 @@ def test_status_strings():
     assert "10.3" in G.status_string(3)
 
 
-@pytest.mark.parametrize("name,M,N,K,majors,grid", [
-    ("gemm256_int_f16", 256, 256, 256, ("K", "K"), (2, 1, 4)),
-    ("gemm4096_f16", 4096, 4096, 4096, ("K", "K"), (32, 16, 64)),
-    ("gemm8192_bf16_c", 8192, 8192, 8192, ("K", "K"), (64, 32, 128)),
-    ("gemm16384x1024x4096_mnmajor_f16", 16384, 1024, 4096, ("MN", "MN"), (128, 4, 64)),
-    ("gemm5000x3000x4104_ragged_f16", 5000, 3000, 4104, ("K", "K"), (40, 12, 65)),
+@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+def variant(request):
+    G.set_kernel_variant(request.param)
+    yield request.param
+    G.set_kernel_variant(0)
+
+
+@pytest.mark.parametrize("name,M,N,K,majors,grid1,grid2", [
+    ("gemm256_int_f16", 256, 256, 256, ("K", "K"), (2, 1, 4), (1, 1, 4)),
+    ("gemm4096_f16", 4096, 4096, 4096, ("K", "K"), (32, 16, 64), (16, 16, 64)),
+    ("gemm8192_bf16_c", 8192, 8192, 8192, ("K", "K"), (64, 32, 128), (32, 32, 128)),
+    ("gemm16384x1024x4096_mnmajor_f16", 16384, 1024, 4096, ("MN", "MN"), (128, 4, 64), (64, 4, 64)),
+    ("gemm5000x3000x4104_ragged_f16", 5000, 3000, 4104, ("K", "K"), (40, 12, 65), (20, 12, 65)),
 ])
-def test_plans_of_the_workloads(name, M, N, K, majors, grid):
+def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     lda = K if majors[0] == "K" else M
     ldb = K if majors[1] == "K" else N
     p = G.plan("f16", M, N, K, lda, majors[0], ldb, majors[1])
+    grid = grid1 if variant == 1 else grid2
+    tile_m = 128 if variant == 1 else 256
+    rows_b = 256 if variant == 1 else 128        # B rows staged per CTA
+    assert p["variant"] == variant and p["tile_m"] == tile_m
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
     # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
-    for i, (ext, want) in enumerate(zip(grid[:2], [128 * N, 256])):
+    for i, (ext, want) in enumerate(zip(grid[:2], [tile_m * N, 256])):
         if ext > 1:
             assert p["d_grid_stride"][i] == want
     assert p["d_elem_stride"] == [N, 1]
@@ -60,22 +71,30 @@ def test_plans_of_the_workloads(name, M, N, K, majors, grid):
     else:
         assert p["a_dim"] == [M, K] and p["a_box"] == [64, 64] and p["a_boxes"] == 2
     if majors[1] == "K":
-        assert p["b_dim"] == [K, N] and p["b_box"] == [64, 256] and p["b_boxes"] == 1
+        assert p["b_dim"] == [K, N] and p["b_box"] == [64, rows_b] and p["b_boxes"] == 1
     else:
-        assert p["b_dim"] == [N, K] and p["b_box"] == [64, 64] and p["b_boxes"] == 4
+        assert p["b_dim"] == [N, K] and p["b_box"] == [64, 64] and p["b_boxes"] == rows_b // 64
     # instruction descriptor: fp32 accumulate, fp16 inputs, majors, N/8, M/16
     d = p["instr_desc"]
     assert (d >> 4) & 3 == 1 and (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0
     assert (d >> 15) & 1 == (majors[0] == "MN") and (d >> 16) & 1 == (majors[1] == "MN")
-    assert (d >> 17) & 63 == 256 >> 3 and (d >> 24) & 31 == 128 >> 4
+    assert (d >> 17) & 63 == 256 >> 3 and (d >> 24) & 31 == tile_m >> 4
     assert p["vector_epilogue"] == 1
 
 
-def test_plan_bf16_descriptor_and_scalar_epilogue():
+def test_variant_choice_by_shape():
+    G.set_kernel_variant(0)
+    assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 1
+    assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 2
+    with pytest.raises(G.GemmError):
+        G.set_kernel_variant(3)
+
+
+def test_plan_bf16_descriptor_and_scalar_epilogue(variant):
     p = G.plan("bf16", 129, 77, 40, 40, "K", 40, "K")
     assert (p["instr_desc"] >> 7) & 7 == 1 and (p["instr_desc"] >> 10) & 7 == 1
     assert p["vector_epilogue"] == 0          # rows of 77 elements are not 16-byte aligned
-    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (2, 1, 1)
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == ((2, 1, 1) if variant == 1 else (1, 1, 1))
 
 
 @pytest.mark.parametrize("args,status", [

@@ -19,6 +19,14 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
+@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+def variant(request):
+    """Run a test with the single-CTA kernel and with the CTA-pair kernel."""
+    G.set_kernel_variant(request.param)
+    yield request.param
+    G.set_kernel_variant(0)
+
+
 def code(p):
     return O.dtype_code(p.dtype)
 
@@ -113,7 +121,7 @@ def test_ragged_workload_full_compare():
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("majors", [("K", "K"), ("MN", "MN"), ("K", "MN"), ("MN", "K")])
-def test_multi_tile_ragged_all_majors(dtype, majors):
+def test_multi_tile_ragged_all_majors(variant, dtype, majors):
     M, N, K = 300, 520, 200        # 3 x 3 tiles, tails of 44 rows / 8 columns, 4 k-blocks
     lda = K if majors[0] == "K" else 304
     p = W.Problem("mt", M, N, K, dtype, majorA=majors[0], majorB=majors[1], has_c=True,
@@ -123,7 +131,7 @@ def test_multi_tile_ragged_all_majors(dtype, majors):
 
 
 @pytest.mark.parametrize("majors", [("K", "K"), ("MN", "MN"), ("MN", "K"), ("K", "MN")])
-def test_integer_ragged_exact(majors):
+def test_integer_ragged_exact(variant, majors):
     M, N, K = 129, 77, 40
     lda = K if majors[0] == "K" else 136
     ldb = K if majors[1] == "K" else 80
@@ -135,7 +143,7 @@ def test_integer_ragged_exact(majors):
 
 @pytest.mark.parametrize("shape", [(1, 8, 8), (1, 1, 1), (7, 3, 5), (128, 256, 64),
                                    (129, 257, 65), (256, 512, 1000), (8, 2000, 16)])
-def test_small_and_boundary_shapes(shape):
+def test_small_and_boundary_shapes(variant, shape):
     M, N, K = shape
     lda = -(-K // 8) * 8
     ldb = -(-K // 8) * 8
@@ -151,7 +159,7 @@ def test_long_k():
     check(p, data, run(p, data))
 
 
-def test_k_zero_gives_beta_c():
+def test_k_zero_gives_beta_c(variant):
     p = W.Problem("k0", 200, 264, 0, "f16", has_c=True, alpha=2.0, beta=0.5,
                   c_dist="uniform", seed=61)
     data = W.make(p)
@@ -163,7 +171,7 @@ def test_k_zero_gives_beta_c():
     check(p, data, D, exact=True)          # 0.5 * c is exact
 
 
-def test_alpha_zero_and_beta_zero():
+def test_alpha_zero_and_beta_zero(variant):
     p = W.Problem("a0", 130, 260, 70, "bf16", has_c=True, alpha=0.0, beta=1.5,
                   dist="normal", c_dist="normal", seed=62, lda=72, ldb=72)
     data = W.make(p)
@@ -185,7 +193,7 @@ def test_empty_problem_writes_nothing():
     assert torch.all(D == 7.0)
 
 
-def test_canary_outside_d_untouched():
+def test_canary_outside_d_untouched(variant):
     p = W.Problem("can", 200, 300, 64, "f16", dist="uniform", seed=64)
     data = W.make(p)
     D = torch.full((p.M * p.N + 4096,), -3.0, dtype=torch.float16, device=DEV)
@@ -230,7 +238,7 @@ def test_device_misalignment_rejected():
 # --------------------------------------------------------------------------- failure path
 
 
-def test_wait_timeout_is_reported_and_context_survives():
+def test_wait_timeout_is_reported_and_context_survives(variant):
     p = W.Problem("to", 256, 256, 512, "f16", dist="int2", seed=71)
     data = W.make(p)
     G.set_wait_timeout_ns(50_000_000)
@@ -251,23 +259,25 @@ def test_wait_timeout_is_reported_and_context_survives():
 # --------------------------------------------------------------------------- device-side maps
 
 
-@pytest.mark.parametrize("M,N,tile", [(5000, 3000, (39, 11)), (5000, 3000, (0, 0)),
-                                      (256, 128, (1, 0)), (8192, 8192, (17, 30))])
-def test_epilogue_map_matches_host_layout(M, N, tile):
+@pytest.mark.parametrize("var", [1, 2])
+@pytest.mark.parametrize("M,N,tile", [(5000, 3000, (19, 11)), (5000, 3000, (0, 0)),
+                                      (256, 128, (0, 0)), (8192, 8192, (17, 30))])
+def test_epilogue_map_matches_host_layout(var, M, N, tile):
     """The device evaluation of the C/D tile map equals the host layout library's."""
-    out = torch.empty(128 * 256, dtype=torch.int64, device=DEV)
+    tm = 128 if var == 1 else 256
+    out = torch.empty(tm * 256, dtype=torch.int64, device=DEV)
     st = __import__("layout_algebra_gb300._native", fromlist=["lib"]).lib().gb_debug_epilogue_map(
-        M, N, tile[0], tile[1], out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        var, M, N, tile[0], tile[1], out.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == 0
-    got = out.cpu().numpy().reshape(128, 256)
-    origin, tl = L.local_tile("(%d,%d):(%d,1)" % (M, N, N), "(128,256)", list(tile))
-    rr, cc = np.meshgrid(np.arange(128), np.arange(256), indexing="ij")
-    idx = (rr + 128 * cc).ravel()                    # colexicographic index of (r, c)
-    want = (origin + L.evaluate(tl, idx)).reshape(128, 256)
-    inside = ((tile[0] * 128 + rr) < M) & ((tile[1] * 256 + cc) < N)
+    got = out.cpu().numpy().reshape(tm, 256)
+    origin, tl = L.local_tile("(%d,%d):(%d,1)" % (M, N, N), "(%d,256)" % tm, list(tile))
+    rr, cc = np.meshgrid(np.arange(tm), np.arange(256), indexing="ij")
+    idx = (rr + tm * cc).ravel()                     # colexicographic index of (r, c)
+    want = (origin + L.evaluate(tl, idx)).reshape(tm, 256)
+    inside = ((tile[0] * tm + rr) < M) & ((tile[1] * 256 + cc) < N)
     want = np.where(inside, want, -1)
     assert np.array_equal(got, want)
-    assert np.array_equal(got[inside], ((tile[0] * 128 + rr) * N + tile[1] * 256 + cc)[inside])
+    assert np.array_equal(got[inside], ((tile[0] * tm + rr) * N + tile[1] * 256 + cc)[inside])
 
 
 def _swizzle_offset(row, byte_in_row):
