@@ -136,14 +136,17 @@ __device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) {
     return mbar_try_wait(bar, parity);
 }
 
-// Single-thread bounded wait; gives up on the abort flag or the time limit.
-template <bool kPair>
+// Single-thread bounded wait; gives up on the abort flag or the time limit.  kCluster
+// selects a cluster-scope acquire: needed only where the arrivals are plain thread
+// arrivals from the peer CTA; barriers completed by copies or tcgen05.commit are
+// waited at CTA scope.
+template <bool kPair, bool kCluster = false>
 __device__ __noinline__ bool wait_one(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
                                       uint32_t site) {
-  if (probe<kPair>(bar, parity)) return true;
+  if (probe<kCluster>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 1;; ++n) {
-    if (probe<kPair>(bar, parity)) return true;
+    if (probe<kCluster>(bar, parity)) return true;
     if ((n & 7) == 0) {
       if (aborted(ctl)) return false;
       if (global_timer_ns() - t0 > limit) {
@@ -172,7 +175,7 @@ __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, 
                                        uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t n = 0;; ++n) {
-    const bool ok = probe<kPair>(bar, parity);
+    const bool ok = probe<false>(bar, parity);
     if (__all_sync(0xffffffffu, ok)) return true;
     if ((n & 7) == 7) {
       int stop = 0;
@@ -310,7 +313,8 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
   for (int32_t t = cluster; ok && t < p.num_tiles; t += nclusters, ++it) {
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
-    if (!wait_one<kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns, kSiteAccEmpty)) {
+    if (!wait_one<kPair, kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns,
+                                kSiteAccEmpty)) {
       ok = false;
       break;
     }
