@@ -59,18 +59,24 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 // Two variants share all code:
 //  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64;
 //  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x 256 tile; each CTA
-//         stages its own 128 A rows and 128 of the 256 B rows (6 stages of 32 KiB), the even
+//         stages its own 128 A rows and 128 of the 256 B rows, two 64-wide k-blocks per
+//         stage (3 stages of 64 KiB: every stage carries a fixed cost in the copy engine
+//         and the barrier hand-off, so fewer, larger stages feed the pair faster), the even
 //         CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory,
 //         and each CTA's TMEM holds its own 128 rows of the accumulator.
 template <bool kPair>
 struct Cfg {
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kRowsB = kPair ? 128 : 256;
-  static constexpr int kStages = kPair ? 6 : 4;
-  static constexpr int kAStage = kRowsA * kBK * 2;
-  static constexpr int kBStage = kRowsB * kBK * 2;
+  static constexpr int kStages = kPair ? 3 : 4;
+  static constexpr int kKB = kPair ? 2 : 1;               // 64-wide k-blocks per stage
+  static constexpr int kAHalf = kRowsA * kBK * 2;          // one k-block of A (bytes)
+  static constexpr int kBHalf = kRowsB * kBK * 2;          // one k-block of B (bytes)
+  static constexpr int kAStage = kAHalf * kKB;
+  static constexpr int kBStage = kBHalf * kKB;
   static constexpr int kStageBytes = kAStage + kBStage;
-  static constexpr uint32_t kTxBytes = kStageBytes * (kPair ? 2 : 1);   // bytes per full barrier
+  // bytes one k-block adds to the (even CTA's) full barrier: both CTAs' copies in a pair
+  static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf) * (kPair ? 2 : 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static constexpr uint32_t kAccEmptyArrivals = 4 * (kPair ? 2 : 1);   // epilogue warps
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
@@ -256,7 +262,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
     tile_coords(p, t, mt, nt);
     const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(rank) * kRowsA;
     const int32_t b_row0 = nt * kBN + static_cast<int32_t>(rank) * C::kRowsB;
-    for (int32_t kb = 0; kb < p.k_blocks; ++kb, ++gkb) {
+    for (int32_t sb = 0; sb * C::kKB < p.k_blocks; ++sb, ++gkb) {
       if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
         ok = false;
         break;
@@ -266,9 +272,15 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         // in a pair both CTAs' copies are counted on the even CTA's barrier
         const uint32_t full_tgt = kPair ? map_to_cta(full, 0) : full;
         const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
-        if (!kPair || rank == 0) mbar_arrive_expect_tx(full, C::kTxBytes);
-        issue_operand<kPair>(p.majorA, tmA, sa, full_tgt, a_row0, kRowsA, kb);
-        issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage, full_tgt, b_row0, C::kRowsB, kb);
+        // the last stage of a tile may hold fewer k-blocks: copy and count only those
+        const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
+        if (!kPair || rank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
+        for (int h = 0; h < nkb; ++h) {
+          const int32_t kb = sb * C::kKB + h;
+          issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb);
+          issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf, full_tgt, b_row0,
+                               C::kRowsB, kb);
+        }
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       } else {
@@ -296,7 +308,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         wait_drain(smem_addr(&ctl->full[s]), (issued_parity >> s) & 1u, p.timeout_ns);
   } else {
     // the odd CTA's copies complete on the even CTA's barrier, which it cannot observe;
-    // a copy of 32 KiB lands in microseconds
+    // a stage of 64 KiB lands in microseconds
     __nanosleep(200000);
   }
 }
@@ -320,7 +332,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + buf * kBN;
-    for (int32_t kb = 0; kb < p.k_blocks; ++kb) {
+    for (int32_t sbk = 0; sbk * C::kKB < p.k_blocks; ++sbk) {
       if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
         ok = false;
         break;
@@ -328,14 +340,18 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       tc_fence_after_sync();
       const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
       const uint32_t sb = sa + C::kAStage;
+      const int nkb = min(C::kKB, p.k_blocks - sbk * C::kKB);
+      for (int h = 0; h < nkb; ++h) {
 #pragma unroll
-      for (int k = 0; k < kBK / kUmmaK; ++k) {
-        const uint64_t da = operand_desc(sa, p.majorA, k), db = operand_desc(sb, p.majorB, k);
-        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
-        if constexpr (kPair)
-          tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
-        else
-          tc_mma_f16(d_tmem, da, db, p.idesc, acc);
+        for (int k = 0; k < kBK / kUmmaK; ++k) {
+          const uint64_t da = operand_desc(sa + h * C::kAHalf, p.majorA, k);
+          const uint64_t db = operand_desc(sb + h * C::kBHalf, p.majorB, k);
+          const uint32_t acc = (sbk | h | k) != 0 ? 1u : 0u;
+          if constexpr (kPair)
+            tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
+          else
+            tc_mma_f16(d_tmem, da, db, p.idesc, acc);
+        }
       }
       issued_any = true;
       if constexpr (kPair)
