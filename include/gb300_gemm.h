@@ -73,6 +73,36 @@ gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
                        const void* B, int64_t ldb, int majorB,
                        float beta, const void* C, void* D, void* stream);
 
+/* The same GEMM with a caller-owned scratch workspace, which lets the kernel split the
+   K loop of some tiles across CTAs ("stream-K", after "CUTLASS, in depth" — "Kernel
+   schedules": split-K and stream-K divide K across CTAs when output tiles are too few to
+   fill the GPU, at the cost of a reduction and a workspace).  Each CTA first runs whole
+   tiles, then an even contiguous share of the remaining (tile, k-block) units; the CTA that
+   holds a tile's first k-units adds the other CTAs' fp32 partials before the epilogue.
+   workspace: device memory of at least gb_gemm_workspace_bytes() bytes, 256-byte aligned,
+   zero-filled before its first use and not shared by calls that may run at the same time
+   (it is reused as is by later calls; each launch tags its hand-offs with a new number).
+   Results equal the plain call's within the same bound; summation order differs. */
+gb_status gb_gemm_f16_ws(int64_t M, int64_t N, int64_t K, float alpha,
+                         const void* A, int64_t lda, int majorA,
+                         const void* B, int64_t ldb, int majorB,
+                         float beta, const void* C, void* D,
+                         void* workspace, size_t workspace_bytes, void* stream);
+gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha,
+                          const void* A, int64_t lda, int majorA,
+                          const void* B, int64_t ldb, int majorB,
+                          float beta, const void* C, void* D,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace size for the *_ws calls on the current device (one 128 x 256 fp32 partial and
+   one flag per SM).  GB_ERR_UNSUPPORTED_ARCH without a compute capability 10.3 device. */
+gb_status gb_gemm_workspace_bytes(size_t* bytes);
+
+/* Schedule for later *_ws calls (process-wide): 0 stream-K when the output tiles leave a
+   ragged last wave or are fewer than the CTAs (the default), 1 whole tiles only, 2 stream-K
+   whenever K > 0.  GB_ERR_INVALID_ARG for other values. */
+gb_status gb_set_schedule(int schedule);
+
 /* Synchronises `stream`, then returns GB_ERR_TIMEOUT if any kernel of this library on the
    current device recorded a wait that ran out since the last call (the raw code goes to
    *detail when detail != NULL: bits 0-7 the wait that ran out, bits 8-31 the CTA), and

@@ -13,6 +13,7 @@ GEMM_SYMBOLS = [
     "gb_gemm_f16", "gb_gemm_bf16", "gb_last_device_status", "gb_status_string",
     "gb_gemm_make_plan", "gb_set_wait_timeout_ns", "gb_debug_skip_k_block",
     "gb_debug_epilogue_map", "gb_debug_stage_bytes", "gb_set_kernel_variant",
+    "gb_gemm_f16_ws", "gb_gemm_bf16_ws", "gb_gemm_workspace_bytes", "gb_set_schedule",
 ]
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
@@ -56,6 +57,14 @@ def lib():
         fn = getattr(L, name)
         fn.restype = ci
         fn.argtypes = [i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp]
+    for name in ("gb_gemm_f16_ws", "gb_gemm_bf16_ws"):
+        fn = getattr(L, name)
+        fn.restype = ci
+        fn.argtypes = [i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp, sz, vp]
+    L.gb_gemm_workspace_bytes.restype = ci
+    L.gb_gemm_workspace_bytes.argtypes = [ctypes.POINTER(sz)]
+    L.gb_set_schedule.restype = ci
+    L.gb_set_schedule.argtypes = [ci]
     L.gb_last_device_status.restype = ci
     L.gb_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.gb_status_string.restype = cp

@@ -53,7 +53,7 @@ def _stream_handle(stream):
 
 
 def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0, C=None,
-         D=None, stream=None):
+         D=None, stream=None, workspace=None):
     """D = alpha * A @ B + beta * C.  Returns D (M*N elements, row-major).
 
     A, B, C are flat (or any contiguous) tensors of one dtype.  Device tensors: D is
@@ -73,9 +73,15 @@ def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0
     else:
         A_d, B_d, C_d = A, B, C
         D_d = D if D is not None else torch.empty(M * N, dtype=A.dtype, device=A.device)
-    fn = lib().gb_gemm_bf16 if dt == BF16 else lib().gb_gemm_f16
-    st = fn(M, N, K, float(alpha), _ptr(A_d), lda, major_code(majorA), _ptr(B_d), ldb,
-            major_code(majorB), float(beta), _ptr(C_d), _ptr(D_d), _stream_handle(stream))
+    if workspace is None:
+        fn = lib().gb_gemm_bf16 if dt == BF16 else lib().gb_gemm_f16
+        st = fn(M, N, K, float(alpha), _ptr(A_d), lda, major_code(majorA), _ptr(B_d), ldb,
+                major_code(majorB), float(beta), _ptr(C_d), _ptr(D_d), _stream_handle(stream))
+    else:
+        fn = lib().gb_gemm_bf16_ws if dt == BF16 else lib().gb_gemm_f16_ws
+        st = fn(M, N, K, float(alpha), _ptr(A_d), lda, major_code(majorA), _ptr(B_d), ldb,
+                major_code(majorB), float(beta), _ptr(C_d), _ptr(D_d), workspace.data_ptr(),
+                workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if st != 0:
         raise GemmError(st)
     if host:
@@ -121,6 +127,28 @@ def set_wait_timeout_ns(ns):
 
 def debug_skip_k_block(kb):
     lib().gb_debug_skip_k_block(int(kb))
+
+
+def workspace_bytes():
+    """Bytes of scratch the *_ws calls need on the current device."""
+    n = ctypes.c_size_t()
+    st = lib().gb_gemm_workspace_bytes(ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "workspace_bytes")
+    return n.value
+
+
+def make_workspace(device=None):
+    """A zero-filled workspace for the *_ws calls (allocated once by the caller)."""
+    return torch.zeros(workspace_bytes(), dtype=torch.uint8,
+                       device=device if device is not None else torch.device("cuda"))
+
+
+def set_schedule(schedule):
+    """0: stream-K for ragged last waves (default); 1: whole tiles only; 2: stream-K always."""
+    st = lib().gb_set_schedule(int(schedule))
+    if st != 0:
+        raise GemmError(st, "set_schedule")
 
 
 def set_kernel_variant(variant):

@@ -98,7 +98,17 @@ struct Params {
   int32_t vec_ok, has_c;
   uint64_t timeout_ns;
   int64_t skip_kb;
+  // stream-K schedule: each CTA (pair) first runs data-parallel tiles t = c, c + G, ... <
+  // dp_tiles, then an even, contiguous share of the remaining (tile, stage-block) units.
+  int32_t nsb;                // stage-blocks per tile
+  int32_t dp_tiles;           // tiles run whole; == num_tiles when stream-K is off
+  uint32_t epoch;             // launch number, written to the partial-ready flags
+  float* ws_part;             // per CTA slot: one 128 x 256 fp32 partial accumulator
+  uint32_t* ws_flags;         // per CTA slot: epoch of the last partial written
 };
+
+// Slot of CTA (cluster c, rank r) in the stream-K workspace.
+constexpr int kSlotFloats = 128 * 256;
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -106,6 +116,7 @@ struct Ctl {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
+  uint64_t part_done;         // epilogue warps finished writing a stream-K partial
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -118,6 +129,7 @@ enum : uint32_t {
   kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
   kSiteDrain = 5,     // abort path: waiting for own operations in flight
   kSiteTail = 6,      // copy stage waiting for the last releases before exit
+  kSiteFixup = 7,     // tile owner waiting for another CTA's stream-K partial
 };
 
 __device__ uint32_t g_status;
@@ -211,6 +223,56 @@ __device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t&
   nt = local / gm;
 }
 
+// One unit of work: stage-blocks [sb0, sb1) of tile `tile`.
+struct Item {
+  int32_t tile, sb0, sb1;
+};
+
+// The work list of one CTA (or pair), walked identically by the copy, MMA and epilogue
+// roles.  Stream-K part: the U = (num_tiles - dp_tiles) * nsb remaining units are cut
+// into G contiguous ranges [c*U/G, (c+1)*U/G); an item never crosses a tile boundary.
+struct Sched {
+  int32_t dp_next;
+  int64_t u, u_end;
+  __device__ __forceinline__ void init(const Params& p, uint32_t c, uint32_t G) {
+    dp_next = static_cast<int32_t>(c);
+    const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+    u = U * c / G;
+    u_end = U * (c + 1) / G;
+  }
+  __device__ __forceinline__ bool next(const Params& p, uint32_t G, Item& it) {
+    if (dp_next < p.dp_tiles) {
+      it.tile = dp_next;
+      it.sb0 = 0;
+      it.sb1 = p.nsb;
+      dp_next += static_cast<int32_t>(G);
+      return true;
+    }
+    if (u >= u_end) return false;
+    const int64_t gu = static_cast<int64_t>(p.dp_tiles) * p.nsb + u;
+    it.tile = static_cast<int32_t>(gu / p.nsb);
+    it.sb0 = static_cast<int32_t>(gu % p.nsb);
+    const int64_t span = u_end - u, room = p.nsb - it.sb0;
+    it.sb1 = it.sb0 + static_cast<int32_t>(span < room ? span : room);
+    u += it.sb1 - it.sb0;
+    return true;
+  }
+};
+
+// The CTA (pair) whose stream-K range holds unit index `gu` (counted over all tiles).
+__device__ __forceinline__ uint32_t sk_owner_of(const Params& p, uint32_t G, int64_t gu) {
+  const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+  const int64_t v = gu - static_cast<int64_t>(p.dp_tiles) * p.nsb;
+  return static_cast<uint32_t>(((v + 1) * G + U - 1) / U - 1);
+}
+
+// True when CTA (pair) c's stream-K range holds at least one unit (with fewer units than
+// CTAs some ranges are empty, and those CTAs hand nothing over).
+__device__ __forceinline__ bool sk_has_units(const Params& p, uint32_t G, uint32_t c) {
+  const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+  return U * (c + 1) / G > U * c / G;
+}
+
 // C/D offset of in-tile element (r, c) of tile (mt, nt): the divided layout evaluated.
 __device__ __forceinline__ int64_t d_offset(const Params& p, int32_t mt, int32_t nt, int32_t r,
                                             int32_t c) {
@@ -257,12 +319,15 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   int64_t gkb = 0;
   uint32_t issued = 0, issued_parity = 0;
   bool ok = true;
-  for (int32_t t = cluster; ok && t < p.num_tiles; t += nclusters) {
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  while (ok && sched.next(p, nclusters, item)) {
     int32_t mt, nt;
-    tile_coords(p, t, mt, nt);
+    tile_coords(p, item.tile, mt, nt);
     const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(rank) * kRowsA;
     const int32_t b_row0 = nt * kBN + static_cast<int32_t>(rank) * C::kRowsB;
-    for (int32_t sb = 0; sb * C::kKB < p.k_blocks; ++sb, ++gkb) {
+    for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
       if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
         ok = false;
         break;
@@ -322,7 +387,10 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
   uint32_t phase = 0;
   bool ok = true, issued_any = false;
   int32_t it = 0;
-  for (int32_t t = cluster; ok && t < p.num_tiles; t += nclusters, ++it) {
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  for (; ok && sched.next(p, nclusters, item); ++it) {
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
     if (!wait_one<kPair, kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns,
@@ -332,7 +400,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + buf * kBN;
-    for (int32_t sbk = 0; sbk * C::kKB < p.k_blocks; ++sbk) {
+    for (int32_t sbk = item.sb0; sbk < item.sb1; ++sbk) {
       if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
         ok = false;
         break;
@@ -346,7 +414,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
         for (int k = 0; k < kBK / kUmmaK; ++k) {
           const uint64_t da = operand_desc(sa + h * C::kAHalf, p.majorA, k);
           const uint64_t db = operand_desc(sb + h * C::kBHalf, p.majorB, k);
-          const uint32_t acc = (sbk | h | k) != 0 ? 1u : 0u;
+          const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
           if constexpr (kPair)
             tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
           else
@@ -454,20 +522,79 @@ __device__ __forceinline__ void store_run(const Params& p, int64_t off, const ui
   }
 }
 
+// Stream-K workspace slot of CTA (cluster c, rank r): a 128 x 256 fp32 partial stored
+// column-major ([column][row]) so that a warp's 32 rows form one 128-byte access.
+template <bool kPair>
+__device__ __forceinline__ float* part_slot(const Params& p, uint32_t c, uint32_t rank) {
+  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * kSlotFloats;
+}
+
+template <bool kPair>
+__device__ __forceinline__ uint32_t* part_flag(const Params& p, uint32_t c, uint32_t rank) {
+  return p.ws_flags + static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank;
+}
+
+// Warp-collective bounded wait until a partial-ready flag carries this launch's epoch.
+template <bool kPair>
+__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl* ctl, uint64_t limit) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+      if (ld_acquire_gpu(flag) == epoch) {
+        ok = 1;
+        break;
+      }
+      if ((n & 63) == 63) {
+        if (aborted(ctl)) break;
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > limit) {
+          raise_status<kPair>(ctl, kSiteFixup);
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(flag);   // every lane acquires before reading the partial
+  return ok != 0;
+}
+
 template <bool kBF16, bool kPair>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair>;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
-  const int r = static_cast<int>(rank) * kRowsA + q * 32 + lane;   // row within the tile
+  const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
+  const int r = static_cast<int>(rank) * kRowsA + lrow;   // row within the tile
   int32_t it = 0;
-  for (int32_t t = cluster; t < p.num_tiles; t += nclusters, ++it) {
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  for (; sched.next(p, nclusters, item); ++it) {
     int32_t mt, nt;
-    tile_coords(p, t, mt, nt);
+    tile_coords(p, item.tile, mt, nt);
     const int buf = it & 1;
     const uint32_t use = (it >> 1) & 1;
     if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
     tc_fence_after_sync();
+    // stream-K roles: a contributor holds later k-units of a tile and hands its partial
+    // over; the owner (which holds k = 0) adds every contributor's partial.
+    const bool contributor = item.sb0 > 0;
+    const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
+    uint32_t c_lo = 1, c_hi = 0;
+    if (owner_with_parts) {
+      c_lo = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile) * p.nsb + item.sb1);
+      c_hi = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile + 1) * p.nsb - 1);
+      bool ok = true;
+      for (uint32_t c = c_lo; ok && c <= c_hi; ++c)
+        if (sk_has_units(p, nclusters, c))
+          ok = wait_flag<kPair>(part_flag<kPair>(p, c, rank), p.epoch, ctl, p.timeout_ns);
+      if (!ok) break;
+    }
+    float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
     const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
     const int32_t cols_left = p.N - nt * kBN;
     const int64_t base = d_offset(p, mt, nt, r, 0);
@@ -480,8 +607,21 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
         for (int i = 0; i < 32; ++i) acc[i] = 0u;
       }
+      if (contributor) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
+        continue;
+      }
+      for (uint32_t c = c_lo; c <= c_hi; ++c) {
+        if (!sk_has_units(p, nclusters, c)) continue;
+        const float* part = part_slot<kPair>(p, c, rank);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+      }
       if (row_ok) store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0));
     }
+    if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) {
@@ -490,6 +630,17 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
         mbar_arrive_cluster(map_to_cta(ae, 0));
       else
         mbar_arrive(ae);
+      if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
+    }
+    if (contributor && warp == 2) {
+      // a CTA contributes at most one partial per launch: part_done completes phase 0 once
+      // all four epilogue warps have written theirs; then publish it at device scope
+      if (!wait_warp<kPair>(smem_addr(&ctl->part_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        st_release_gpu(part_flag<kPair>(p, cluster, rank), p.epoch);
+      }
+      __syncwarp();
     }
   }
 }
@@ -522,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&ctl->acc_empty[b]), C::kAccEmptyArrivals);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
+    mbar_init(smem_addr(&ctl->part_done), 4);
     ctl->abort = 0;
     fence_barrier_init();
     if (p.k_blocks > 0) {
@@ -617,6 +769,8 @@ std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
 int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair
+int g_force_schedule = 0;  // 0: stream-K when a workspace is given and tiles leave a ragged
+                           // last wave; 1: data-parallel only; 2: stream-K whenever possible
 
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
@@ -627,6 +781,7 @@ struct DeviceState {
   bool attr_single[2] = {false, false};
   bool attr_pair[2] = {false, false};
   int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
+  uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
 };
 DeviceState g_dev[128];
@@ -821,6 +976,9 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
   p->k_blocks = static_cast<int32_t>(pl.k_blocks);
   p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);
   p->group_m = pl.variant == kVariantPair ? 8 : 16;
+  const int kkb = pl.variant == kVariantPair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
+  p->nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
+  p->dp_tiles = p->num_tiles;   // data-parallel unless the caller sets up stream-K
   p->majorA = majorA;
   p->majorB = majorB;
   p->alpha = alpha;
@@ -841,7 +999,7 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
 
 template <bool kBF16>
 gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                        cudaStream_t s) {
+                        int grid, cudaStream_t s) {
   using C = gb::Cfg<false>;
   if (!dev->attr_single[kBF16]) {
     if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -849,14 +1007,12 @@ gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensor
       return GB_ERR_LAUNCH;
     dev->attr_single[kBF16] = true;
   }
-  const int grid = std::min(p.num_tiles, dev->sms);
   gb::gemm_kernel<kBF16, false><<<grid, gb::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
 template <bool kBF16>
-gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                      cudaStream_t s) {
+gb_status prepare_pair(DeviceState* dev) {
   using C = gb::Cfg<true>;
   if (!dev->attr_pair[kBF16]) {
     if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -864,6 +1020,31 @@ gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMa
       return GB_ERR_LAUNCH;
     dev->attr_pair[kBF16] = true;
   }
+  if (dev->pair_clusters == 0) {
+    // a persistent grid must fit at once: ask how many pairs can be resident together
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(gb::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * (dev->sms / 2), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true>, &cfg) != cudaSuccess || n <= 0)
+      n = dev->sms / 2;
+    dev->pair_clusters = std::min(n, dev->sms / 2);
+  }
+  return GB_OK;
+}
+
+template <bool kBF16>
+gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+                      int clusters, cudaStream_t s) {
+  using C = gb::Cfg<true>;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -875,23 +1056,21 @@ gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMa
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dev->pair_clusters == 0) {
-    // a persistent grid must fit at once: ask how many pairs can be resident together
-    int n = 0;
-    cfg.gridDim = dim3(2 * (dev->sms / 2), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true>, &cfg) != cudaSuccess || n <= 0)
-      n = dev->sms / 2;
-    dev->pair_clusters = std::min(n, dev->sms / 2);
-  }
-  const int clusters = std::min(p.num_tiles, dev->pair_clusters);
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true>, tmA, tmB, p) != cudaSuccess) return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
+// Workspace layout: one 32-bit flag per CTA (padded to 256 B), then one 128 x 256 fp32
+// partial per CTA.  Every slot a grid on this device can use fits (one per SM).
+int64_t workspace_bytes_for(int sms) {
+  const int64_t flags = ((static_cast<int64_t>(sms) * 4 + 255) / 256) * 256;
+  return flags + static_cast<int64_t>(sms) * gb::kSlotFloats * 4;
+}
+
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
-                     void* stream) {
+                     void* workspace, size_t workspace_size, void* stream) {
   gb_gemm_plan pl;
   gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl);
   if (st != GB_OK) return st;
@@ -901,8 +1080,11 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if (K > 0 && (A == nullptr || B == nullptr)) return GB_ERR_INVALID_ARG;
   if (!aligned16(D) || (C && !aligned16(C))) return GB_ERR_MISALIGNED;
   if (K > 0 && (!aligned16(A) || !aligned16(B))) return GB_ERR_MISALIGNED;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GB_ERR_MISALIGNED;
   DeviceState* dev;
   if ((st = device_state(&dev)) != GB_OK) return st;
+  if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
+    return GB_ERR_INVALID_ARG;
 
   CUtensorMap tmA, tmB;
   std::memset(&tmA, 0, sizeof(tmA));
@@ -913,10 +1095,40 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
+  const bool pair = pl.variant == kVariantPair;
+  if (pair && (st = dtype == GB_BF16 ? prepare_pair<true>(dev) : prepare_pair<false>(dev)) != GB_OK) return st;
+  const int slots = pair ? dev->pair_clusters : dev->sms;   // CTAs (pairs) that can run at once
+
+  // schedule: stream-K needs a workspace and some K; by default it is used when the tiles
+  // leave a ragged last wave (or fewer tiles than CTAs)
+  int sched;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    sched = g_force_schedule;
+  }
+  const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
+  p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
+  bool sk = workspace != nullptr && p.nsb > 0 && sched != 1;
+  if (sk && sched == 0) sk = p.num_tiles % slots != 0;
+  int G;
+  if (sk) {
+    G = slots;
+    const int full = p.num_tiles / G;
+    p.dp_tiles = full >= 2 ? (full - 1) * G : 0;
+    if (++dev->epoch == 0) dev->epoch = 1;
+    p.epoch = dev->epoch;
+    p.ws_flags = static_cast<uint32_t*>(workspace);
+    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         ((static_cast<int64_t>(dev->sms) * 4 + 255) / 256) * 256);
+  } else {
+    G = std::min(p.num_tiles, slots);
+    p.dp_tiles = p.num_tiles;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pl.variant == kVariantPair)
-    return dtype == GB_BF16 ? launch_pair<true>(dev, tmA, tmB, p, s) : launch_pair<false>(dev, tmA, tmB, p, s);
-  return dtype == GB_BF16 ? launch_single<true>(dev, tmA, tmB, p, s) : launch_single<false>(dev, tmA, tmB, p, s);
+  if (pair)
+    return dtype == GB_BF16 ? launch_pair<true>(dev, tmA, tmB, p, G, s) : launch_pair<false>(dev, tmA, tmB, p, G, s);
+  return dtype == GB_BF16 ? launch_single<true>(dev, tmA, tmB, p, G, s)
+                          : launch_single<false>(dev, tmA, tmB, p, G, s);
 }
 
 }  // namespace
@@ -926,13 +1138,45 @@ extern "C" {
 gb_status gb_gemm_f16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
                       const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
                       void* stream) {
-  return gemm_entry(GB_F16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, stream);
+  return gemm_entry(GB_F16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, nullptr, 0, stream);
 }
 
 gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
                        const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
                        void* stream) {
-  return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, stream);
+  return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, nullptr, 0, stream);
+}
+
+gb_status gb_gemm_f16_ws(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
+                         const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return GB_ERR_INVALID_ARG;
+  return gemm_entry(GB_F16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, workspace,
+                    workspace_bytes, stream);
+}
+
+gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda, int majorA,
+                          const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace) return GB_ERR_INVALID_ARG;
+  return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, workspace,
+                    workspace_bytes, stream);
+}
+
+gb_status gb_gemm_workspace_bytes(size_t* bytes) {
+  if (!bytes) return GB_ERR_INVALID_ARG;
+  DeviceState* dev;
+  gb_status st = device_state(&dev);
+  if (st != GB_OK) return st;
+  *bytes = static_cast<size_t>(workspace_bytes_for(dev->sms));
+  return GB_OK;
+}
+
+gb_status gb_set_schedule(int schedule) {
+  if (schedule < 0 || schedule > 2) return GB_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_force_schedule = schedule;
+  return GB_OK;
 }
 
 gb_status gb_last_device_status(void* stream, uint32_t* detail) {

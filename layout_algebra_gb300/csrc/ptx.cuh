@@ -324,3 +324,22 @@ __device__ __forceinline__ void st_global_stream(void* p, uint4 v, uint64_t poli
 }
 
 }  // namespace gb
+
+namespace gb {
+
+// Device-scope release/acquire on a 32-bit flag in global memory (cross-CTA hand-off).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+}  // namespace gb
