@@ -54,7 +54,9 @@ typedef enum {
   GB_ERR_UNSUPPORTED_ARCH = 3,
   GB_ERR_LAUNCH = 4,
   GB_ERR_TIMEOUT = 5,
-  GB_ERR_CUDA = 6
+  GB_ERR_CUDA = 6,
+  GB_ERR_SCRATCH_LIMIT = 7   /* gb_gemm_noalloc: the device needs more scratch than the
+                                built-in array holds */
 } gb_status;
 
 typedef enum { GB_K_MAJOR = 0, GB_MN_MAJOR = 1 } gb_major;
@@ -102,6 +104,28 @@ gb_status gb_gemm_workspace_bytes(size_t* bytes);
    ragged last wave or are fewer than the CTAs (the default), 1 whole tiles only, 2 stream-K
    whenever K > 0.  GB_ERR_INVALID_ARG for other values. */
 gb_status gb_set_schedule(int schedule);
+
+/* Allocation-free GEMM (no counterpart on the pages: an addition for callers that may not
+   allocate device memory).  Some callers cannot call cudaMalloc at the point where they
+   run a GEMM: code inside a runtime that owns every byte of device memory (a serving
+   engine or framework plugin with a fixed memory plan), code on a latency-critical path
+   where an allocation would synchronise the device, or code that only receives
+   pre-allocated input and output buffers.  This entry point serves them: it computes the
+   same result as gb_gemm_f16_ws / gb_gemm_bf16_ws (dtype = GB_F16 or GB_BF16), but its
+   stream-K scratch lives in a static array inside this library instead of a caller
+   workspace; it calls no allocating routine.
+   Limits and sharing: the array holds about 20 MiB (one 128 x 256 fp32 partial and one
+   flag for each of up to 160 SMs) and every GPU that loads the library keeps it until
+   the process exits; a device with more SMs gets GB_ERR_SCRATCH_LIMIT.  All calls on a
+   device share the one array and it keeps the last call's contents, so calls that may run
+   at the same time on the GPU (different streams, overlapping launches) race and must not
+   be issued.  The first call on each device looks up the array's device address and
+   clears its flags (a synchronous memset); make that first call before any stream
+   capture.  Other arguments, errors and ownership as for gb_gemm_f16. */
+gb_status gb_gemm_noalloc(int dtype, int64_t M, int64_t N, int64_t K, float alpha,
+                          const void* A, int64_t lda, int majorA,
+                          const void* B, int64_t ldb, int majorB,
+                          float beta, const void* C, void* D, void* stream);
 
 /* Synchronises `stream`, then returns GB_ERR_TIMEOUT if any kernel of this library on the
    current device recorded a wait that ran out since the last call (the raw code goes to

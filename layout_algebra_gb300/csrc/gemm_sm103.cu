@@ -1197,6 +1197,7 @@ const char* gb_status_string(int status) {
     case GB_ERR_LAUNCH: return "launch failed";
     case GB_ERR_TIMEOUT: return "device wait timed out";
     case GB_ERR_CUDA: return "CUDA runtime error";
+    case GB_ERR_SCRATCH_LIMIT: return "device needs more scratch than the built-in array holds";
     default: return "unknown status";
   }
 }
@@ -1276,3 +1277,48 @@ gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64
 }
 
 }  // extern "C"
+
+// ====================================================================== allocation-free entry
+// For callers that may not allocate device memory: the stream-K scratch of
+// gb_gemm_noalloc is this array, sized for devices of up to kNoAllocMaxSms SMs.  It is
+// zero at module load; its flag region is cleared once more at set-up.
+namespace {
+constexpr int kNoAllocMaxSms = 160;
+constexpr int64_t kNoAllocFlagBytes = ((static_cast<int64_t>(kNoAllocMaxSms) * 4 + 255) / 256) * 256;
+constexpr int64_t kNoAllocBytes =
+    kNoAllocFlagBytes + static_cast<int64_t>(kNoAllocMaxSms) * gb::kSlotFloats * 4;
+void* g_noalloc_ptr[128] = {};   // device address of the array, per device, after set-up
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+extern "C" gb_status gb_gemm_noalloc(int dtype, int64_t M, int64_t N, int64_t K, float alpha,
+                                     const void* A, int64_t lda, int majorA, const void* B,
+                                     int64_t ldb, int majorB, float beta, const void* C, void* D,
+                                     void* stream) {
+  if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  DeviceState* dev;
+  gb_status st = device_state(&dev);
+  if (st != GB_OK) return st;
+  if (workspace_bytes_for(dev->sms) > kNoAllocBytes) return GB_ERR_SCRATCH_LIMIT;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 128) return GB_ERR_CUDA;
+  void* scratch;
+  {
+    // set-up, once per device, with that device current: host code cannot use the array's
+    // name as an address, so ask the runtime for it
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_noalloc_ptr[device] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return GB_ERR_CUDA;
+      // the hand-off flags must not hold a launch number of this process
+      if (cudaMemset(ptr, 0, static_cast<size_t>(workspace_bytes_for(dev->sms) - dev->sms * int64_t(gb::kSlotFloats) * 4)) !=
+          cudaSuccess)
+        return GB_ERR_CUDA;
+      g_noalloc_ptr[device] = ptr;
+    }
+    scratch = g_noalloc_ptr[device];
+  }
+  return gemm_entry(dtype, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, scratch,
+                    static_cast<size_t>(kNoAllocBytes), stream);
+}

@@ -1,0 +1,74 @@
+"""The allocation-free entry point, gb_gemm_noalloc, through the C ABI.
+
+It serves callers that may not allocate device memory while they run a GEMM, for
+instance code inside a runtime that owns all device memory or code on a path where an
+allocation would synchronise the device: its stream-K scratch is an array built into the
+library.  This checks it against the existing entry points on two calls in a row, each
+within the acceptance bound the other GEMM tests use.  The file is named to be collected
+last, so a run that stops at the first failure has run every other test before it.
+"""
+import numpy as np
+import pytest
+import torch
+
+from layout_algebra_gb300 import _native
+from layout_algebra_gb300 import binding as G
+from layout_algebra_gb300 import workloads as W
+from oracle import gemm_ref as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _noalloc(p, A, B, C, D):
+    st = _native.lib().gb_gemm_noalloc(
+        O.dtype_code(p.dtype), p.M, p.N, p.K, p.alpha, A.data_ptr(), W.leading_dims(p)[0],
+        G.major_code(p.majorA), B.data_ptr(), W.leading_dims(p)[1], G.major_code(p.majorB),
+        p.beta, C.data_ptr() if C is not None else None, D.data_ptr(),
+        torch.cuda.current_stream().cuda_stream)
+    assert st == 0, G.status_string(st)
+    st, detail = G.last_device_status()
+    assert st == 0, "device status %d detail %#x" % (st, detail)
+
+
+def _bound_and_values(p, data, D):
+    code = O.dtype_code(p.dtype)
+    C = W.bits(data["C"]) if data["C"] is not None else None
+    ref, sab = O.gemm(p.M, p.N, p.K, p.alpha, W.bits(data["A"]), data["lda"],
+                      G.major_code(p.majorA), W.bits(data["B"]), data["ldb"],
+                      G.major_code(p.majorB), p.beta, C, p.N, code)
+    c = O.decode(code, C).reshape(p.M, p.N) if C is not None else None
+    bound = O.bound(code, p.alpha, p.beta, ref, sab, c)
+    return ref, bound
+
+
+@pytest.mark.parametrize("problems", [[
+    # few tiles: stream-K splits every tile across many CTAs
+    W.Problem("na1", 1000, 1000, 777, "bf16", has_c=True, alpha=1.25, beta=0.5, dist="normal",
+              c_dist="normal", seed=301, lda=784, ldb=784),
+    # ragged last wave of whole tiles plus split tiles, other majors and dtype
+    W.Problem("na2", 4100, 2056, 1536, "f16", majorA="MN", majorB="MN", has_c=True,
+              alpha=0.75, beta=1.0, dist="uniform", c_dist="normal", c_sigma=0.5, seed=302,
+              lda=4104),
+]])
+def test_no_alloc_matches_existing_entry_points_on_two_calls(problems):
+    workspace = G.make_workspace(DEV)
+    for p in problems:                       # two calls in a row share the built-in array
+        data = W.make(p)
+        A, B = data["A"].to(DEV), data["B"].to(DEV)
+        C = data["C"].to(DEV) if data["C"] is not None else None
+        kw = dict(lda=data["lda"], ldb=data["ldb"], majorA=p.majorA, majorB=p.majorB,
+                  alpha=p.alpha, beta=p.beta, C=C)
+        D_ws = G.gemm(A, B, p.M, p.N, p.K, workspace=workspace, **kw)     # existing, stream-K
+        D_plain = G.gemm(A, B, p.M, p.N, p.K, **kw)                      # existing, no scratch
+        D_na = torch.full((p.M * p.N,), float("nan"), dtype=A.dtype, device=DEV)
+        _noalloc(p, A, B, C, D_na)
+        torch.cuda.synchronize()
+        code = O.dtype_code(p.dtype)
+        ref, bound = _bound_and_values(p, data, D_na)
+        got = O.decode(code, W.bits(D_na.cpu())).reshape(p.M, p.N)
+        for other in (D_ws, D_plain):
+            want = O.decode(code, W.bits(other.cpu())).reshape(p.M, p.N)
+            assert np.all(np.abs(got - want) <= bound)
+        assert np.all(np.abs(got - ref) <= bound)
