@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workspace", action="store_true",
+                    help="time the workspace entry point (stream-K schedule where it helps)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
                     help="CPU time budget of the whole reference run")
     return ap.parse_args(argv)
@@ -280,10 +282,16 @@ def run_gb300(args):
     sh = stream.cuda_stream
     lda, ldb = data["lda"], data["ldb"]
     cptr = C.data_ptr() if C is not None else None
+    ws = G.make_workspace(dev) if args.workspace else None
 
     def launch():
-        st = G.raw_call(A.dtype, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda, p.majorA, B.data_ptr(), ldb,
-                        p.majorB, p.beta, cptr, D.data_ptr(), sh)
+        if ws is not None:
+            st = G.raw_call_ws(A.dtype, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda, p.majorA,
+                               B.data_ptr(), ldb, p.majorB, p.beta, cptr, D.data_ptr(),
+                               ws.data_ptr(), ws.numel(), sh)
+        else:
+            st = G.raw_call(A.dtype, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda, p.majorA,
+                            B.data_ptr(), ldb, p.majorB, p.beta, cptr, D.data_ptr(), sh)
         if st != 0:
             raise G.GemmError(st)
 
@@ -328,7 +336,7 @@ def run_gb300(args):
     D_h = torch.empty(p.M * p.N, dtype=A.dtype, pin_memory=True)
     for _ in range(2):
         G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
-               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h)
+               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
     torch.cuda.synchronize()
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     barrier(world, local)
@@ -338,7 +346,7 @@ def run_gb300(args):
     e0.record(stream)
     for _ in range(e2e_steps):
         G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
-               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h)
+               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world, local)
@@ -372,6 +380,8 @@ def run_gb300(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "roofline": roofline, "clocks": clocks, "gpu_launches": args.steps,
     }
+    line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
+                                     if ws is not None else "gb_gemm_%s" % p.dtype)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(p, data, args.cpu_seconds)
         line["cpu_baseline"] = {

@@ -100,6 +100,14 @@ def raw_call(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta
               major_code(majorB), float(beta), C_ptr, D_ptr, stream_handle)
 
 
+def raw_call_ws(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta, C_ptr,
+                D_ptr, ws_ptr, ws_bytes, stream_handle):
+    """Direct C-ABI call of the workspace (stream-K) entry point; returns the status."""
+    fn = lib().gb_gemm_bf16_ws if dtype_code(dtype) == BF16 else lib().gb_gemm_f16_ws
+    return fn(M, N, K, float(alpha), A_ptr, lda, major_code(majorA), B_ptr, ldb,
+              major_code(majorB), float(beta), C_ptr, D_ptr, ws_ptr, ws_bytes, stream_handle)
+
+
 def plan(dtype, M, N, K, lda, majorA, ldb, majorB):
     """Host-side plan (tile grid, copy geometry, instruction descriptor) as a dict."""
     p = GemmPlan()
