@@ -77,6 +77,16 @@ int la_local_tile(const char* layout, const char* tiler, const int64_t* grid, in
 int la_local_partition(const char* layout, const char* thr, int64_t tid, int64_t* origin,
                        char* out, size_t cap);
 
+/* logical_product(A, B) = (A, complement(A, size(A)*cosize(B)) o B): copies of A laid out
+   by the pattern B ("Layouts as Algebra" — "Divide is tiling", the mirror of divide). */
+int la_logical_product(const char* a, const char* b, char* out, size_t cap);
+
+/* Swizzle functor Sw<bits,base,shift> applied to n offsets:
+   out[i] = x ^ ((x >> shift) & (((1 << bits) - 1) << base)), x = in[i].  Needs
+   0 <= bits <= shift and bits + base + shift <= 62.  The tensor copies' 128-byte
+   shared-memory swizzle is Sw<3,4,3> on byte offsets. */
+int la_swizzle(int bits, int base, int shift, const int64_t* in, int64_t n, int64_t* out);
+
 /* Offset grid of a rank-2 layout (rows = mode 0, columns = mode 1) as text. */
 int la_print_layout(const char* layout, char* out, size_t cap);
 

@@ -19,7 +19,8 @@ GEMM_SYMBOLS = [
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
     "la_composition", "la_complement", "la_logical_divide", "la_zipped_divide",
-    "la_local_tile", "la_local_partition", "la_print_layout",
+    "la_local_tile", "la_local_partition", "la_print_layout", "la_logical_product",
+    "la_swizzle",
 ]
 
 
@@ -107,6 +108,10 @@ def lib():
     L.la_local_tile.argtypes = [cp, cp, vp, ci, ctypes.POINTER(i64), cp, sz]
     L.la_local_partition.restype = ci
     L.la_local_partition.argtypes = [cp, cp, i64, ctypes.POINTER(i64), cp, sz]
+    L.la_logical_product.restype = ci
+    L.la_logical_product.argtypes = [cp, cp, cp, sz]
+    L.la_swizzle.restype = ci
+    L.la_swizzle.argtypes = [ci, ci, ci, vp, i64, vp]
     L.la_print_layout.restype = ci
     L.la_print_layout.argtypes = [cp, cp, sz]
     _lib = L

@@ -401,6 +401,19 @@ Layout zipped_divide(const Layout& a, const Tiler& t) {
   return tuple_layout({tile, grid});
 }
 
+Layout logical_product(const Layout& a, const Layout& b) {
+  const int64_t target = checked_mul(size(a), cosize(b));
+  Layout c = complement(a, target);
+  return tuple_layout({a, composition(c, b)});
+}
+
+int64_t swizzle(int bits, int base, int shift, int64_t x) {
+  if (bits < 0 || base < 0 || shift < bits || bits + base + shift > 62)
+    throw Error(LA_ERR_ARG, "swizzle needs 0 <= bits <= shift and bits + base + shift <= 62");
+  const int64_t mask = ((int64_t(1) << bits) - 1) << base;
+  return x ^ ((x >> shift) & mask);
+}
+
 Layout local_tile(const Layout& a, const Tiler& t, const std::vector<int64_t>& grid_coord,
                   int64_t* origin) {
   Layout z = zipped_divide(a, t);

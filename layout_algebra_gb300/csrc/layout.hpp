@@ -96,6 +96,13 @@ Layout composition(const Layout& a, const Layout& b);
 Layout complement(const Layout& b, int64_t cotarget);
 Layout logical_divide(const Layout& a, const Tiler& t);
 Layout zipped_divide(const Layout& a, const Tiler& t);
+// logical_product(A, B) = (A, A* o B), A* = complement(A, size(A) * cosize(B)): copies of A
+// laid out by the pattern B ("Layouts as Algebra", "Divide is tiling": the mirror of divide).
+Layout logical_product(const Layout& a, const Layout& b);
+// Swizzle functor Sw<B,M,S>: x -> x ^ ((x >> S) & (((1 << B) - 1) << M)), i.e. the B bits
+// above bit M+S are folded into the B bits above bit M.  The 128-byte shared-memory
+// swizzle of the tensor copies, in byte offsets, is Sw<3,4,3>.
+int64_t swizzle(int bits, int base, int shift, int64_t x);
 // local_tile: the tile of zipped_divide(a, t) at grid coordinate `grid_coord`
 // (one index per grid leaf).  Returns the tile layout and its origin offset.
 Layout local_tile(const Layout& a, const Tiler& t, const std::vector<int64_t>& grid_coord,

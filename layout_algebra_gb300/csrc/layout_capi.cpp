@@ -136,6 +136,21 @@ int la_local_partition(const char* layout, const char* thr, int64_t tid, int64_t
   });
 }
 
+int la_logical_product(const char* a, const char* b, char* out, size_t cap) {
+  if (!a || !b) return LA_ERR_ARG;
+  return guarded([&] {
+    return put(la::to_string(la::logical_product(la::parse_layout(a), la::parse_layout(b))), out, cap);
+  });
+}
+
+int la_swizzle(int bits, int base, int shift, const int64_t* in, int64_t n, int64_t* out) {
+  if (n < 0 || (n > 0 && (!in || !out))) return LA_ERR_ARG;
+  return guarded([&] {
+    for (int64_t i = 0; i < n; ++i) out[i] = la::swizzle(bits, base, shift, in[i]);
+    return LA_OK;
+  });
+}
+
 int la_print_layout(const char* layout, char* out, size_t cap) {
   if (!layout) return LA_ERR_ARG;
   return guarded([&] { return put(la::print_layout(la::parse_layout(layout)), out, cap); });

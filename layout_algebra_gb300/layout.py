@@ -102,3 +102,19 @@ def local_partition(layout, thr, tid):
 
 def print_layout(layout):
     return _text(lib().la_print_layout, _b(layout))
+
+
+def logical_product(a, b):
+    return _text(lib().la_logical_product, _b(a), _b(b))
+
+
+def swizzle(bits, base, shift, offsets):
+    """Sw<bits,base,shift> applied to an int or a sequence of offsets."""
+    scalar = np.isscalar(offsets)
+    x = np.ascontiguousarray(np.atleast_1d(np.asarray(offsets, dtype=np.int64)))
+    out = np.empty_like(x)
+    rc = lib().la_swizzle(int(bits), int(base), int(shift), x.ctypes.data, x.size, out.ctypes.data)
+    if rc:
+        raise LayoutError(rc, "la_swizzle")
+    return int(out[0]) if scalar else out
+

@@ -214,3 +214,13 @@ def grid(layout):
     for i in range(size(r[0])):
         rows.append([evaluate(r, i) + evaluate(c, j) for j in range(size(c[0]))])
     return rows
+
+
+def product_table(a, b):
+    """logical_product(A, B) point by point: copy j of A starts where the complement of A
+    (the offsets its translated copies occupy) puts B(j).  Index i + size(A) * j."""
+    sa = size(a[0])
+    starts = complement_by_search(a, sa * cosize(b))
+    if starts is None:
+        raise ValueError("complement does not exist")
+    return [evaluate(a, i) + starts[evaluate(b, j)] for j in range(size(b[0])) for i in range(sa)]

@@ -118,3 +118,13 @@ def test_logical_divide_by_definition():
 def test_ragged_divide_drops_off_edge():
     d = R.divide_table(R.parse("10:1"), R.parse("4:1"))
     assert sorted(d) == list(range(10))     # 3 tiles of 4, the last two entries off the edge
+
+
+def test_product_table_pins():
+    # a compact tile repeated by a contiguous pattern fills 0..n-1 in order
+    assert R.product_table(R.parse("4:1"), R.parse("3:1")) == list(range(12))
+    assert R.product_table(R.parse("(2,2):(1,2)"), R.parse("3:1")) == list(range(12))
+    # worked by hand: 2:2 touches {0,2}; its copies start at 0 and 1 -> 0,2,1,3
+    assert R.product_table(R.parse("2:2"), R.parse("2:1")) == [0, 2, 1, 3]
+    # a strided pattern of copies: copy j of 2:1 sits at 2*B(j), B = 2:2 -> 0,1,4,5
+    assert R.product_table(R.parse("2:1"), R.parse("2:2")) == [0, 1, 4, 5]
