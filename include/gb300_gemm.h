@@ -105,6 +105,35 @@ gb_status gb_gemm_workspace_bytes(size_t* bytes);
    whenever K > 0.  GB_ERR_INVALID_ARG for other values. */
 gb_status gb_set_schedule(int schedule);
 
+/* Fused epilogue ("CUTLASS, in depth" — "Epilogue fusion": load C, load a bias vector,
+   add, activate, compute an absolute maximum for FP8 scaling, and store, on the
+   accumulator before it leaves the chip).  Per output, in fp32:
+     v = alpha*acc + beta*C[i,j];  v += bias[j] (if bias);  v = act(v);
+     *amax = max(*amax, |v|) (if amax);  D[i,j] = round(v) to the input type, or, for an FP8
+     output, round(v * out_scale) to FP8 with saturation at the largest finite value.
+   bias: N values of the input type (column j of D gets bias[j]), or NULL.
+   amax: a device float, combined with its current contents by max (zero it first), or NULL.
+   FP8 outputs are one byte per element, row-major with leading dimension N. */
+typedef enum { GB_ACT_NONE = 0, GB_ACT_RELU = 1, GB_ACT_GELU = 2 } gb_activation;
+typedef enum { GB_OUT_INPUT_TYPE = 0, GB_OUT_E4M3 = 1, GB_OUT_E5M2 = 2 } gb_out_format;
+typedef struct {
+  const void* bias;
+  int activation;     /* gb_activation; GELU is 0.5 v (1 + erf(v / sqrt 2)) */
+  float* amax;
+  int out_format;     /* gb_out_format */
+  float out_scale;    /* used by FP8 outputs; must be finite and > 0 for them */
+} gb_epilogue;
+
+/* D = epilogue(alpha*A*B + beta*C) with fp16 (dtype GB_F16) or bf16 (GB_BF16) inputs.  epi
+   NULL gives the plain call.  workspace / workspace_bytes: as for gb_gemm_f16_ws, or NULL/0
+   for whole tiles only.  Errors as for gb_gemm_f16, plus GB_ERR_INVALID_ARG for an unknown
+   activation or output format or a bad FP8 scale. */
+gb_status gb_gemm_ex(int dtype, int64_t M, int64_t N, int64_t K, float alpha,
+                     const void* A, int64_t lda, int majorA,
+                     const void* B, int64_t ldb, int majorB,
+                     float beta, const void* C, void* D, const gb_epilogue* epi,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free GEMM (no counterpart on the pages: an addition for callers that may not
    allocate device memory).  Some callers cannot call cudaMalloc at the point where they
    run a GEMM: code inside a runtime that owns every byte of device memory (a serving

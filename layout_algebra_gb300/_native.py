@@ -14,7 +14,7 @@ GEMM_SYMBOLS = [
     "gb_gemm_make_plan", "gb_set_wait_timeout_ns", "gb_debug_skip_k_block",
     "gb_debug_epilogue_map", "gb_debug_stage_bytes", "gb_set_kernel_variant",
     "gb_gemm_f16_ws", "gb_gemm_bf16_ws", "gb_gemm_workspace_bytes", "gb_set_schedule",
-    "gb_gemm_noalloc",
+    "gb_gemm_noalloc", "gb_gemm_ex",
 ]
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
@@ -26,6 +26,12 @@ LAYOUT_SYMBOLS = [
 
 class NativeLibraryMissing(RuntimeError):
     pass
+
+
+class Epilogue(ctypes.Structure):
+    _fields_ = [("bias", ctypes.c_void_p), ("activation", ctypes.c_int),
+                ("amax", ctypes.c_void_p), ("out_format", ctypes.c_int),
+                ("out_scale", ctypes.c_float)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -63,6 +69,9 @@ def lib():
         fn = getattr(L, name)
         fn.restype = ci
         fn.argtypes = [i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp, sz, vp]
+    L.gb_gemm_ex.restype = ci
+    L.gb_gemm_ex.argtypes = [ci, i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp,
+                             ctypes.POINTER(Epilogue), vp, sz, vp]
     L.gb_gemm_noalloc.restype = ci
     L.gb_gemm_noalloc.argtypes = [ci, i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp]
     L.gb_gemm_workspace_bytes.restype = ci

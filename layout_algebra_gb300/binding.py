@@ -10,7 +10,7 @@ import ctypes
 
 import torch
 
-from ._native import GemmPlan, lib
+from ._native import Epilogue, GemmPlan, lib
 
 K_MAJOR, MN_MAJOR = 0, 1
 F16, BF16 = 0, 1
@@ -90,6 +90,34 @@ def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0
         D.copy_(D_d, non_blocking=True)
         return D
     return D_d
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+OUT_FORMATS = {"input": 0, "e4m3": 1, "e5m2": 2}
+
+
+def gemm_fused(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0, C=None,
+               bias=None, activation="none", amax=None, out_format="input", out_scale=1.0,
+               D=None, workspace=None, stream=None):
+    """D = epilogue(alpha*A@B + beta*C) through gb_gemm_ex (device tensors only).
+
+    bias: N values of the input dtype; amax: a 1-element float32 device tensor (combined by
+    max with its contents); out_format "e4m3"/"e5m2" returns float8 tensors of M*N elements.
+    """
+    dt = dtype_code(A.dtype)
+    fmt = OUT_FORMATS[out_format]
+    if D is None:
+        out_dtype = {0: A.dtype, 1: torch.float8_e4m3fn, 2: torch.float8_e5m2}[fmt]
+        D = torch.empty(M * N, dtype=out_dtype, device=A.device)
+    epi = Epilogue(_ptr(bias), ACTIVATIONS[activation], _ptr(amax), fmt, float(out_scale))
+    st = lib().gb_gemm_ex(dt, M, N, K, float(alpha), _ptr(A), lda, major_code(majorA), _ptr(B),
+                          ldb, major_code(majorB), float(beta), _ptr(C), _ptr(D),
+                          ctypes.byref(epi), _ptr(workspace),
+                          0 if workspace is None else workspace.numel() * workspace.element_size(),
+                          _stream_handle(stream))
+    if st != 0:
+        raise GemmError(st, "gemm_fused")
+    return D
 
 
 def raw_call(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta, C_ptr, D_ptr,

@@ -30,6 +30,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -105,6 +106,15 @@ struct Params {
   uint32_t epoch;             // launch number, written to the partial-ready flags
   float* ws_part;             // per CTA slot: one 128 x 256 fp32 partial accumulator
   uint32_t* ws_flags;         // per CTA slot: epoch of the last partial written
+  // fused epilogue ("CUTLASS, in depth" — "Epilogue fusion"): v = alpha*acc + beta*c,
+  // v += bias[column], v = act(v), amax = max |v|, D = v (16-bit) or sat_fp8(v * out_scale)
+  int32_t fused;              // 0: plain alpha/beta epilogue
+  const uint16_t* bias;       // N values of the input type, or null
+  int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf form)
+  float* amax;                // device float receiving max |v| (by atomic max), or null
+  int32_t out_fmt;            // 0 same 16-bit type as the inputs, 1 FP8 E4M3, 2 FP8 E5M2
+  float out_scale;
+  int32_t vec8_ok;            // 16-byte FP8 stores legal (N % 16 == 0)
 };
 
 // Slot of CTA (cluster c, rank r) in the stream-K workspace.
@@ -489,36 +499,38 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
          (static_cast<uint32_t>(from_f32<kBF16>(hi)) << 16);
 }
 
-// 32 consecutive outputs of one row: v = alpha*acc (+ beta*c), rounded and stored.
+// 32 consecutive outputs of one row: v = alpha*acc (+ beta*c) in fp32.
 template <bool kBF16>
-__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint32_t (&acc)[32],
-                                          int valid) {
-  float v[32];
+__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, const uint32_t (&acc)[32],
+                                                int valid, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
-  const bool vec = p.vec_ok && valid == 32;
-  if (p.has_c) {
-    if (vec) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.C + off);
+  if (!p.has_c) return;
+  if (p.vec_ok && valid == 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.C + off);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 u = __ldg(src + j);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    for (int j = 0; j < 4; ++j) {
+      const uint4 u = __ldg(src + j);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
-                                  v[8 * j + 2 * e]);
-          v[8 * j + 2 * e + 1] =
-              fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
-        }
+      for (int e = 0; e < 4; ++e) {
+        v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
+                                v[8 * j + 2 * e]);
+        v[8 * j + 2 * e + 1] =
+            fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[off + i * p.d_col]), v[i]);
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[off + i * p.d_col]), v[i]);
   }
-  if (vec) {
+}
+
+// Round v to the 16-bit output type and store it (16-byte stores when legal).
+template <bool kBF16>
+__device__ __forceinline__ void store_16(const Params& p, int64_t off, const float (&v)[32], int valid) {
+  if (p.vec_ok && valid == 32) {
     uint4* dst = reinterpret_cast<uint4*>(p.D + off);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -534,6 +546,58 @@ __device__ __forceinline__ void store_run(const Params& p, int64_t off, const ui
     for (int i = 0; i < 32; ++i)
       if (i < valid) p.D[off + i * p.d_col] = from_f32<kBF16>(v[i]);
   }
+}
+
+// v * out_scale to FP8 with saturation to the largest finite value (round to nearest even).
+__device__ __forceinline__ uint32_t to_fp8(float x, int fmt) {
+  return fmt == 1 ? static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3))
+                  : static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2));
+}
+
+__device__ __forceinline__ void store_fp8(const Params& p, int64_t off, const float (&v)[32], int valid) {
+  uint8_t* d8 = reinterpret_cast<uint8_t*>(p.D);
+  if (p.vec8_ok && valid == 32) {
+    uint4* dst = reinterpret_cast<uint4*>(d8 + off);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int b = 16 * j + 4 * e;
+        w[e] = to_fp8(v[b] * p.out_scale, p.out_fmt) | (to_fp8(v[b + 1] * p.out_scale, p.out_fmt) << 8) |
+               (to_fp8(v[b + 2] * p.out_scale, p.out_fmt) << 16) |
+               (to_fp8(v[b + 3] * p.out_scale, p.out_fmt) << 24);
+      }
+      dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) d8[off + i * p.d_col] = static_cast<uint8_t>(to_fp8(v[i] * p.out_scale, p.out_fmt));
+  }
+}
+
+// The epilogue of 32 consecutive outputs of one row (columns col0 .. col0+31).
+template <bool kBF16>
+__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint32_t (&acc)[32], int valid,
+                                          int64_t col0, float& amax) {
+  float v[32];
+  epilogue_values<kBF16>(p, off, acc, valid, v);
+  if (!p.fused) {
+    store_16<kBF16>(p, off, v, valid);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (p.bias != nullptr && i < valid) v[i] += to_f32<kBF16>(__ldg(p.bias + col0 + i));
+    if (p.act == 1) v[i] = fmaxf(v[i], 0.0f);
+    if (p.act == 2) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
+    if (i < valid) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  if (p.out_fmt == 0)
+    store_16<kBF16>(p, off, v, valid);
+  else
+    store_fp8(p, off, v, valid);
 }
 
 // Stream-K workspace slot of CTA (cluster c, rank r): a 128 x 256 fp32 partial stored
@@ -584,6 +648,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
   const int r = static_cast<int>(rank) * kRowsA + lrow;   // row within the tile
   int32_t it = 0;
+  float amax = 0.0f;                 // this thread's max |v| (fused epilogue)
   Sched sched;
   sched.init(p, cluster, nclusters);
   Item item;
@@ -633,7 +698,9 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
         for (int i = 0; i < 32; ++i)
           acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
       }
-      if (row_ok) store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0));
+      if (row_ok)
+        store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0),
+                         static_cast<int64_t>(nt) * kBN + c0, amax);
     }
     if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
     tc_fence_before_sync();
@@ -656,6 +723,12 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       }
       __syncwarp();
     }
+  }
+  if (p.fused && p.amax != nullptr) {
+    // one atomic per warp; |v| >= 0, so the float order equals the integer order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(p.amax), __float_as_int(amax));
   }
 }
 
@@ -1084,7 +1157,7 @@ int64_t workspace_bytes_for(int sms) {
 
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
-                     void* workspace, size_t workspace_size, void* stream) {
+                     void* workspace, size_t workspace_size, void* stream, const gb_epilogue* epi = nullptr) {
   gb_gemm_plan pl;
   gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl);
   if (st != GB_OK) return st;
@@ -1095,6 +1168,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if (!aligned16(D) || (C && !aligned16(C))) return GB_ERR_MISALIGNED;
   if (K > 0 && (!aligned16(A) || !aligned16(B))) return GB_ERR_MISALIGNED;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GB_ERR_MISALIGNED;
+  if (epi) {
+    if (epi->activation < GB_ACT_NONE || epi->activation > GB_ACT_GELU) return GB_ERR_INVALID_ARG;
+    if (epi->out_format < GB_OUT_INPUT_TYPE || epi->out_format > GB_OUT_E5M2) return GB_ERR_INVALID_ARG;
+    if (epi->out_format != GB_OUT_INPUT_TYPE && !(epi->out_scale > 0.0f && epi->out_scale < 3.0e38f))
+      return GB_ERR_INVALID_ARG;
+    if (epi->amax && (reinterpret_cast<uintptr_t>(epi->amax) & 3u) != 0) return GB_ERR_MISALIGNED;
+    if (epi->bias && (reinterpret_cast<uintptr_t>(epi->bias) & 1u) != 0) return GB_ERR_MISALIGNED;
+  }
   DeviceState* dev;
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
@@ -1109,6 +1190,15 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
+  if (epi) {
+    p.fused = 1;
+    p.bias = static_cast<const uint16_t*>(epi->bias);
+    p.act = epi->activation;
+    p.amax = epi->amax;
+    p.out_fmt = epi->out_format;
+    p.out_scale = epi->out_scale;
+    p.vec8_ok = (pl.d_elem_stride[1] == 1 && N % 16 == 0) ? 1 : 0;
+  }
   const bool pair = pl.variant == kVariantPair;
   if (pair && (st = dtype == GB_BF16 ? prepare_pair<true>(dev) : prepare_pair<false>(dev)) != GB_OK) return st;
   const int slots = pair ? dev->pair_clusters : dev->sms;   // CTAs (pairs) that can run at once
@@ -1175,6 +1265,14 @@ gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha, const vo
   if (!workspace) return GB_ERR_INVALID_ARG;
   return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, workspace,
                     workspace_bytes, stream);
+}
+
+gb_status gb_gemm_ex(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
+                     int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
+                     const gb_epilogue* epi, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  return gemm_entry(dtype, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, workspace,
+                    workspace_bytes, stream, epi);
 }
 
 gb_status gb_gemm_workspace_bytes(size_t* bytes) {

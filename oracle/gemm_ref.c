@@ -34,7 +34,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2, ORACLE_E5M2 = 3 };
 enum { ORACLE_K_MAJOR = 0, ORACLE_MN_MAJOR = 1 };
 
 /* binary16: sign 1 bit, exponent 5 bits (bias 15), fraction 10 bits. */
@@ -69,8 +69,46 @@ static double decode_bf16(uint16_t b) {
     return sign ? -v : v;
 }
 
+/* FP8 E4M3 (the "fn" variant: 1/4/3, bias 7, no infinities; S.1111.111 is NaN, the
+   largest finite value is 448). */
+static double decode_e4m3(uint16_t bits) {
+    int sign = (bits >> 7) & 1;
+    int e = (bits >> 3) & 0xf;
+    int f = bits & 0x7;
+    double v;
+    if (e == 15 && f == 7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, -9);                  /* f * 2^(1-7-3) */
+    } else {
+        v = ldexp((double)(f + 8), e - 10);        /* (1 + f/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+/* FP8 E5M2 (1/5/2, bias 15, IEEE-style infinities and NaNs; largest finite 57344). */
+static double decode_e5m2(uint16_t bits) {
+    int sign = (bits >> 7) & 1;
+    int e = (bits >> 2) & 0x1f;
+    int f = bits & 0x3;
+    double v;
+    if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)f, -16);                 /* f * 2^(1-15-2) */
+    } else {
+        v = ldexp((double)(f + 4), e - 17);        /* (1 + f/4) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
 static double decode(int dtype, uint16_t bits) {
-    return dtype == ORACLE_BF16 ? decode_bf16(bits) : decode_f16(bits);
+    switch (dtype) {
+        case ORACLE_BF16: return decode_bf16(bits);
+        case ORACLE_E4M3: return decode_e4m3(bits);
+        case ORACLE_E5M2: return decode_e5m2(bits);
+        default: return decode_f16(bits);
+    }
 }
 
 /*
@@ -111,9 +149,45 @@ static uint16_t encode_rne(double x, int p, int emin, int exp_bits, double maxfi
     return (uint16_t)(sign | (field << frac_bits) | frac);
 }
 
+/*
+ * Round to FP8 with saturation to the largest finite value (the conversion a scaled FP8
+ * output uses): round to nearest, ties to even, on the format's grid; magnitudes beyond
+ * the largest finite value become that value; NaN stays NaN.
+ */
+static uint16_t encode_fp8_sat(int dtype, double x) {
+    int frac_bits = dtype == ORACLE_E4M3 ? 3 : 2;
+    int bias = dtype == ORACLE_E4M3 ? 7 : 15;
+    int emin = 1 - bias;
+    double maxfin = dtype == ORACLE_E4M3 ? 448.0 : 57344.0;
+    uint16_t sign = (uint16_t)(signbit(x) ? 0x80u : 0u);
+    if (isnan(x)) return (uint16_t)(dtype == ORACLE_E4M3 ? 0x7f : 0x7e);
+    double a = fabs(x);
+    if (a >= maxfin) a = maxfin;
+    double q;
+    int unbiased;
+    if (a < ldexp(1.0, emin)) {
+        q = rint(ldexp(a, frac_bits - emin));              /* subnormal grid 2^(emin-frac) */
+        return (uint16_t)(sign | (uint16_t)q);             /* q == 2^frac is the smallest normal */
+    }
+    int E;
+    double fr = frexp(a, &E);
+    unbiased = E - 1;
+    q = rint(ldexp(fr, frac_bits + 1));
+    if (q == ldexp(1.0, frac_bits + 1)) {
+        q = ldexp(1.0, frac_bits);
+        unbiased += 1;
+    }
+    uint32_t bits = ((uint32_t)(unbiased + bias) << frac_bits) | ((uint32_t)q - (1u << frac_bits));
+    /* rounding up past the largest finite value saturates */
+    double back = ldexp(q, unbiased - frac_bits);
+    if (back > maxfin) return (uint16_t)(sign | (dtype == ORACLE_E4M3 ? 0x7e : 0x7b));
+    return (uint16_t)(sign | bits);
+}
+
 static uint16_t encode(int dtype, double x) {
     if (dtype == ORACLE_BF16)
         return encode_rne(x, 8, -126, 8, ldexp(255.0, 120));   /* (2 - 2^-7) * 2^127 */
+    if (dtype == ORACLE_E4M3 || dtype == ORACLE_E5M2) return encode_fp8_sat(dtype, x);
     return encode_rne(x, 11, -14, 5, 65504.0);                  /* (2 - 2^-10) * 2^15 */
 }
 

@@ -20,7 +20,7 @@ import numpy as np
 
 from . import build as _build
 
-F16, BF16 = 0, 1
+F16, BF16, E4M3, E5M2 = 0, 1, 2, 3
 K_MAJOR, MN_MAJOR = 0, 1
 
 _lib = None
@@ -108,6 +108,42 @@ def gemm(M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, ldc, dtype,
     if rows is None:
         return ref.reshape(M, N), sab.reshape(M, N)
     return ref, sab
+
+
+def gelu(v):
+    """GELU in its erf form, 0.5 v (1 + erf(v / sqrt 2)), in float64."""
+    from scipy.special import erf
+    v = np.asarray(v, dtype=np.float64)
+    return 0.5 * v * (1.0 + erf(v / math.sqrt(2.0)))
+
+
+def fused(ref, bias_cols=None, activation="none"):
+    """The fused epilogue after alpha*acc + beta*c ("CUTLASS, in depth", "Epilogue fusion"):
+    add the column's bias, then activate.  ref is (M, N) or per-entry with bias_cols given per
+    entry."""
+    v = np.asarray(ref, dtype=np.float64)
+    if bias_cols is not None:
+        v = v + bias_cols
+    if activation == "relu":
+        v = np.maximum(v, 0.0)
+    elif activation == "gelu":
+        v = gelu(v)
+    return v
+
+
+# Largest Lipschitz constant of the activations (bounds how accumulated error propagates):
+# ReLU 1; GELU max |d/dv| = 1.1289 (at v = +-sqrt(2)).
+LIPSCHITZ = {"none": 1.0, "relu": 1.0, "gelu": 1.13}
+
+
+def ulp_fp8(dtype, r):
+    """Spacing of an FP8 format at |r| (subnormal spacing near zero)."""
+    r = np.abs(np.asarray(r, dtype=np.float64))
+    emin, frac = (-6, 3) if dtype == E4M3 else (-14, 2)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(r > 0, r, 1.0)))
+    e = np.where(r > 0, np.maximum(e, emin), emin)
+    return np.ldexp(1.0, (e - frac).astype(np.int64))
 
 
 def ulp_out(dtype, r):

@@ -1,0 +1,69 @@
+"""Pins for the oracle's FP8 codecs, GELU and the fused-epilogue bound constants."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import gemm_ref as O
+
+
+@pytest.mark.parametrize("code,tdt", [(O.E4M3, torch.float8_e4m3fn), (O.E5M2, torch.float8_e5m2)])
+def test_fp8_decode_exhaustive(code, tdt):
+    b = np.arange(256, dtype=np.uint16)
+    got = O.decode(code, b)
+    want = torch.from_numpy(b.astype(np.uint8)).view(tdt).double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+@pytest.mark.parametrize("code,maxfin,maxcode", [(O.E4M3, 448.0, 0x7E), (O.E5M2, 57344.0, 0x7B)])
+def test_fp8_round_nearest_even_saturating(code, maxfin, maxcode):
+    rng = np.random.default_rng(int(maxfin))
+    x = np.ldexp(rng.random(20000) + 0.5, rng.integers(-20, 17, 20000))
+    x *= np.where(rng.random(20000) < 0.5, -1.0, 1.0)
+    got = O.round_to(code, x)
+    val = O.decode(code, got)
+    inside = np.abs(x) <= maxfin
+    # saturation: beyond the largest finite value the result is that value
+    assert np.all(np.abs(val[~inside]) == maxfin)
+    assert np.all(np.sign(val[~inside]) == np.sign(x[~inside]))
+    # inside: no neighbouring finite code is nearer
+    for delta in (-1, 1):
+        nb = got.astype(np.int64) + delta
+        ok = inside & ((nb & 0x7F) <= maxcode) & ((nb & 0x7F) >= 0)
+        nv = O.decode(code, nb[ok].astype(np.uint16))
+        assert np.all(np.abs(x[ok] - val[ok]) <= np.abs(x[ok] - nv))
+    # hand-placed ties go to the even code
+    one = 0x38 if code == O.E4M3 else 0x3C
+    step = 0.125 if code == O.E4M3 else 0.25
+    assert O.round_to(code, [1 + step / 2])[0] == one            # between 1 (even) and 1+step
+    assert O.round_to(code, [1 + 1.5 * step])[0] == one + 2      # between 1+step and 1+2step (even)
+    assert O.round_to(code, [maxfin * 4])[0] == maxcode
+    assert O.round_to(code, [-maxfin * 4])[0] == 0x80 | maxcode
+
+
+def test_gelu_pins():
+    # GELU(v) = v * Phi(v): textbook normal-CDF values
+    assert math.isclose(float(O.gelu([1.0])[0]), 0.8413447460685429, rel_tol=1e-14)
+    assert math.isclose(float(O.gelu([2.0])[0]), 2 * 0.9772498680518208, rel_tol=1e-14)
+    assert O.gelu([0.0])[0] == 0.0
+    v = np.linspace(-6, 6, 1001)
+    assert np.allclose(O.gelu(v) - O.gelu(-v), v, atol=1e-14)   # erf is odd
+    assert np.all(np.abs(O.gelu([-40.0, 40.0]) - np.array([0.0, 40.0])) < 1e-12)
+
+
+def test_lipschitz_constants_bound_the_activations():
+    v = np.linspace(-10, 10, 200001)
+    for act in ("relu", "gelu"):
+        y = O.fused(v, activation=act)
+        slope = np.max(np.abs(np.diff(y) / np.diff(v)))
+        assert slope <= O.LIPSCHITZ[act]
+
+
+def test_fused_bias_then_activation():
+    ref = np.array([[-1.0, 0.5], [2.0, -3.0]])
+    bias = np.array([1.5, -1.0])
+    assert np.array_equal(O.fused(ref, bias, "relu"), np.array([[0.5, 0.0], [3.5, 0.0]]))
+    assert np.array_equal(O.fused(ref, bias, "none"), ref + bias)
