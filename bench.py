@@ -46,6 +46,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--epilogue", default="plain", choices=["plain", "bias-gelu", "bias-gelu-e4m3"],
+                    help="fused epilogue to time (gb_gemm_ex): bias + GELU, optionally with amax "
+                         "and a scaled E4M3 output")
     ap.add_argument("--workspace", action="store_true",
                     help="time the workspace entry point (stream-K schedule where it helps)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -283,9 +286,28 @@ def run_gb300(args):
     lda, ldb = data["lda"], data["ldb"]
     cptr = C.data_ptr() if C is not None else None
     ws = G.make_workspace(dev) if args.workspace else None
+    epi = None
+    if args.epilogue != "plain":
+        import ctypes
+        from layout_algebra_gb300._native import Epilogue
+        g = torch.Generator().manual_seed(p.seed + 1)
+        bias = torch.randn(p.N, generator=g).to(A.dtype).to(dev)
+        amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        fp8 = args.epilogue.endswith("e4m3")
+        if fp8:
+            D = torch.empty(p.M * p.N, dtype=torch.float8_e4m3fn, device=dev)
+        epi = Epilogue(bias.data_ptr(), 2, amax.data_ptr() if fp8 else None, 1 if fp8 else 0,
+                       16.0 if fp8 else 1.0)
+        dcode = 1 if A.dtype == torch.bfloat16 else 0
 
     def launch():
-        if ws is not None:
+        if epi is not None:
+            st = G.lib().gb_gemm_ex(dcode, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda,
+                                    G.major_code(p.majorA), B.data_ptr(), ldb, G.major_code(p.majorB),
+                                    p.beta, cptr, D.data_ptr(), ctypes.byref(epi),
+                                    ws.data_ptr() if ws is not None else None,
+                                    ws.numel() if ws is not None else 0, sh)
+        elif ws is not None:
             st = G.raw_call_ws(A.dtype, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda, p.majorA,
                                B.data_ptr(), ldb, p.majorB, p.beta, cptr, D.data_ptr(),
                                ws.data_ptr(), ws.numel(), sh)
@@ -382,6 +404,9 @@ def run_gb300(args):
     }
     line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
                                      if ws is not None else "gb_gemm_%s" % p.dtype)
+    if epi is not None:
+        line["config"]["entry_point"] = "gb_gemm_ex"
+        line["config"]["epilogue"] = args.epilogue
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(p, data, args.cpu_seconds)
         line["cpu_baseline"] = {
