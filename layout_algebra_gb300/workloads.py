@@ -9,7 +9,9 @@ Generation recipe (the same for every problem):
   * draw the LOGICAL A (M x K), then the logical B (K x N), then C (M x N) if present,
     in float32: ``int2`` = integers uniform in {-2..2}; ``uniform`` = U[-1, 1];
     ``normal`` = N(0, sigma) with sigma the standard deviation;
-  * cast once to fp16/bf16 (round to nearest even);
+  * cast once to fp16/bf16 (round to nearest even), or, for FP8 inputs (a_fmt / b_fmt
+    "e4m3" / "e5m2"), cast A and B once to that format with torch's conversion and keep
+    their one-byte codes (C stays in the 16-bit dtype);
   * store in the requested major.  The values never depend on the major:
       A K-major : A[m*lda + k]      A M-major : A[m + k*lda]
       B K-major : B[n*ldb + k]      B N-major : B[k*ldb + n]
@@ -45,6 +47,12 @@ class Problem:
     seed: int = 0
     lda: Optional[int] = None   # None = packed
     ldb: Optional[int] = None
+    a_fmt: Optional[str] = None  # None: A in dtype; "e4m3" | "e5m2": one-byte FP8 codes
+    b_fmt: Optional[str] = None
+
+    @property
+    def in_bytes(self) -> int:
+        return 1 if self.a_fmt else 2
 
     @property
     def flops(self) -> int:
@@ -52,11 +60,9 @@ class Problem:
 
     @property
     def algorithmic_bytes(self) -> int:
-        """A, B, (C) read once and D written once, 2 bytes per element."""
-        e = self.M * self.K + self.K * self.N + self.M * self.N
-        if self.has_c:
-            e += self.M * self.N
-        return 2 * e
+        """A, B (input element size), (C) read once and D written once (2 bytes each)."""
+        cd = self.M * self.N * (2 if self.has_c else 1)
+        return self.in_bytes * (self.M * self.K + self.K * self.N) + 2 * cd
 
     def with_(self, **kw) -> "Problem":
         return replace(self, **kw)
@@ -78,6 +84,15 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# FP8-input problems: E4M3 x E4M3 with bf16 C and D, the square size of the 16-bit headline.
+FP8_WORKLOADS = {
+    "gemm8192_e4m3_bf16_c": Problem("gemm8192_e4m3_bf16_c", 8192, 8192, 8192, "bf16",
+                                    has_c=True, alpha=1.25, beta=0.5, dist="normal",
+                                    sigma=1.0, c_dist="normal", c_sigma=1.0, seed=5,
+                                    a_fmt="e4m3", b_fmt="e4m3"),
+}
+FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
 
 def torch_dtype(name: str) -> torch.dtype:
     return {"f16": torch.float16, "bf16": torch.bfloat16}[name]
@@ -93,6 +108,12 @@ def _draw(g, shape, dist, sigma):
     if dist == "ones":
         return torch.ones(shape, dtype=torch.float32)
     raise ValueError(dist)
+
+
+def _cast(x, dt, fmt):
+    if fmt is None:
+        return x.to(dt)
+    return x.to(FP8_TORCH[fmt]).view(torch.uint8)
 
 
 def leading_dims(p: Problem):
@@ -128,14 +149,17 @@ def store_b(b_logical: torch.Tensor, major: str, ldb: int) -> torch.Tensor:
 def make(p: Problem, logical: bool = False):
     """Host (CPU) operands for problem p.
 
-    Returns a dict with A, B (flat stored 16-bit tensors), lda, ldb, C (flat M*N, or
-    None) and, with logical=True, the logical matrices a (M x K), b (K x N), c (M x N).
+    Returns a dict with A, B (flat stored 16-bit tensors, or uint8 FP8 codes), lda, ldb, C
+    (flat M*N, or None) and, with logical=True, the logical matrices a (M x K), b (K x N),
+    c (M x N).
     """
     g = torch.Generator(device="cpu")
     g.manual_seed(p.seed)
     dt = torch_dtype(p.dtype)
-    a = _draw(g, (p.M, p.K), p.dist, p.sigma).to(dt)
-    b = _draw(g, (p.K, p.N), p.dist, p.sigma).to(dt)
+    if (p.a_fmt or p.b_fmt) and (p.majorA != K_MAJOR or p.majorB != K_MAJOR):
+        raise ValueError("FP8 operands are K-major")
+    a = _cast(_draw(g, (p.M, p.K), p.dist, p.sigma), dt, p.a_fmt)
+    b = _cast(_draw(g, (p.K, p.N), p.dist, p.sigma), dt, p.b_fmt)
     c = _draw(g, (p.M, p.N), p.c_dist, p.c_sigma).to(dt) if p.has_c else None
     lda, ldb = leading_dims(p)
     out = {
@@ -151,6 +175,10 @@ def make(p: Problem, logical: bool = False):
 
 
 def bits(t: torch.Tensor):
-    """Raw 16-bit patterns of a CPU fp16/bf16 tensor as a numpy uint16 array."""
+    """Raw codes of a CPU tensor as a numpy uint16 array: the 16-bit patterns of fp16/bf16,
+    or one-byte FP8 codes (uint8 / float8) widened to 16 bits."""
     import numpy as np
-    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    t = t.contiguous()
+    if t.element_size() == 1:
+        return t.view(torch.uint8).numpy().astype(np.uint16)
+    return t.view(torch.int16).numpy().view(np.uint16)

@@ -208,7 +208,11 @@ static uint16_t b_at(const uint16_t* B, int64_t ldb, int majorB, int64_t k, int6
 }
 
 /*
- * Reference values for a set of output entries.
+ * Reference values for a set of output entries, each operand in its own format.
+ *   dtA, dtB, dtC: ORACLE_F16 / ORACLE_BF16 / ORACLE_E4M3 / ORACLE_E5M2 codes, one per
+ *              operand (FP8 operands are one-byte codes widened to 16 bits).  The tensor
+ *              cores take FP8 operands with a 16-bit C and D ("CUTLASS, in depth", sections
+ *              "Epilogue fusion" and "Numerics"); the definition of D does not change.
  *   rows/cols: n entries (i, j).  When rows == NULL the entries are all M*N outputs in
  *              row-major order (n is then ignored).
  *   ref[e]   : alpha * sum_k a(i,k) b(k,j) + beta * c(i,j)   (beta*c skipped if beta == 0)
@@ -216,12 +220,12 @@ static uint16_t b_at(const uint16_t* B, int64_t ldb, int majorB, int64_t k, int6
  *   C may be NULL when beta == 0.
  * Returns 0, or -1 on an invalid argument.
  */
-int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
-                const uint16_t* A, int64_t lda, int majorA,
-                const uint16_t* B, int64_t ldb, int majorB,
-                double beta, const uint16_t* C, int64_t ldc, int dtype,
-                const int64_t* rows, const int64_t* cols, int64_t n,
-                double* ref, double* sumabs, int nthreads) {
+int oracle_gemm_typed(int64_t M, int64_t N, int64_t K, double alpha,
+                      const uint16_t* A, int64_t lda, int majorA, int dtA,
+                      const uint16_t* B, int64_t ldb, int majorB, int dtB,
+                      double beta, const uint16_t* C, int64_t ldc, int dtC,
+                      const int64_t* rows, const int64_t* cols, int64_t n,
+                      double* ref, double* sumabs, int nthreads) {
     if (M < 0 || N < 0 || K < 0) return -1;
     if (beta != 0.0 && C == NULL) return -1;
     int64_t total = rows ? n : M * N;
@@ -236,17 +240,28 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
         int64_t j = rows ? cols[e] : e % (N ? N : 1);
         double acc = 0.0, mag = 0.0;
         for (int64_t k = 0; k < K; ++k) {
-            double prod = decode(dtype, a_at(A, lda, majorA, i, k)) *
-                          decode(dtype, b_at(B, ldb, majorB, k, j));
+            double prod = decode(dtA, a_at(A, lda, majorA, i, k)) *
+                          decode(dtB, b_at(B, ldb, majorB, k, j));
             acc += prod;
             mag += fabs(prod);
         }
         double r = alpha * acc;
-        if (beta != 0.0) r += beta * decode(dtype, C[i * ldc + j]);
+        if (beta != 0.0) r += beta * decode(dtC, C[i * ldc + j]);
         ref[e] = r;
         if (sumabs) sumabs[e] = mag;
     }
     return 0;
+}
+
+/* All three operands in one format `dtype`. */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
+                const uint16_t* A, int64_t lda, int majorA,
+                const uint16_t* B, int64_t ldb, int majorB,
+                double beta, const uint16_t* C, int64_t ldc, int dtype,
+                const int64_t* rows, const int64_t* cols, int64_t n,
+                double* ref, double* sumabs, int nthreads) {
+    return oracle_gemm_typed(M, N, K, alpha, A, lda, majorA, dtype, B, ldb, majorB, dtype,
+                             beta, C, ldc, dtype, rows, cols, n, ref, sumabs, nthreads);
 }
 
 int oracle_max_threads(void) {

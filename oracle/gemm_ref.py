@@ -36,6 +36,10 @@ def _load():
         lib.oracle_gemm.argtypes = [i64, i64, i64, dbl, vp, i64, ctypes.c_int, vp, i64,
                                     ctypes.c_int, dbl, vp, i64, ctypes.c_int, vp, vp, i64,
                                     vp, vp, ctypes.c_int]
+        ci = ctypes.c_int
+        lib.oracle_gemm_typed.restype = ci
+        lib.oracle_gemm_typed.argtypes = [i64, i64, i64, dbl, vp, i64, ci, ci, vp, i64, ci, ci,
+                                          dbl, vp, i64, ci, vp, vp, i64, vp, vp, ci]
         lib.oracle_decode.restype = None
         lib.oracle_decode.argtypes = [ctypes.c_int, vp, i64, vp]
         lib.oracle_round.restype = None
@@ -46,7 +50,8 @@ def _load():
 
 
 def dtype_code(name):
-    return {"f16": F16, "fp16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16}[name]
+    return {"f16": F16, "fp16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16,
+            "e4m3": E4M3, "e5m2": E5M2}[name]
 
 
 def _bits(arr):
@@ -77,13 +82,17 @@ def max_threads():
 
 
 def gemm(M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, ldc, dtype,
-         rows=None, cols=None, threads=0):
+         rows=None, cols=None, threads=0, a_dtype=None, b_dtype=None):
     """fp64 reference outputs and sum_k |a b| for the requested entries.
 
     A, B, C are flat uint16 arrays holding the stored operands (C may be None when
-    beta == 0).  With rows/cols None every output is returned as an (M, N) array;
-    otherwise 1-D arrays for the entries (rows[e], cols[e]).
+    beta == 0); FP8 operands are their one-byte codes widened to uint16.  dtype is the
+    format of C (and of A and B unless a_dtype / b_dtype name theirs).  With rows/cols None
+    every output is returned as an (M, N) array; otherwise 1-D arrays for the entries
+    (rows[e], cols[e]).
     """
+    dtA = dtype if a_dtype is None else a_dtype
+    dtB = dtype if b_dtype is None else b_dtype
     A = _bits(A)
     B = _bits(B)
     Cp = None
@@ -100,9 +109,10 @@ def gemm(M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, ldc, dtype,
         r_p, c_p = rows.ctypes.data, cols.ctypes.data
     ref = np.empty(n, dtype=np.float64)
     sab = np.empty(n, dtype=np.float64)
-    rc = _load().oracle_gemm(M, N, K, float(alpha), A.ctypes.data, lda, majorA,
-                             B.ctypes.data, ldb, majorB, float(beta), Cp, ldc, dtype,
-                             r_p, c_p, n, ref.ctypes.data, sab.ctypes.data, threads)
+    rc = _load().oracle_gemm_typed(M, N, K, float(alpha), A.ctypes.data, lda, majorA, dtA,
+                                   B.ctypes.data, ldb, majorB, dtB, float(beta), Cp, ldc,
+                                   dtype, r_p, c_p, n, ref.ctypes.data, sab.ctypes.data,
+                                   threads)
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
     if rows is None:

@@ -67,3 +67,54 @@ def test_fused_bias_then_activation():
     bias = np.array([1.5, -1.0])
     assert np.array_equal(O.fused(ref, bias, "relu"), np.array([[0.5, 0.0], [3.5, 0.0]]))
     assert np.array_equal(O.fused(ref, bias, "none"), ref + bias)
+
+
+def _fp8_codes(rng, n, code):
+    """Random finite FP8 codes (NaN codes excluded; E5M2 infinities excluded)."""
+    c = rng.integers(0, 256, n).astype(np.uint16)
+    if code == O.E4M3:
+        bad = (c & 0x7F) == 0x7F
+    else:
+        bad = (c & 0x7C) == 0x7C
+    c[bad] &= 0x83          # a small finite value of the same sign instead
+    return c
+
+
+def _torch_decode(code, c):
+    tdt = torch.float8_e4m3fn if code == O.E4M3 else torch.float8_e5m2
+    return torch.from_numpy(c.astype(np.uint8)).view(tdt).double().numpy()
+
+
+@pytest.mark.parametrize("fa,fb", [(O.E4M3, O.E5M2), (O.E5M2, O.E4M3), (O.E4M3, O.E4M3)])
+def test_typed_gemm_against_library_matmul(fa, fb):
+    # Decoding by torch's own FP8 types and a float64 matmul (a library routine) is
+    # independent of the oracle's decoders and loop; a swapped A/B format fails it.
+    rng = np.random.default_rng(7 + fa + 2 * fb)
+    M, N, K = 9, 11, 37
+    A = _fp8_codes(rng, M * K, fa)          # K-major: A[i*K + k]
+    B = _fp8_codes(rng, N * K, fb)          # K-major: B[j*K + k]
+    C = O.round_to(O.BF16, rng.standard_normal(M * N))
+    a = _torch_decode(fa, A).reshape(M, K)
+    b = _torch_decode(fb, B).reshape(N, K).T
+    want = 0.75 * (a @ b) + 0.5 * O.decode(O.BF16, C).reshape(M, N)
+    ref, sab = O.gemm(M, N, K, 0.75, A, K, O.K_MAJOR, B, K, O.K_MAJOR, 0.5, C, N, O.BF16,
+                      a_dtype=fa, b_dtype=fb)
+    assert np.allclose(ref, want, rtol=0, atol=1e-12 * (np.max(sab) + 1.0))
+    assert np.allclose(sab, np.abs(a) @ np.abs(b), rtol=1e-13)
+    if fa != fb:
+        swapped, _ = O.gemm(M, N, K, 0.75, A, K, O.K_MAJOR, B, K, O.K_MAJOR, 0.5, C, N, O.BF16,
+                            a_dtype=fb, b_dtype=fa)
+        assert not np.allclose(swapped, want)
+
+
+def test_typed_gemm_integer_exact():
+    # integers -2..2 are exact in both FP8 formats: the result is an integer matmul
+    rng = np.random.default_rng(11)
+    M, N, K = 6, 5, 40
+    ai = rng.integers(-2, 3, (M, K))
+    bi = rng.integers(-2, 3, (K, N))
+    A = O.round_to(O.E4M3, ai.astype(np.float64).ravel())
+    B = O.round_to(O.E5M2, bi.T.astype(np.float64).ravel())
+    ref, _ = O.gemm(M, N, K, 1.0, A, K, O.K_MAJOR, B, K, O.K_MAJOR, 0.0, None, N, O.F16,
+                    a_dtype=O.E4M3, b_dtype=O.E5M2)
+    assert np.array_equal(ref, (ai @ bi).astype(np.float64))
