@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (2MNK/s) at 8192^3 fp16->fp32 acc; % of GB300 dense FP16 peak"
 DEFAULT_WORKLOAD = "gemm8192_bf16_c"
+METRIC_FP8 = "GEMM TFLOP/s (2MNK/s) at 8192^3 e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/ptx.cuh"]
 
@@ -187,6 +188,8 @@ def oracle_sample(problem, data, seconds, max_rows=None):
     A, B = W.bits(data["A"]), W.bits(data["B"])
     C = W.bits(data["C"]) if data["C"] is not None else None
     code = O.dtype_code(p.dtype)
+    a_code = O.dtype_code(p.a_fmt) if p.a_fmt else code
+    b_code = O.dtype_code(p.b_fmt) if p.b_fmt else code
     ma = 0 if p.majorA == "K" else 1
     mb = 0 if p.majorB == "K" else 1
     threads = O.max_threads()
@@ -197,7 +200,7 @@ def oracle_sample(problem, data, seconds, max_rows=None):
         cols = np.tile(cols_all[:ncols], nrows)
         t = time.perf_counter()
         O.gemm(p.M, p.N, p.K, p.alpha, A, data["lda"], ma, B, data["ldb"], mb, p.beta, C, p.N,
-               code, rows, cols, threads=threads)
+               code, rows, cols, threads=threads, a_dtype=a_code, b_dtype=b_code)
         return time.perf_counter() - t
 
     # probe with a slice of one row, then size the sample to the time budget
@@ -226,7 +229,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from layout_algebra_gb300 import workloads as W
-    p = W.WORKLOADS[args.workload]
+    p = problem_of(args.workload)
     data = W.make(p)
     total_budget = args.ref_seconds
     per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
@@ -240,7 +243,7 @@ def run_reference(args):
         secs += last["seconds"]
     value = flops / secs / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_FP8 if p.a_fmt else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(p),
@@ -254,13 +257,23 @@ def run_reference(args):
     return 0
 
 
+def problem_of(name):
+    from layout_algebra_gb300 import workloads as W
+    if name in W.FP8_WORKLOADS:
+        return W.FP8_WORKLOADS[name]
+    return W.WORKLOADS[name]
+
+
 def workload_config(p):
-    return {"workload": p.name, "M": p.M, "N": p.N, "K": p.K, "operand_dtype": p.dtype,
+    cfg = {"workload": p.name, "M": p.M, "N": p.N, "K": p.K, "operand_dtype": p.dtype,
             "majorA": p.majorA, "majorB": p.majorB, "alpha": p.alpha, "beta": p.beta,
             "has_C": p.has_c, "values": p.dist, "seed": p.seed,
             "l2": "inputs larger than L2 (no flush between steps)"
             if p.algorithmic_bytes > 256 * 2**20 else "working set may fit in L2",
             "parallelism": "replicas"}
+    if p.a_fmt:
+        cfg["operand_dtype"] = "%s x %s inputs, %s C and D" % (p.a_fmt, p.b_fmt, p.dtype)
+    return cfg
 
 
 def run_gb300(args):
@@ -276,32 +289,41 @@ def run_gb300(args):
 
     from layout_algebra_gb300 import binding as G
     from layout_algebra_gb300 import workloads as W
-    p = W.WORKLOADS[args.workload]
+    p = problem_of(args.workload)
+    f8 = p.a_fmt is not None
+    out_dt = W.torch_dtype(p.dtype)
     data = W.make(p)
     A, B = data["A"].to(dev), data["B"].to(dev)
     C = data["C"].to(dev) if data["C"] is not None else None
-    D = torch.empty(p.M * p.N, dtype=A.dtype, device=dev)
+    D = torch.empty(p.M * p.N, dtype=out_dt, device=dev)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     lda, ldb = data["lda"], data["ldb"]
     cptr = C.data_ptr() if C is not None else None
     ws = G.make_workspace(dev) if args.workspace else None
+    import ctypes
     epi = None
     if args.epilogue != "plain":
-        import ctypes
         from layout_algebra_gb300._native import Epilogue
         g = torch.Generator().manual_seed(p.seed + 1)
-        bias = torch.randn(p.N, generator=g).to(A.dtype).to(dev)
+        bias = torch.randn(p.N, generator=g).to(out_dt).to(dev)
         amax = torch.zeros(1, dtype=torch.float32, device=dev)
         fp8 = args.epilogue.endswith("e4m3")
         if fp8:
             D = torch.empty(p.M * p.N, dtype=torch.float8_e4m3fn, device=dev)
         epi = Epilogue(bias.data_ptr(), 2, amax.data_ptr() if fp8 else None, 1 if fp8 else 0,
                        16.0 if fp8 else 1.0)
-        dcode = 1 if A.dtype == torch.bfloat16 else 0
+    dcode = 1 if out_dt == torch.bfloat16 else 0
 
     def launch():
-        if epi is not None:
+        if f8:
+            st = G.lib().gb_gemm_fp8(G.fp8_format(p.a_fmt), G.fp8_format(p.b_fmt), dcode, p.M, p.N,
+                                     p.K, p.alpha, A.data_ptr(), lda, B.data_ptr(), ldb, p.beta,
+                                     cptr, D.data_ptr(),
+                                     ctypes.byref(epi) if epi is not None else None,
+                                     ws.data_ptr() if ws is not None else None,
+                                     ws.numel() if ws is not None else 0, sh)
+        elif epi is not None:
             st = G.lib().gb_gemm_ex(dcode, p.M, p.N, p.K, p.alpha, A.data_ptr(), lda,
                                     G.major_code(p.majorA), B.data_ptr(), ldb, G.major_code(p.majorB),
                                     p.beta, cptr, D.data_ptr(), ctypes.byref(epi),
@@ -355,10 +377,19 @@ def run_gb300(args):
     # end to end through the public API with pinned host buffers
     A_h, B_h = data["A"].pin_memory(), data["B"].pin_memory()
     C_h = data["C"].pin_memory() if data["C"] is not None else None
-    D_h = torch.empty(p.M * p.N, dtype=A.dtype, pin_memory=True)
+    D_h = torch.empty(p.M * p.N, dtype=out_dt, pin_memory=True)
+
+    def public_call():
+        if f8:
+            G.gemm_fp8(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, a_format=p.a_fmt,
+                       b_format=p.b_fmt, out_dtype=out_dt, alpha=p.alpha, beta=p.beta, C=C_h,
+                       D=D_h, workspace=ws)
+        else:
+            G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
+                   alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
+
     for _ in range(2):
-        G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
-               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
+        public_call()
     torch.cuda.synchronize()
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
     barrier(world, local)
@@ -367,36 +398,41 @@ def run_gb300(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
-               alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
+        public_call()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world, local)
     e2e_s, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, float(p.flops) * e2e_steps, world, dev)
-    h2d = (data["A"].numel() + data["B"].numel() + (data["C"].numel() if data["C"] is not None else 0)) * 2
+    h2d = sum(t.numel() * t.element_size() for t in (data["A"], data["B"], data["C"]) if t is not None)
     d2h = p.M * p.N * 2
     st, detail = G.last_device_status()
     if st != 0:
         raise RuntimeError("device status %d (%#x) in the end-to-end region" % (st, detail))
 
     peaks, peak_src = load_peaks()
-    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # an FP8 contraction runs at twice the 16-bit tensor rate (nominal 4.5 vs 2.25 PFLOP/s
+    # dense): its peak is the measured bf16 peak times that ratio
+    ratio = 2.0 if f8 else 1.0
+    burst = ratio * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = ratio * float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     achieved = p.flops / (kernel_ms / 1e3) / 1e12
     traffic = load_traffic(p.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
                 "frac": achieved / burst, "traffic": traffic,
-                "peak_source": "%s burst (MEASURED_PEAKS.json bf16_tflops); fp16 and bf16 share the rate"
+                "peak_source": ("%s burst (MEASURED_PEAKS.json bf16_tflops) x 2, the nominal FP8:bf16 "
+                                "dense ratio" if f8 else
+                                "%s burst (MEASURED_PEAKS.json bf16_tflops); fp16 and bf16 share the rate")
                                % peak_src,
-                "frac_of_sustained": achieved / sustained, "frac_of_nominal_2250": achieved / 2250.0,
+                "frac_of_sustained": achieved / sustained,
+                "frac_of_nominal": achieved / (2250.0 * ratio),
                 "kernel": "gb::gemm_kernel", "kernel_ms": kernel_ms,
                 "algorithmic_flops_per_launch": p.flops,
                 "algorithmic_bytes_per_launch": p.algorithmic_bytes}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC_FP8 if f8 else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": p.dtype, "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": p.a_fmt if f8 else p.dtype, "data": "synthetic",
         "config": workload_config(p),
         "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -404,7 +440,9 @@ def run_gb300(args):
     }
     line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
                                      if ws is not None else "gb_gemm_%s" % p.dtype)
-    if epi is not None:
+    if f8:
+        line["config"]["entry_point"] = "gb_gemm_fp8" + (" (workspace)" if ws is not None else "")
+    elif epi is not None:
         line["config"]["entry_point"] = "gb_gemm_ex"
         line["config"]["epilogue"] = args.epilogue
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

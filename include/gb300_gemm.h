@@ -134,6 +134,27 @@ gb_status gb_gemm_ex(int dtype, int64_t M, int64_t N, int64_t K, float alpha,
                      float beta, const void* C, void* D, const gb_epilogue* epi,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* GEMM with 8-bit floating-point inputs ("CUTLASS, in depth" — "Epilogue fusion" and
+   "Numerics": the tensor cores take FP8 operands; FP8 data carries a scale factor, and a
+   GEMM without the right scales overflows).  Computes, in fp32 on the tensor cores,
+     D = epilogue(alpha * A*B + beta*C)
+   where A (M x K) and B (K x N) hold FP8 codes: a_format / b_format are GB_FP8_E4M3 (OCP
+   E4M3: no infinities, largest finite 448) or GB_FP8_E5M2 (OCP E5M2), one byte each, and
+   may differ.  Both operands are K-major: A row-major with leading dimension lda, B stored
+   as its transpose (N rows of K, leading dimension ldb); lda and ldb are multiples of 16
+   elements and A, B are 16-byte aligned.  Per-tensor scale factors are folded into alpha
+   by the caller (alpha = alpha' * scale_A * scale_B for dequantised operands
+   scale_A * A, scale_B * B).  C, D and the bias are of out_dtype (GB_F16 or GB_BF16), laid
+   out as for gb_gemm_f16; epi, workspace and stream as for gb_gemm_ex (an FP8 output via
+   epi->out_format gives an FP8-in, FP8-out GEMM).  Errors as for gb_gemm_ex, plus
+   GB_ERR_INVALID_ARG for an unknown format or out_dtype and GB_ERR_MISALIGNED for lda or
+   ldb not a multiple of 16. */
+typedef enum { GB_FP8_E4M3 = 0, GB_FP8_E5M2 = 1 } gb_fp8_format;
+gb_status gb_gemm_fp8(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K,
+                      float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                      float beta, const void* C, void* D, const gb_epilogue* epi,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Allocation-free GEMM (no counterpart on the pages: an addition for callers that may not
    allocate device memory).  Some callers cannot call cudaMalloc at the point where they
    run a GEMM: code inside a runtime that owns every byte of device memory (a serving

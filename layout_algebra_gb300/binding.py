@@ -120,6 +120,61 @@ def gemm_fused(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, be
     return D
 
 
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def fp8_format(x):
+    if x in FP8_FORMATS:
+        return FP8_FORMATS[x]
+    if x == torch.float8_e4m3fn:
+        return 0
+    if x == torch.float8_e5m2:
+        return 1
+    raise TypeError("FP8 operands must be e4m3 (float8_e4m3fn) or e5m2 (float8_e5m2)")
+
+
+def gemm_fp8(A, B, M, N, K, *, lda, ldb, a_format=None, b_format=None, out_dtype=torch.bfloat16,
+             alpha=1.0, beta=0.0, C=None, bias=None, activation="none", amax=None,
+             out_format="input", out_scale=1.0, D=None, workspace=None, stream=None):
+    """D = epilogue(alpha*A@B + beta*C) with FP8 inputs through gb_gemm_fp8.
+
+    A (M x K, leading dimension lda) and B (stored as N rows of K, leading dimension ldb) are
+    K-major byte tensors: float8_e4m3fn / float8_e5m2, or uint8 codes with a_format /
+    b_format naming the format.  C, D and bias are of out_dtype; per-tensor scales belong in
+    alpha.  out_format "e4m3"/"e5m2" gives a float8 D.  Host operands are staged to the
+    device and D (a host tensor, pinned if given so) receives the result, as for ``gemm``.
+    """
+    fa = fp8_format(a_format if a_format is not None else A.dtype)
+    fb = fp8_format(b_format if b_format is not None else B.dtype)
+    od = dtype_code(out_dtype)
+    fmt = OUT_FORMATS[out_format]
+    dd = {0: out_dtype, 1: torch.float8_e4m3fn, 2: torch.float8_e5m2}[fmt]
+    host = not A.is_cuda
+    D_h = None
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        A = A.to(dev, non_blocking=True)
+        B = B.to(dev, non_blocking=True)
+        C = C.to(dev, non_blocking=True) if C is not None else None
+        bias = bias.to(dev, non_blocking=True) if bias is not None else None
+        D_h, D = D, torch.empty(M * N, dtype=dd, device=dev)
+    elif D is None:
+        D = torch.empty(M * N, dtype=dd, device=A.device)
+    epi = Epilogue(_ptr(bias), ACTIVATIONS[activation], _ptr(amax), fmt, float(out_scale))
+    st = lib().gb_gemm_fp8(fa, fb, od, M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                           float(beta), _ptr(C), _ptr(D), ctypes.byref(epi), _ptr(workspace),
+                           0 if workspace is None else workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream))
+    if st != 0:
+        raise GemmError(st, "gemm_fp8")
+    if host:
+        if D_h is None:
+            D_h = torch.empty(M * N, dtype=dd, pin_memory=True)
+        D_h.copy_(D, non_blocking=True)
+        return D_h
+    return D
+
+
 def raw_call(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta, C_ptr, D_ptr,
              stream_handle):
     """Direct C-ABI call with integer pointers; returns the status code."""

@@ -115,6 +115,7 @@ struct Params {
   int32_t out_fmt;            // 0 same 16-bit type as the inputs, 1 FP8 E4M3, 2 FP8 E5M2
   float out_scale;
   int32_t vec8_ok;            // 16-byte FP8 stores legal (N % 16 == 0)
+  int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
 };
 
 // Slot of CTA (cluster c, rank r) in the stream-K workspace.
@@ -302,12 +303,14 @@ __device__ __forceinline__ int64_t d_offset(const Params& p, int32_t mt, int32_t
 // 64 (K) x rows.  MN-major: rows/64 boxes of 64 (M or N) x 64 (K), 8 KiB each, back to back.
 template <bool kPair>
 __device__ __forceinline__ void issue_operand(int major, const void* tm, uint32_t dst, uint32_t bar,
-                                              int32_t row0, int rows, int32_t kb) {
+                                              int32_t row0, int rows, int32_t kb, int32_t bk_elems) {
   if (major == 0) {
+    // a K-major k-block is one 128-byte swizzle row per operand row: 64 16-bit or 128
+    // 8-bit elements
     if constexpr (kPair)
-      tma_load_2d_pair(dst, tm, bar, kb * kBK, row0);
+      tma_load_2d_pair(dst, tm, bar, kb * bk_elems, row0);
     else
-      tma_load_2d(dst, tm, bar, kb * kBK, row0);
+      tma_load_2d(dst, tm, bar, kb * bk_elems, row0);
   } else {
     for (int j = 0; j < rows / kSwz; ++j) {
       if constexpr (kPair)
@@ -361,9 +364,10 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         if (!kPair || rank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
-          issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb);
+          issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
+                               p.bk_elems);
           issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf, full_tgt, b_row0,
-                               C::kRowsB, kb);
+                               C::kRowsB, kb, p.bk_elems);
         }
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -397,7 +401,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   }
 }
 
-template <bool kPair>
+template <bool kPair, bool kF8>
 __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
                         uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair>;
@@ -439,8 +443,13 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
           const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
           const uint64_t db = db0 + ((h * C::kBHalf) >> 4) + k * kb_;
           const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
-          if constexpr (kPair)
+          // one instruction covers 32 bytes of K: 16 16-bit or 32 8-bit elements
+          if constexpr (kPair && kF8)
+            tc_mma_f8_pair(d_tmem, da, db, p.idesc, acc);
+          else if constexpr (kPair)
             tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
+          else if constexpr (kF8)
+            tc_mma_f8(d_tmem, da, db, p.idesc, acc);
           else
             tc_mma_f16(d_tmem, da, db, p.idesc, acc);
         }
@@ -736,7 +745,7 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <bool kBF16, bool kPair>
+template <bool kBF16, bool kPair, bool kF8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
@@ -787,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) run_producer<kPair>(p, &tmA, &tmB, smem, ctl, rank, cluster, nclusters);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<kPair>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
+    if (lane == 0) run_mma<kPair, kF8>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
     run_epilogue<kBF16, kPair>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
@@ -837,7 +846,7 @@ __global__ void __launch_bounds__(32, 1)
     const uint32_t full = smem_addr(&ctl->full[0]);
     mbar_arrive_expect_tx(full, bytes);
     issue_operand<false>(which == 0 ? p.majorA : p.majorB, &tm, smem_addr(smem), full, tile * rows,
-                         rows, kb);
+                         rows, kb, p.bk_elems);
     wait_drain(full, 0u, p.timeout_ns);
   }
   __syncthreads();
@@ -865,8 +874,8 @@ constexpr int kVariantPair = 2;
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
-  bool attr_single[2] = {false, false};
-  bool attr_pair[2] = {false, false};
+  bool attr_single[2][2] = {{false, false}, {false, false}};   // [bf16 out][fp8 in]
+  bool attr_pair[2][2] = {{false, false}, {false, false}};
   int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
@@ -895,10 +904,22 @@ struct OperandPlan {
   int64_t grid_rows, k_blocks;
 };
 
+// Input element type: 16-bit (fp16/bf16) or 8-bit (E4M3/E5M2).  A 128-byte swizzle row holds
+// 128 / bytes elements, which sets the K extent of a k-block.
+struct InType {
+  int a_fmt, b_fmt;   // instruction-descriptor formats: 0 fp16 / E4M3, 1 bf16 / E5M2
+  bool f8;
+  int bytes;          // 2 or 1
+  int bk() const { return 128 / bytes; }
+};
+
+InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false, 2}; }
+
 gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t tile_rows,
-                       int64_t cta_rows, OperandPlan* o) {
+                       int64_t cta_rows, OperandPlan* o, const InType& in) {
+  if (in.f8 && major != GB_K_MAJOR) return GB_ERR_INVALID_ARG;   // 8-bit operands: K-major only
   la::Layout m = major == GB_K_MAJOR ? la::make_layout({rows, K}, {ld, 1}) : la::make_layout({rows, K}, {1, ld});
-  la::Layout z = la::zipped_divide(m, la::tiler_of({tile_rows, gb::kBK}));
+  la::Layout z = la::zipped_divide(m, la::tiler_of({tile_rows, in.bk()}));
   auto grid = la::flatten(z.mode(1).shape);   // (row tiles, k-blocks)
   o->grid_rows = grid[0];
   o->k_blocks = grid[1];
@@ -907,14 +928,14 @@ gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t t
   if (s_k == 1 && major == GB_K_MAJOR) {
     o->dim[0] = K;
     o->dim[1] = rows;
-    o->row_bytes = s_rows * 2;
-    o->box[0] = gb::kSwz;
+    o->row_bytes = s_rows * in.bytes;
+    o->box[0] = in.bk();
     o->box[1] = cta_rows;
     o->boxes = 1;
   } else if (s_rows == 1) {
     o->dim[0] = rows;
     o->dim[1] = K;
-    o->row_bytes = s_k * 2;
+    o->row_bytes = s_k * in.bytes;
     o->box[0] = gb::kSwz;
     o->box[1] = gb::kBK;
     o->boxes = cta_rows / gb::kSwz;
@@ -925,7 +946,7 @@ gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t t
 }
 
 gb_status validate_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int majorA, int64_t ldb,
-                         int majorB) {
+                         int majorB, int bytes = 2) {
   if (M < 0 || N < 0 || K < 0) return GB_ERR_INVALID_ARG;
   if (majorA != GB_K_MAJOR && majorA != GB_MN_MAJOR) return GB_ERR_INVALID_ARG;
   if (majorB != GB_K_MAJOR && majorB != GB_MN_MAJOR) return GB_ERR_INVALID_ARG;
@@ -934,17 +955,17 @@ gb_status validate_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int major
   if (K > 0 && M > 0 && N > 0) {
     if (lda < (majorA == GB_K_MAJOR ? K : M)) return GB_ERR_INVALID_ARG;
     if (ldb < (majorB == GB_K_MAJOR ? K : N)) return GB_ERR_INVALID_ARG;
-    if ((lda * 2) % 16 != 0 || (ldb * 2) % 16 != 0) return GB_ERR_MISALIGNED;
-    if (lda * 2 >= (int64_t(1) << 40) || ldb * 2 >= (int64_t(1) << 40)) return GB_ERR_INVALID_ARG;
+    if ((lda * bytes) % 16 != 0 || (ldb * bytes) % 16 != 0) return GB_ERR_MISALIGNED;
+    if (lda * bytes >= (int64_t(1) << 40) || ldb * bytes >= (int64_t(1) << 40)) return GB_ERR_INVALID_ARG;
   }
   return GB_OK;
 }
 
-uint32_t make_idesc(int dtype, int majorA, int majorB, int tile_m) {
+uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m) {
   uint32_t d = 0;
   d |= 1u << 4;                                        // accumulator format: fp32
-  d |= static_cast<uint32_t>(dtype == GB_BF16) << 7;   // A format: 0 fp16, 1 bf16
-  d |= static_cast<uint32_t>(dtype == GB_BF16) << 10;  // B format
+  d |= static_cast<uint32_t>(in.a_fmt) << 7;           // A format: 0 fp16/E4M3, 1 bf16/E5M2
+  d |= static_cast<uint32_t>(in.b_fmt) << 10;          // B format
   d |= static_cast<uint32_t>(majorA) << 15;            // A: 0 K-major, 1 MN-major
   d |= static_cast<uint32_t>(majorB) << 16;            // B: 0 K-major, 1 MN-major
   d |= static_cast<uint32_t>(gb::kBN >> 3) << 17;      // N / 8
@@ -963,8 +984,9 @@ int choose_variant(int64_t M) {
 }
 
 gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
-                    int64_t ldb, int majorB, gb_gemm_plan* pl) {
-  gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB);
+                    int64_t ldb, int majorB, gb_gemm_plan* pl, const InType* in_override = nullptr) {
+  const InType in = in_override ? *in_override : in16(dtype);
+  gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB, in.bytes);
   if (st != GB_OK) return st;
   if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
   if (variant != kVariantSingle && variant != kVariantPair) return GB_ERR_INVALID_ARG;
@@ -975,7 +997,7 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   pl->variant = variant;
   pl->tile_m = tile_m;
   pl->tile_n = gb::kBN;
-  pl->tile_k = gb::kBK;
+  pl->tile_k = in.bk();
   if (M == 0 || N == 0) return GB_OK;
   try {
     // D (and C): (M,N):(N,1) divided into (tile_m, 256) tiles -> ((tile),(grid))
@@ -993,8 +1015,8 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
     pl->vector_epilogue = (pl->d_elem_stride[1] == 1 && N % 8 == 0) ? 1 : 0;
     if (K > 0) {
       OperandPlan a, b;
-      if ((st = plan_operand(M, K, lda, majorA, tile_m, gb::kRowsA, &a)) != GB_OK) return st;
-      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, rows_b, &b)) != GB_OK) return st;
+      if ((st = plan_operand(M, K, lda, majorA, tile_m, gb::kRowsA, &a, in)) != GB_OK) return st;
+      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, rows_b, &b, in)) != GB_OK) return st;
       if (a.grid_rows != pl->m_tiles || b.grid_rows != pl->n_tiles || a.k_blocks != b.k_blocks)
         return GB_ERR_INVALID_ARG;
       pl->k_blocks = a.k_blocks;
@@ -1014,21 +1036,24 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   } catch (const la::Error&) {
     return GB_ERR_INVALID_ARG;
   }
-  pl->instr_desc = make_idesc(dtype, majorA, majorB, static_cast<int>(tile_m));
+  pl->instr_desc = make_idesc(in, majorA, majorB, static_cast<int>(tile_m));
   return GB_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
-                     const int64_t box[2], int dtype) {
+                     const int64_t box[2], int dtype, bool f8 = false) {
   auto fn = encode_fn();
   if (!fn) return GB_ERR_LAUNCH;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(dim[0]), static_cast<cuuint64_t>(dim[1])};
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
   cuuint32_t bdim[2] = {static_cast<cuuint32_t>(box[0]), static_cast<cuuint32_t>(box[1])};
   cuuint32_t estride[2] = {1, 1};
-  CUresult r = fn(map, dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  const CUtensorMapDataType t = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : (dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUresult r = fn(map, t,
                   2, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1066,6 +1091,7 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
   const int kkb = pl.variant == kVariantPair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
   p->nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   p->dp_tiles = p->num_tiles;   // data-parallel unless the caller sets up stream-K
+  p->bk_elems = 64;             // 16-bit inputs; 8-bit inputs set 128
   p->majorA = majorA;
   p->majorB = majorB;
   p->alpha = alpha;
@@ -1084,28 +1110,28 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
   p->skip_kb = g_skip_kb;
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kF8>
 gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                         int grid, cudaStream_t s) {
   using C = gb::Cfg<false>;
-  if (!dev->attr_single[kBF16]) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!dev->attr_single[kBF16][kF8]) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    dev->attr_single[kBF16] = true;
+    dev->attr_single[kBF16][kF8] = true;
   }
-  gb::gemm_kernel<kBF16, false><<<grid, gb::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  gb::gemm_kernel<kBF16, false, kF8><<<grid, gb::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kF8>
 gb_status prepare_pair(DeviceState* dev) {
   using C = gb::Cfg<true>;
-  if (!dev->attr_pair[kBF16]) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!dev->attr_pair[kBF16][kF8]) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    dev->attr_pair[kBF16] = true;
+    dev->attr_pair[kBF16][kF8] = true;
   }
   if (dev->pair_clusters == 0) {
     // a persistent grid must fit at once: ask how many pairs can be resident together
@@ -1121,14 +1147,14 @@ gb_status prepare_pair(DeviceState* dev) {
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(2 * (dev->sms / 2), 1, 1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kF8>, &cfg) != cudaSuccess || n <= 0)
       n = dev->sms / 2;
     dev->pair_clusters = std::min(n, dev->sms / 2);
   }
   return GB_OK;
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kF8>
 gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
                       int clusters, cudaStream_t s) {
   using C = gb::Cfg<true>;
@@ -1144,7 +1170,8 @@ gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMa
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true>, tmA, tmB, p) != cudaSuccess) return GB_ERR_LAUNCH;
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kF8>, tmA, tmB, p) != cudaSuccess)
+    return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
@@ -1157,9 +1184,13 @@ int64_t workspace_bytes_for(int sms) {
 
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
-                     void* workspace, size_t workspace_size, void* stream, const gb_epilogue* epi = nullptr) {
+                     void* workspace, size_t workspace_size, void* stream, const gb_epilogue* epi = nullptr,
+                     const InType* in_f8 = nullptr) {
+  // dtype names the 16-bit type of C, D and the bias; the inputs share it unless in_f8 names
+  // 8-bit input formats
+  const InType in = in_f8 ? *in_f8 : in16(dtype);
   gb_gemm_plan pl;
-  gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl);
+  gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl, &in);
   if (st != GB_OK) return st;
   if (M == 0 || N == 0) return GB_OK;
   if (D == nullptr) return GB_ERR_INVALID_ARG;
@@ -1185,11 +1216,12 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   std::memset(&tmA, 0, sizeof(tmA));
   std::memset(&tmB, 0, sizeof(tmB));
   if (K > 0) {
-    if ((st = encode_map(&tmA, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype)) != GB_OK) return st;
-    if ((st = encode_map(&tmB, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype)) != GB_OK) return st;
+    if ((st = encode_map(&tmA, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
+    if ((st = encode_map(&tmB, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
+  p.bk_elems = in.bk();
   if (epi) {
     p.fused = 1;
     p.bias = static_cast<const uint16_t*>(epi->bias);
@@ -1200,7 +1232,12 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.vec8_ok = (pl.d_elem_stride[1] == 1 && N % 16 == 0) ? 1 : 0;
   }
   const bool pair = pl.variant == kVariantPair;
-  if (pair && (st = dtype == GB_BF16 ? prepare_pair<true>(dev) : prepare_pair<false>(dev)) != GB_OK) return st;
+  const bool bf = dtype == GB_BF16;
+  if (pair) {
+    st = in.f8 ? (bf ? prepare_pair<true, true>(dev) : prepare_pair<false, true>(dev))
+               : (bf ? prepare_pair<true, false>(dev) : prepare_pair<false, false>(dev));
+    if (st != GB_OK) return st;
+  }
   const int slots = pair ? dev->pair_clusters : dev->sms;   // CTAs (pairs) that can run at once
 
   // schedule: stream-K needs a workspace and some K; by default it is used when the tiles
@@ -1229,10 +1266,12 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.dp_tiles = p.num_tiles;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pair)
-    return dtype == GB_BF16 ? launch_pair<true>(dev, tmA, tmB, p, G, s) : launch_pair<false>(dev, tmA, tmB, p, G, s);
-  return dtype == GB_BF16 ? launch_single<true>(dev, tmA, tmB, p, G, s)
-                          : launch_single<false>(dev, tmA, tmB, p, G, s);
+  if (pair) {
+    if (in.f8) return bf ? launch_pair<true, true>(dev, tmA, tmB, p, G, s) : launch_pair<false, true>(dev, tmA, tmB, p, G, s);
+    return bf ? launch_pair<true, false>(dev, tmA, tmB, p, G, s) : launch_pair<false, false>(dev, tmA, tmB, p, G, s);
+  }
+  if (in.f8) return bf ? launch_single<true, true>(dev, tmA, tmB, p, G, s) : launch_single<false, true>(dev, tmA, tmB, p, G, s);
+  return bf ? launch_single<true, false>(dev, tmA, tmB, p, G, s) : launch_single<false, false>(dev, tmA, tmB, p, G, s);
 }
 
 }  // namespace
@@ -1265,6 +1304,17 @@ gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha, const vo
   if (!workspace) return GB_ERR_INVALID_ARG;
   return gemm_entry(GB_BF16, M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, D, workspace,
                     workspace_bytes, stream);
+}
+
+gb_status gb_gemm_fp8(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K, float alpha,
+                      const void* A, int64_t lda, const void* B, int64_t ldb, float beta, const void* C, void* D,
+                      const gb_epilogue* epi, void* workspace, size_t workspace_bytes, void* stream) {
+  if (a_format != GB_FP8_E4M3 && a_format != GB_FP8_E5M2) return GB_ERR_INVALID_ARG;
+  if (b_format != GB_FP8_E4M3 && b_format != GB_FP8_E5M2) return GB_ERR_INVALID_ARG;
+  if (out_dtype != GB_F16 && out_dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  const InType in{a_format, b_format, true, 1};
+  return gemm_entry(out_dtype, M, N, K, alpha, A, lda, GB_K_MAJOR, B, ldb, GB_K_MAJOR, beta, C, D, workspace,
+                    workspace_bytes, stream, epi, &in);
 }
 
 gb_status gb_gemm_ex(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
