@@ -215,14 +215,16 @@ gb_status gb_set_wait_timeout_ns(uint64_t ns);
 gb_status gb_debug_skip_k_block(int64_t k_block);
 
 /* Kernel variant for later calls (process-wide): 0 chooses by shape (the default), 1 the
-   single-CTA 128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel.  GB_ERR_INVALID_ARG for
-   other values. */
+   single-CTA 128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 3 the CTA-pair kernel in
+   clusters of two pairs that share each B tile through multicast copies (whole tiles only:
+   the *_ws calls do not use stream-K with it).  GB_ERR_INVALID_ARG for other values. */
 gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1 or 2)
-   uses for tile (m_tile, n_tile) of an M x N problem: out[r*256 + c] = offset of in-tile
-   element (r, c) (r < tile_m, c < 256), or -1 when the element lies outside M x N.  out is
-   a device buffer of tile_m * 256 int64.  Asynchronous on stream. */
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2 or
+   3) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
+   in-tile element (r, c) (r < tile_m, c < tile_n, both from gb_gemm_make_plan), or -1
+   when the element lies outside M x N.  out is a device buffer of tile_m * tile_n int64.
+   Asynchronous on stream. */
 gb_status gb_debug_epilogue_map(int variant, int64_t M, int64_t N, int64_t m_tile,
                                 int64_t n_tile, int64_t* out, void* stream);
 

@@ -45,33 +45,45 @@
 
 namespace gb {
 
-constexpr int kBN = 256;             // output tile columns (one MMA's N)
+constexpr int kBN = 256;             // N of one MMA instruction (and the single variant's tile)
+constexpr int kPairTileN = 256;      // output tile columns of the pair variant (256 or 512)
 constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
 constexpr int kRowsA = 128;          // A rows staged per CTA (one MMA's M per SM)
 constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
 constexpr int kSwz = 64;             // elements per 128-byte swizzle span
 constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 2 * kBN;
+constexpr int kTmemCols = 512;       // all of Tensor Memory: accumulators of 512 fp32 columns
 constexpr int kCtlBytes = 256;
 constexpr int kMaxStages = 6;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 // Two variants share all code:
-//  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64;
-//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x 256 tile; each CTA
-//         stages its own 128 A rows and 128 of the 256 B rows, two 64-wide k-blocks per
-//         stage (3 stages of 64 KiB: every stage carries a fixed cost in the copy engine
-//         and the barrier hand-off, so fewer, larger stages feed the pair faster), the even
-//         CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared memory,
-//         and each CTA's TMEM holds its own 128 rows of the accumulator.
+//  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64,
+//         two 256-column accumulators in TMEM (the epilogue of one tile overlaps the main
+//         loop of the next);
+//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x kPairTileN tile; the
+//         even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256) reading both CTAs'
+//         shared memory, and each CTA's TMEM holds its own 128 rows of the accumulator.
+//         Each CTA stages its 128 A rows and, per 256-column MMA, its 128 of the 256 B rows.
+//         A 512-column tile (kPairTileN = 512) feeds two MMAs from one k-block of A; the
+//         accumulator then fills TMEM, the epilogue no longer overlaps the next tile, and
+//         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
+//         the copy side's time did not drop with the 25 % fewer bytes (it follows the count
+//         of pipeline stages), so 256-column tiles with the overlapped epilogue stay.
 template <bool kPair>
 struct Cfg {
   static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kRowsB = kPair ? 128 : 256;
-  static constexpr int kStages = kPair ? 3 : 4;
-  static constexpr int kKB = kPair ? 2 : 1;               // 64-wide k-blocks per stage
+  static constexpr int kTileN = kPair ? kPairTileN : kBN;
+  static constexpr int kNSub = kTileN / kBN;                  // MMAs per K step (along N)
+  static constexpr int kRowsBSub = kPair ? kBN / 2 : kBN;    // B rows a CTA stages per MMA
+  static constexpr int kRowsB = kRowsBSub * kNSub;          // B rows a CTA stages per k-block
+  static constexpr int kAccBufs = kTmemCols / kTileN;       // accumulators in TMEM
+  static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1; // 64-wide k-blocks per stage
+  static constexpr int kStages = (kPair && kNSub == 1) ? 3 : 4;
+  static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;      // producer, MMA, epilogue warps
   static constexpr int kAHalf = kRowsA * kBK * 2;          // one k-block of A (bytes)
+  static constexpr int kBSub = kRowsBSub * kBK * 2;        // one k-block of one MMA's B rows
   static constexpr int kBHalf = kRowsB * kBK * 2;          // one k-block of B (bytes)
   static constexpr int kAStage = kAHalf * kKB;
   static constexpr int kBStage = kBHalf * kKB;
@@ -79,11 +91,12 @@ struct Cfg {
   // bytes one k-block adds to the (even CTA's) full barrier: both CTAs' copies in a pair
   static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf) * (kPair ? 2 : 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
-  static constexpr uint32_t kAccEmptyArrivals = 4 * (kPair ? 2 : 1);   // epilogue warps
+  static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
+  static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
   static_assert(kStages <= kMaxStages, "control block");
+  static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kBN == 0, "TMEM accumulators");
 };
-static_assert(kTmemCols <= 512, "Tensor Memory holds 512 columns per SM");
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
 struct Params {
@@ -118,8 +131,8 @@ struct Params {
   int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
 };
 
-// Slot of CTA (cluster c, rank r) in the stream-K workspace.
-constexpr int kSlotFloats = 128 * 256;
+// Largest stream-K slot of any variant (floats): sizes the workspace.
+constexpr int kSlotFloats = kRowsA * (kPairTileN > kBN ? kPairTileN : kBN);
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -150,7 +163,11 @@ template <bool kPair>
 __device__ __forceinline__ void raise_status(Ctl* ctl, uint32_t site) {
   atomicCAS(&g_status, 0u, site | (blockIdx.x << 8));
   *reinterpret_cast<volatile int32_t*>(&ctl->abort) = 1;
-  if constexpr (kPair) st_cluster_u32(map_to_cta(smem_addr(&ctl->abort), cluster_ctarank() ^ 1u), 1u);
+  if constexpr (kPair) {
+    const uint32_t me = cluster_ctarank(), n = cluster_nctarank();
+    for (uint32_t c = 0; c < n; ++c)
+      if (c != me) st_cluster_u32(map_to_cta(smem_addr(&ctl->abort), c), 1u);
+  }
 }
 
 __device__ __forceinline__ bool aborted(Ctl* ctl) {
@@ -233,14 +250,35 @@ __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, 
 // Grouped raster order: runs of group_m M-tiles, walked down M first, then across N,
 // so that CTAs working at the same time share A rows and B columns in L2 ("CUTLASS, in
 // depth" — "Kernel schedules", rasterisation).
-__device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t& mt, int32_t& nt) {
-  const int32_t per_group = p.group_m * p.n_tiles;
+__device__ __forceinline__ void raster(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
+                                       int32_t& mt, int32_t& nt) {
+  const int32_t per_group = group_m * n_tiles;
   const int32_t g = t / per_group;
-  const int32_t first_m = g * p.group_m;
-  const int32_t gm = min(p.m_tiles - first_m, p.group_m);
+  const int32_t first_m = g * group_m;
+  const int32_t gm = min(m_tiles - first_m, group_m);
   const int32_t local = t - g * per_group;
   mt = first_m + local % gm;
   nt = local / gm;
+}
+
+__device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t& mt, int32_t& nt) {
+  raster(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+}
+
+// Tile of work item t for pair `pidx` of its cluster.  With B multicast (kMc) a work item
+// is a super-tile of two M-tiles over one column of B tiles: pair 0 takes M-tile 2s,
+// pair 1 takes 2s + 1 (past the last M-tile when m_tiles is odd: its rows are all out of
+// range, and it still loads its share of B for pair 0).
+template <bool kMc>
+__device__ __forceinline__ void item_coords(const Params& p, int32_t t, uint32_t pidx, int32_t& mt,
+                                            int32_t& nt) {
+  if constexpr (kMc) {
+    int32_t sm;
+    raster(t, (p.m_tiles + 1) / 2, p.n_tiles, max(1, p.group_m / 2), sm, nt);
+    mt = 2 * sm + static_cast<int32_t>(pidx);
+  } else {
+    tile_coords(p, t, mt, nt);
+  }
 }
 
 // One unit of work: stage-blocks [sb0, sb1) of tile `tile`.
@@ -332,10 +370,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k
   return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
 }
 
-template <bool kPair>
+template <bool kPair, bool kMc>
 __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, uint8_t* smem,
                              Ctl* ctl, uint32_t rank, uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair>;
+  // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
+  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
   int stage = 0;
   uint32_t phase = 0;
   int64_t gkb = 0;
@@ -346,9 +386,9 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   Item item;
   while (ok && sched.next(p, nclusters, item)) {
     int32_t mt, nt;
-    tile_coords(p, item.tile, mt, nt);
-    const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(rank) * kRowsA;
-    const int32_t b_row0 = nt * kBN + static_cast<int32_t>(rank) * C::kRowsB;
+    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA;
+    const int32_t b_row0 = nt * C::kTileN + static_cast<int32_t>(prank) * C::kRowsBSub;
     for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
       if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
         ok = false;
@@ -357,17 +397,31 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
       if (gkb != p.skip_kb) {
         const uint32_t full = smem_addr(&ctl->full[stage]);
         // in a pair both CTAs' copies are counted on the even CTA's barrier
-        const uint32_t full_tgt = kPair ? map_to_cta(full, 0) : full;
+        const uint32_t full_tgt = kPair ? map_to_cta(full, leader) : full;
         const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
         // the last stage of a tile may hold fewer k-blocks: copy and count only those
         const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
-        if (!kPair || rank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
+        if (!kPair || prank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
           issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
                                p.bk_elems);
-          issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf, full_tgt, b_row0,
-                               C::kRowsB, kb, p.bk_elems);
+          if constexpr (kMc) {
+            // both pairs need the same B rows: this CTA copies its pair's quarter of them
+            // (64 rows) into itself and the same-rank CTA of the other pair
+            const uint32_t dst = sa + C::kAStage + h * C::kBHalf + pidx * kChunkBytes;
+            const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+            if (p.majorB == 0)
+              tma_load_2d_pair_mc(dst, tmB, full_tgt, kb * p.bk_elems, b_row0 + pidx * kSwz, mask);
+            else
+              tma_load_2d_pair_mc(dst, tmB, full_tgt, b_row0 + pidx * kSwz, kb * kBK, mask);
+          } else {
+            // per MMA along N: this CTA's rows of that MMA's 256 tile columns
+#pragma unroll
+            for (int j = 0; j < C::kNSub; ++j)
+              issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
+                                   full_tgt, b_row0 + j * kBN, C::kRowsBSub, kb, p.bk_elems);
+          }
         }
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -390,7 +444,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         phase ^= 1u;
       }
     }
-  } else if (!kPair || rank == 0) {
+  } else if (!kPair || prank == 0) {
     for (int s = 0; s < C::kStages; ++s)
       if (issued & (1u << s))
         wait_drain(smem_addr(&ctl->full[s]), (issued_parity >> s) & 1u, p.timeout_ns);
@@ -401,11 +455,15 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   }
 }
 
-template <bool kPair, bool kF8>
+template <bool kPair, bool kF8, bool kMc>
 __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
                         uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair>;
-  if (kPair && rank != 0) return;          // the even CTA issues for the pair
+  if (kPair && (rank & 1u) != 0) return;   // the even CTA issues for the pair
+  // a stage is free once every pair reading it has finished: with B multicast the other
+  // pair's copies land in this pair's stages too, so releases go to all four CTAs
+  const uint16_t release_mask = kMc ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true, issued_any = false;
@@ -414,15 +472,15 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
   sched.init(p, cluster, nclusters);
   Item item;
   for (; ok && sched.next(p, nclusters, item); ++it) {
-    const int buf = it & 1;
-    const uint32_t use = (it >> 1) & 1;
+    const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+    const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
     if (!wait_one<kPair, kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns,
                                 kSiteAccEmpty)) {
       ok = false;
       break;
     }
     tc_fence_after_sync();
-    const uint32_t d_tmem = tmem_base + buf * kBN;
+    const uint32_t d_tmem = tmem_base + buf * C::kTileN;
     for (int32_t sbk = item.sb0; sbk < item.sb1; ++sbk) {
       if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
         ok = false;
@@ -441,22 +499,27 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k) {
           const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
-          const uint64_t db = db0 + ((h * C::kBHalf) >> 4) + k * kb_;
           const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
-          // one instruction covers 32 bytes of K: 16 16-bit or 32 8-bit elements
-          if constexpr (kPair && kF8)
-            tc_mma_f8_pair(d_tmem, da, db, p.idesc, acc);
-          else if constexpr (kPair)
-            tc_mma_f16_pair(d_tmem, da, db, p.idesc, acc);
-          else if constexpr (kF8)
-            tc_mma_f8(d_tmem, da, db, p.idesc, acc);
-          else
-            tc_mma_f16(d_tmem, da, db, p.idesc, acc);
+          // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and 256
+          // columns; the N sub-tiles share the A slice
+#pragma unroll
+          for (int j = 0; j < C::kNSub; ++j) {
+            const uint64_t db = db0 + ((h * C::kBHalf + j * C::kBSub) >> 4) + k * kb_;
+            const uint32_t dt = d_tmem + j * kBN;
+            if constexpr (kPair && kF8)
+              tc_mma_f8_pair(dt, da, db, p.idesc, acc);
+            else if constexpr (kPair)
+              tc_mma_f16_pair(dt, da, db, p.idesc, acc);
+            else if constexpr (kF8)
+              tc_mma_f8(dt, da, db, p.idesc, acc);
+            else
+              tc_mma_f16(dt, da, db, p.idesc, acc);
+          }
         }
       }
       issued_any = true;
       if constexpr (kPair)
-        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), 0x3);
+        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), release_mask);
       else
         tc_commit(smem_addr(&ctl->empty[stage]));
       if (++stage == C::kStages) {
@@ -468,10 +531,10 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
     const uint32_t af = smem_addr(&ctl->acc_full[buf]);
     if (p.k_blocks == 0) {
       mbar_arrive(af);
-      if constexpr (kPair) mbar_arrive_cluster(map_to_cta(af, 1));
+      if constexpr (kPair) mbar_arrive_cluster(map_to_cta(af, rank + 1));
     } else {
       if constexpr (kPair)
-        tc_commit_pair_mc(af, 0x3);
+        tc_commit_pair_mc(af, pair_mask);
       else
         tc_commit(af);
     }
@@ -510,17 +573,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // 32 consecutive outputs of one row: v = alpha*acc (+ beta*c) in fp32.
 template <bool kBF16>
-__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, const uint32_t (&acc)[32],
+__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, const uint4* cw,
+                                                const uint32_t (&acc)[32],
                                                 int valid, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
   if (!p.has_c) return;
-  if (p.vec_ok && valid == 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.C + off);
+  if (cw != nullptr) {
+    // 32 C values loaded ahead as four 16-byte words
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 u = __ldg(src + j);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const uint32_t w[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
@@ -588,10 +651,10 @@ __device__ __forceinline__ void store_fp8(const Params& p, int64_t off, const fl
 
 // The epilogue of 32 consecutive outputs of one row (columns col0 .. col0+31).
 template <bool kBF16>
-__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint32_t (&acc)[32], int valid,
-                                          int64_t col0, float& amax) {
+__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint4* cw,
+                                          const uint32_t (&acc)[32], int valid, int64_t col0, float& amax) {
   float v[32];
-  epilogue_values<kBF16>(p, off, acc, valid, v);
+  epilogue_values<kBF16>(p, off, cw, acc, valid, v);
   if (!p.fused) {
     store_16<kBF16>(p, off, v, valid);
     return;
@@ -613,7 +676,7 @@ __device__ __forceinline__ void store_run(const Params& p, int64_t off, const ui
 // column-major ([column][row]) so that a warp's 32 rows form one 128-byte access.
 template <bool kPair>
 __device__ __forceinline__ float* part_slot(const Params& p, uint32_t c, uint32_t rank) {
-  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * kSlotFloats;
+  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * Cfg<kPair>::kSlotFloats;
 }
 
 template <bool kPair>
@@ -649,13 +712,17 @@ __device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl
   return ok != 0;
 }
 
-template <bool kBF16, bool kPair>
+template <bool kBF16, bool kPair, bool kMc>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair>;
+  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
-  const int r = static_cast<int>(rank) * kRowsA + lrow;   // row within the tile
+  // with eight epilogue warps two share a lane quarter and split the columns
+  constexpr int kCols = C::kTileN / (C::kEpiWarps / 4);
+  const int cbeg = ((warp - 2) >> 2) * kCols;
+  const int r = static_cast<int>(prank) * kRowsA + lrow;   // row within the tile
   int32_t it = 0;
   float amax = 0.0f;                 // this thread's max |v| (fused epilogue)
   Sched sched;
@@ -663,9 +730,19 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   Item item;
   for (; sched.next(p, nclusters, item); ++it) {
     int32_t mt, nt;
-    tile_coords(p, item.tile, mt, nt);
-    const int buf = it & 1;
-    const uint32_t use = (it >> 1) & 1;
+    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
+    const int32_t cols_left = p.N - nt * C::kTileN;
+    const int64_t base = d_offset(p, mt, nt, r, 0);
+    const int cend = min(cbeg + kCols, static_cast<int>(min(cols_left, C::kTileN)));
+    // C in 16-byte words when rows are contiguous and aligned (vec_ok); the tile's C rows
+    // are pulled into L2 while the main loop still runs, and each 32-column run is loaded
+    // one run ahead of its use
+    const bool cvec = p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
+    if (cvec && cend > cbeg)
+      prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
+    const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+    const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
     if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
     tc_fence_after_sync();
     // stream-K roles: a contributor holds later k-units of a tile and hands its partial
@@ -683,13 +760,24 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       if (!ok) break;
     }
     float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
-    const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
-    const int32_t cols_left = p.N - nt * kBN;
-    const int64_t base = d_offset(p, mt, nt, r, 0);
-    for (int c0 = 0; c0 < kBN && c0 < cols_left; c0 += 32) {
+    uint4 cw[4], cn[4];
+    if (cvec && cbeg + 32 <= cend) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cw[j] = __ldg(src + j);
+    }
+    for (int c0 = cbeg; c0 < cend; c0 += 32) {
       uint32_t acc[32];
+      const bool vec_run = cvec && c0 + 32 <= cend;
+      const bool next_vec = cvec && c0 + 64 <= cend;
+      if (p.k_blocks > 0)
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kTileN + c0, acc);
+      if (next_vec) {   // issued while the TMEM load is in flight
+        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + c0 + 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cn[j] = __ldg(src + j);
+      }
       if (p.k_blocks > 0) {
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kBN + c0, acc);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -708,8 +796,12 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
           acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
       }
       if (row_ok)
-        store_run<kBF16>(p, base + c0 * p.d_col, acc, min(32, cols_left - c0),
-                         static_cast<int64_t>(nt) * kBN + c0, amax);
+        store_run<kBF16>(p, base + c0 * p.d_col, vec_run ? cw : nullptr, acc, min(32, cols_left - c0),
+                         static_cast<int64_t>(nt) * C::kTileN + c0, amax);
+      if (next_vec) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cw[j] = cn[j];
+      }
     }
     if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
     tc_fence_before_sync();
@@ -717,14 +809,14 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     if (lane == 0) {
       const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
       if constexpr (kPair)
-        mbar_arrive_cluster(map_to_cta(ae, 0));
+        mbar_arrive_cluster(map_to_cta(ae, leader));
       else
         mbar_arrive(ae);
       if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
     }
     if (contributor && warp == 2) {
       // a CTA contributes at most one partial per launch: part_done completes phase 0 once
-      // all four epilogue warps have written theirs; then publish it at device scope
+      // all epilogue warps have written theirs; then publish it at device scope
       if (!wait_warp<kPair>(smem_addr(&ctl->part_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
       if (lane == 0) {
         fence_acq_rel_gpu();
@@ -745,8 +837,8 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <bool kBF16, bool kPair, bool kF8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kBF16, bool kPair, bool kF8, bool kMc = false>
+__global__ void __launch_bounds__(Cfg<kPair>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const Params p) {
   using C = Cfg<kPair>;
@@ -762,14 +854,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
-      mbar_init(smem_addr(&ctl->empty[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), kMc ? 2 : 1);   // one release per pair reading it
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
       mbar_init(smem_addr(&ctl->acc_empty[b]), C::kAccEmptyArrivals);
     }
     mbar_init(smem_addr(&ctl->drain), 1);
-    mbar_init(smem_addr(&ctl->part_done), 4);
+    mbar_init(smem_addr(&ctl->part_done), C::kEpiWarps);
     ctl->abort = 0;
     fence_barrier_init();
     if (p.k_blocks > 0) {
@@ -793,13 +885,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<kPair>(p, &tmA, &tmB, smem, ctl, rank, cluster, nclusters);
+    if (lane == 0) run_producer<kPair, kMc>(p, &tmA, &tmB, smem, ctl, rank, cluster, nclusters);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<kPair, kF8>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
+    if (lane == 0) run_mma<kPair, kF8, kMc>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
-    run_epilogue<kBF16, kPair>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
+    run_epilogue<kBF16, kPair, kMc>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
   }
 
   tc_fence_before_sync();
@@ -815,13 +907,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ test kernels
-__global__ void epilogue_map_kernel(const Params p, int32_t tile_m, int32_t mt, int32_t nt,
+__global__ void epilogue_map_kernel(const Params p, int32_t tile_m, int32_t tile_n, int32_t mt, int32_t nt,
                                     int64_t* out) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= tile_m * kBN) return;
-  const int r = idx / kBN, c = idx % kBN;
+  if (idx >= tile_m * tile_n) return;
+  const int r = idx / tile_n, c = idx % tile_n;
   const int64_t row = static_cast<int64_t>(mt) * tile_m + r;
-  const int64_t col = static_cast<int64_t>(nt) * kBN + c;
+  const int64_t col = static_cast<int64_t>(nt) * tile_n + c;
   out[idx] = (row < p.M && col < p.N) ? d_offset(p, mt, nt, r, c) : -1;
 }
 
@@ -864,19 +956,24 @@ using gb::Params;
 std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
-int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair
+int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast
 int g_force_schedule = 0;  // 0: stream-K when a workspace is given and tiles leave a ragged
                            // last wave; 1: data-parallel only; 2: stream-K whenever possible
 
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
+constexpr int kVariantPairMc = 3;   // clusters of two pairs sharing B tiles by multicast
+
+bool is_pair(int variant) { return variant == kVariantPair || variant == kVariantPairMc; }
 
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
   bool attr_single[2][2] = {{false, false}, {false, false}};   // [bf16 out][fp8 in]
   bool attr_pair[2][2] = {{false, false}, {false, false}};
+  bool attr_mc[2][2] = {{false, false}, {false, false}};
   int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
+  int mc_clusters = 0;     // co-resident 4-CTA clusters of the multicast kernel
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
 };
@@ -979,7 +1076,7 @@ int choose_variant(int64_t M) {
     std::lock_guard<std::mutex> lk(g_mu);
     forced = g_force_variant;
   }
-  if (forced == kVariantSingle || forced == kVariantPair) return forced;
+  if (forced == kVariantSingle || is_pair(forced)) return forced;
   return M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
 }
 
@@ -989,20 +1086,23 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB, in.bytes);
   if (st != GB_OK) return st;
   if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
-  if (variant != kVariantSingle && variant != kVariantPair) return GB_ERR_INVALID_ARG;
-  const bool pair = variant == kVariantPair;
+  if (variant != kVariantSingle && !is_pair(variant)) return GB_ERR_INVALID_ARG;
+  const bool pair = is_pair(variant);
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
-  const int64_t rows_b = pair ? gb::Cfg<true>::kRowsB : gb::Cfg<false>::kRowsB;
+  const int64_t tile_n = pair ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
+  // B rows one copy stages: with multicast each CTA copies a quarter of the pair's 256
+  int64_t rows_b = pair ? gb::Cfg<true>::kRowsBSub : gb::Cfg<false>::kRowsBSub;
+  if (variant == kVariantPairMc) rows_b = gb::kSwz;
   std::memset(pl, 0, sizeof(*pl));
   pl->variant = variant;
   pl->tile_m = tile_m;
-  pl->tile_n = gb::kBN;
+  pl->tile_n = tile_n;
   pl->tile_k = in.bk();
   if (M == 0 || N == 0) return GB_OK;
   try {
-    // D (and C): (M,N):(N,1) divided into (tile_m, 256) tiles -> ((tile),(grid))
+    // D (and C): (M,N):(N,1) divided into (tile_m, tile_n) tiles -> ((tile),(grid))
     la::Layout mD = la::make_layout({M, N}, {N, 1});
-    la::Layout zD = la::zipped_divide(mD, la::tiler_of({tile_m, gb::kBN}));
+    la::Layout zD = la::zipped_divide(mD, la::tiler_of({tile_m, tile_n}));
     auto grid_shape = la::flatten(zD.mode(1).shape);
     auto grid_stride = la::flatten(zD.mode(1).stride);
     auto elem_stride = la::flatten(mD.stride);
@@ -1016,7 +1116,8 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
     if (K > 0) {
       OperandPlan a, b;
       if ((st = plan_operand(M, K, lda, majorA, tile_m, gb::kRowsA, &a, in)) != GB_OK) return st;
-      if ((st = plan_operand(N, K, ldb, majorB, gb::kBN, rows_b, &b, in)) != GB_OK) return st;
+      // B's copy box covers one CTA's rows of one 256-column MMA
+      if ((st = plan_operand(N, K, ldb, majorB, tile_n, rows_b, &b, in)) != GB_OK) return st;
       if (a.grid_rows != pl->m_tiles || b.grid_rows != pl->n_tiles || a.k_blocks != b.k_blocks)
         return GB_ERR_INVALID_ARG;
       pl->k_blocks = a.k_blocks;
@@ -1086,9 +1187,11 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
   p->m_tiles = static_cast<int32_t>(pl.m_tiles);
   p->n_tiles = static_cast<int32_t>(pl.n_tiles);
   p->k_blocks = static_cast<int32_t>(pl.k_blocks);
-  p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);
-  p->group_m = pl.variant == kVariantPair ? 8 : 16;
-  const int kkb = pl.variant == kVariantPair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
+  // work items: tiles, or with B multicast super-tiles of two M-tiles
+  p->num_tiles = static_cast<int32_t>(
+      (pl.variant == kVariantPairMc ? (pl.m_tiles + 1) / 2 : pl.m_tiles) * pl.n_tiles);
+  p->group_m = is_pair(pl.variant) ? 8 : 16;
+  const int kkb = is_pair(pl.variant) ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
   p->nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   p->dp_tiles = p->num_tiles;   // data-parallel unless the caller sets up stream-K
   p->bk_elems = 64;             // 16-bit inputs; 8-bit inputs set 128
@@ -1120,59 +1223,81 @@ gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensor
       return GB_ERR_LAUNCH;
     dev->attr_single[kBF16][kF8] = true;
   }
-  gb::gemm_kernel<kBF16, false, kF8><<<grid, gb::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  gb::gemm_kernel<kBF16, false, kF8><<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
-template <bool kBF16, bool kF8>
+template <bool kBF16, bool kF8, bool kMc>
 gb_status prepare_pair(DeviceState* dev) {
   using C = gb::Cfg<true>;
-  if (!dev->attr_pair[kBF16][kF8]) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
+  bool& attr = kMc ? dev->attr_mc[kBF16][kF8] : dev->attr_pair[kBF16][kF8];
+  if (!attr) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kF8, kMc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    dev->attr_pair[kBF16][kF8] = true;
+    attr = true;
   }
-  if (dev->pair_clusters == 0) {
-    // a persistent grid must fit at once: ask how many pairs can be resident together
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+  int& clusters = kMc ? dev->mc_clusters : dev->pair_clusters;
+  if (clusters == 0) {
+    // a persistent grid must fit at once: ask how many clusters can be resident together
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCl;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(gb::kThreads, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.attrs = attr;
+    cfg.attrs = at;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(2 * (dev->sms / 2), 1, 1);
+    cfg.gridDim = dim3(kCl * (dev->sms / kCl), 1, 1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kF8>, &cfg) != cudaSuccess || n <= 0)
-      n = dev->sms / 2;
-    dev->pair_clusters = std::min(n, dev->sms / 2);
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kF8, kMc>, &cfg) != cudaSuccess ||
+        n <= 0)
+      n = dev->sms / kCl;
+    clusters = std::min(n, dev->sms / kCl);
   }
   return GB_OK;
 }
 
-template <bool kBF16, bool kF8>
-gb_status launch_pair(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                      int clusters, cudaStream_t s) {
+template <bool kBF16, bool kF8, bool kMc>
+gb_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p, int clusters,
+                      cudaStream_t s) {
   using C = gb::Cfg<true>;
+  constexpr int kCl = kMc ? 4 : 2;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kCl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(gb::kThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kF8>, tmA, tmB, p) != cudaSuccess)
+  cfg.gridDim = dim3(kCl * clusters, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kF8, kMc>, tmA, tmB, p) != cudaSuccess)
     return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+// Dispatch on the output type and the two pair kernels.
+template <bool kF8>
+gb_status prepare_pair_any(bool bf, bool mc, DeviceState* dev) {
+  if (mc) return bf ? prepare_pair<true, kF8, true>(dev) : prepare_pair<false, kF8, true>(dev);
+  return bf ? prepare_pair<true, kF8, false>(dev) : prepare_pair<false, kF8, false>(dev);
+}
+
+template <bool kF8>
+gb_status launch_pair_any(bool bf, bool mc, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
+                          int clusters, cudaStream_t s) {
+  if (mc)
+    return bf ? launch_pair<true, kF8, true>(tmA, tmB, p, clusters, s)
+              : launch_pair<false, kF8, true>(tmA, tmB, p, clusters, s);
+  return bf ? launch_pair<true, kF8, false>(tmA, tmB, p, clusters, s)
+            : launch_pair<false, kF8, false>(tmA, tmB, p, clusters, s);
 }
 
 // Workspace layout: one 32-bit flag per CTA (padded to 256 B), then one 128 x 256 fp32
@@ -1231,14 +1356,15 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.out_scale = epi->out_scale;
     p.vec8_ok = (pl.d_elem_stride[1] == 1 && N % 16 == 0) ? 1 : 0;
   }
-  const bool pair = pl.variant == kVariantPair;
+  const bool pair = is_pair(pl.variant);
+  const bool mc = pl.variant == kVariantPairMc;
   const bool bf = dtype == GB_BF16;
   if (pair) {
-    st = in.f8 ? (bf ? prepare_pair<true, true>(dev) : prepare_pair<false, true>(dev))
-               : (bf ? prepare_pair<true, false>(dev) : prepare_pair<false, false>(dev));
+    st = in.f8 ? prepare_pair_any<true>(bf, mc, dev) : prepare_pair_any<false>(bf, mc, dev);
     if (st != GB_OK) return st;
   }
-  const int slots = pair ? dev->pair_clusters : dev->sms;   // CTAs (pairs) that can run at once
+  // CTAs (clusters) that can run at once
+  const int slots = mc ? dev->mc_clusters : pair ? dev->pair_clusters : dev->sms;
 
   // schedule: stream-K needs a workspace and some K; by default it is used when the tiles
   // leave a ragged last wave (or fewer tiles than CTAs)
@@ -1249,7 +1375,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
   p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
-  bool sk = workspace != nullptr && p.nsb > 0 && sched != 1;
+  bool sk = !mc && workspace != nullptr && p.nsb > 0 && sched != 1;   // multicast: whole tiles
   if (sk && sched == 0) sk = p.num_tiles % slots != 0;
   int G;
   if (sk) {
@@ -1266,10 +1392,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.dp_tiles = p.num_tiles;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pair) {
-    if (in.f8) return bf ? launch_pair<true, true>(dev, tmA, tmB, p, G, s) : launch_pair<false, true>(dev, tmA, tmB, p, G, s);
-    return bf ? launch_pair<true, false>(dev, tmA, tmB, p, G, s) : launch_pair<false, false>(dev, tmA, tmB, p, G, s);
-  }
+  if (pair)
+    return in.f8 ? launch_pair_any<true>(bf, mc, tmA, tmB, p, G, s) : launch_pair_any<false>(bf, mc, tmA, tmB, p, G, s);
   if (in.f8) return bf ? launch_single<true, true>(dev, tmA, tmB, p, G, s) : launch_single<false, true>(dev, tmA, tmB, p, G, s);
   return bf ? launch_single<true, false>(dev, tmA, tmB, p, G, s) : launch_single<false, false>(dev, tmA, tmB, p, G, s);
 }
@@ -1384,7 +1508,7 @@ gb_status gb_debug_skip_k_block(int64_t k_block) {
 }
 
 gb_status gb_set_kernel_variant(int variant) {
-  if (variant != 0 && variant != kVariantSingle && variant != kVariantPair) return GB_ERR_INVALID_ARG;
+  if (variant != 0 && variant != kVariantSingle && !is_pair(variant)) return GB_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_variant = variant;
   return GB_OK;
@@ -1401,9 +1525,10 @@ gb_status gb_debug_epilogue_map(int variant, int64_t M, int64_t N, int64_t m_til
   if ((st = device_state(&dev)) != GB_OK) return st;
   Params p;
   fill_params(pl, M, N, 0, 1.0f, 0, 0, 0.0f, nullptr, nullptr, &p);
-  const int n = static_cast<int>(pl.tile_m) * gb::kBN;
+  const int n = static_cast<int>(pl.tile_m * pl.tile_n);
   gb::epilogue_map_kernel<<<n / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      p, static_cast<int32_t>(pl.tile_m), static_cast<int32_t>(m_tile), static_cast<int32_t>(n_tile), out);
+      p, static_cast<int32_t>(pl.tile_m), static_cast<int32_t>(pl.tile_n), static_cast<int32_t>(m_tile),
+      static_cast<int32_t>(n_tile), out);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 

@@ -217,6 +217,24 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Pair copy multicast to the CTAs of `mask` (same shared-memory offset in each).  With
+// .cta_group::2 the bytes landing in a destination CTA are counted on the barrier at
+// `bar`'s offset in the even CTA of that destination's pair (`bar` names an even CTA).
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar,
+                                                    int32_t x, int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
 // Tensor Memory allocation for a CTA pair: one warp of each peer CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -279,6 +297,14 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
 }  // namespace gb
 
 namespace gb {
+
+// Bulk prefetch of `bytes` (a multiple of 16) contiguous global bytes into L2; `p` is
+// 16-byte aligned.  No completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
 
 // Warm L2 with one 2-D box of a tensor map (no shared memory, no completion signal).
 __device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {

@@ -37,7 +37,7 @@ def test_status_strings():
     assert "10.3" in G.status_string(3)
 
 
-@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+@pytest.fixture(params=[1, 2, 3], ids=["single", "pair", "pair_mc"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param
@@ -57,11 +57,12 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     p = G.plan("f16", M, N, K, lda, majors[0], ldb, majors[1])
     grid = grid1 if variant == 1 else grid2
     tile_m = 128 if variant == 1 else 256
-    rows_b = 256 if variant == 1 else 128        # B rows staged per CTA
-    assert p["variant"] == variant and p["tile_m"] == tile_m
+    tile_n = 256                                 # every variant: 256-column tiles
+    rows_b = {1: 256, 2: 128, 3: 64}[variant]    # B rows one copy box stages per CTA
+    assert p["variant"] == variant and p["tile_m"] == tile_m and p["tile_n"] == tile_n
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
     # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
-    for i, (ext, want) in enumerate(zip(grid[:2], [tile_m * N, 256])):
+    for i, (ext, want) in enumerate(zip(grid[:2], [tile_m * N, tile_n])):
         if ext > 1:
             assert p["d_grid_stride"][i] == want
     assert p["d_elem_stride"] == [N, 1]
@@ -87,7 +88,7 @@ def test_variant_choice_by_shape():
     assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 1
     assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 2
     with pytest.raises(G.GemmError):
-        G.set_kernel_variant(3)
+        G.set_kernel_variant(4)
 
 
 def test_plan_bf16_descriptor_and_scalar_epilogue(variant):

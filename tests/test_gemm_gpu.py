@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
-@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+@pytest.fixture(params=[1, 2, 3], ids=["single", "pair", "pair_mc"])
 def variant(request):
     """Run a test with the single-CTA kernel and with the CTA-pair kernel."""
     G.set_kernel_variant(request.param)
@@ -259,25 +259,32 @@ def test_wait_timeout_is_reported_and_context_survives(variant):
 # --------------------------------------------------------------------------- device-side maps
 
 
-@pytest.mark.parametrize("var", [1, 2])
+@pytest.mark.parametrize("var", [1, 2, 3])
 @pytest.mark.parametrize("M,N,tile", [(5000, 3000, (19, 11)), (5000, 3000, (0, 0)),
                                       (256, 128, (0, 0)), (8192, 8192, (17, 30))])
 def test_epilogue_map_matches_host_layout(var, M, N, tile):
     """The device evaluation of the C/D tile map equals the host layout library's."""
     tm = 128 if var == 1 else 256
-    out = torch.empty(tm * 256, dtype=torch.int64, device=DEV)
+    G.set_kernel_variant(var)
+    try:
+        tn = int(G.plan("f16", M, N, 64, 64, "K", 64, "K")["tile_n"])
+    finally:
+        G.set_kernel_variant(0)
+    # the last tile along a mode when the index is beyond this variant's grid
+    tile = (min(tile[0], (M + tm - 1) // tm - 1), min(tile[1], (N + tn - 1) // tn - 1))
+    out = torch.empty(tm * tn, dtype=torch.int64, device=DEV)
     st = __import__("layout_algebra_gb300._native", fromlist=["lib"]).lib().gb_debug_epilogue_map(
         var, M, N, tile[0], tile[1], out.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == 0
-    got = out.cpu().numpy().reshape(tm, 256)
-    origin, tl = L.local_tile("(%d,%d):(%d,1)" % (M, N, N), "(%d,256)" % tm, list(tile))
-    rr, cc = np.meshgrid(np.arange(tm), np.arange(256), indexing="ij")
+    got = out.cpu().numpy().reshape(tm, tn)
+    origin, tl = L.local_tile("(%d,%d):(%d,1)" % (M, N, N), "(%d,%d)" % (tm, tn), list(tile))
+    rr, cc = np.meshgrid(np.arange(tm), np.arange(tn), indexing="ij")
     idx = (rr + tm * cc).ravel()                     # colexicographic index of (r, c)
-    want = (origin + L.evaluate(tl, idx)).reshape(tm, 256)
-    inside = ((tile[0] * tm + rr) < M) & ((tile[1] * 256 + cc) < N)
+    want = (origin + L.evaluate(tl, idx)).reshape(tm, tn)
+    inside = ((tile[0] * tm + rr) < M) & ((tile[1] * tn + cc) < N)
     want = np.where(inside, want, -1)
     assert np.array_equal(got, want)
-    assert np.array_equal(got[inside], ((tile[0] * tm + rr) * N + tile[1] * 256 + cc)[inside])
+    assert np.array_equal(got[inside], ((tile[0] * tm + rr) * N + tile[1] * tn + cc)[inside])
 
 
 def _swizzle_offset(row, byte_in_row):
