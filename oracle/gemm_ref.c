@@ -264,6 +264,59 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, double alpha,
                              beta, C, ldc, dtype, rows, cols, n, ref, sumabs, nthreads);
 }
 
+/* E8M0 scale (OCP Microscaling): an 8-bit biased exponent, value 2^(e - 127); 0xFF is NaN. */
+static double decode_e8m0(uint8_t e) {
+    return e == 0xFF ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/*
+ * Block-scaled ("MX") GEMM: every 32 consecutive K elements of a row of A, and of a column
+ * of B, share one E8M0 scale ("CUTLASS, in depth", "Epilogue fusion": FP8 operands carry
+ * per-tensor or per-block scale factors).  The operands are the FP8 codes A, B (as for
+ * oracle_gemm_typed, K-major) and the scales
+ *   SFA[i * ld_sfa + k / 32]  (M rows of ceil(K/32) scales),
+ *   SFB[j * ld_sfb + k / 32]  (N rows of ceil(K/32) scales),
+ * so that
+ *   acc(i,j) = sum_k  (2^(sfa(i,k/32)-127) a(i,k)) * (2^(sfb(j,k/32)-127) b(k,j))
+ *   ref(i,j) = alpha*acc + beta*c(i,j)
+ * with k in order and every product and sum in double.  sumabs as for oracle_gemm_typed,
+ * of the scaled products.
+ */
+int oracle_gemm_mx(int64_t M, int64_t N, int64_t K, double alpha,
+                   const uint16_t* A, int64_t lda, int dtA, const uint8_t* SFA, int64_t ld_sfa,
+                   const uint16_t* B, int64_t ldb, int dtB, const uint8_t* SFB, int64_t ld_sfb,
+                   double beta, const uint16_t* C, int64_t ldc, int dtC,
+                   const int64_t* rows, const int64_t* cols, int64_t n,
+                   double* ref, double* sumabs, int nthreads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (beta != 0.0 && C == NULL) return -1;
+    if (K > 0 && (SFA == NULL || SFB == NULL)) return -1;
+    int64_t total = rows ? n : M * N;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t e = 0; e < total; ++e) {
+        int64_t i = rows ? rows[e] : e / (N ? N : 1);
+        int64_t j = rows ? cols[e] : e % (N ? N : 1);
+        double acc = 0.0, mag = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = decode_e8m0(SFA[i * ld_sfa + k / 32]) * decode(dtA, A[i * lda + k]);
+            double b = decode_e8m0(SFB[j * ld_sfb + k / 32]) * decode(dtB, B[j * ldb + k]);
+            double prod = a * b;
+            acc += prod;
+            mag += fabs(prod);
+        }
+        double r = alpha * acc;
+        if (beta != 0.0) r += beta * decode(dtC, C[i * ldc + j]);
+        ref[e] = r;
+        if (sumabs) sumabs[e] = mag;
+    }
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -40,6 +40,9 @@ def _load():
         lib.oracle_gemm_typed.restype = ci
         lib.oracle_gemm_typed.argtypes = [i64, i64, i64, dbl, vp, i64, ci, ci, vp, i64, ci, ci,
                                           dbl, vp, i64, ci, vp, vp, i64, vp, vp, ci]
+        lib.oracle_gemm_mx.restype = ci
+        lib.oracle_gemm_mx.argtypes = [i64, i64, i64, dbl, vp, i64, ci, vp, i64, vp, i64, ci, vp,
+                                       i64, dbl, vp, i64, ci, vp, vp, i64, vp, vp, ci]
         lib.oracle_decode.restype = None
         lib.oracle_decode.argtypes = [ctypes.c_int, vp, i64, vp]
         lib.oracle_round.restype = None
@@ -115,6 +118,41 @@ def gemm(M, N, K, alpha, A, lda, majorA, B, ldb, majorB, beta, C, ldc, dtype,
                                    threads)
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
+    if rows is None:
+        return ref.reshape(M, N), sab.reshape(M, N)
+    return ref, sab
+
+
+def gemm_mx(M, N, K, alpha, A, lda, a_dtype, SFA, ld_sfa, B, ldb, b_dtype, SFB, ld_sfb, beta, C,
+            ldc, dtype, rows=None, cols=None, threads=0):
+    """Block-scaled FP8 GEMM reference (see oracle_gemm_mx): K-major FP8 codes A (M x K) and
+    B (N rows of K) as uint16-widened codes, E8M0 scales SFA (M x ceil(K/32), row pitch
+    ld_sfa) and SFB (N x ceil(K/32), ld_sfb) as uint8, C in `dtype`.  Returns (ref, sumabs)
+    like ``gemm``."""
+    A = _bits(A)
+    B = _bits(B)
+    SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
+    SFB = np.ascontiguousarray(SFB, dtype=np.uint8)
+    Cp = None
+    if C is not None:
+        C = _bits(C)
+        Cp = C.ctypes.data
+    if rows is None:
+        n = M * N
+        r_p = c_p = None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        n = rows.size
+        r_p, c_p = rows.ctypes.data, cols.ctypes.data
+    ref = np.empty(n, dtype=np.float64)
+    sab = np.empty(n, dtype=np.float64)
+    rc = _load().oracle_gemm_mx(M, N, K, float(alpha), A.ctypes.data, lda, a_dtype, SFA.ctypes.data,
+                                ld_sfa, B.ctypes.data, ldb, b_dtype, SFB.ctypes.data, ld_sfb,
+                                float(beta), Cp, ldc, dtype, r_p, c_p, n, ref.ctypes.data,
+                                sab.ctypes.data, threads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_mx rejected its arguments")
     if rows is None:
         return ref.reshape(M, N), sab.reshape(M, N)
     return ref, sab
