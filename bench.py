@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (2MNK/s) at 8192^3 fp16->fp32 acc; % of GB300 dense FP16 peak"
 DEFAULT_WORKLOAD = "gemm8192_bf16_c"
+METRIC_MX = "GEMM TFLOP/s (2MNK/s) at 8192^3 block-scaled (MX) e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 METRIC_FP8 = "GEMM TFLOP/s (2MNK/s) at 8192^3 e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/ptx.cuh"]
@@ -199,8 +200,13 @@ def oracle_sample(problem, data, seconds, max_rows=None):
         rows = np.repeat(np.arange(r0, r0 + nrows, dtype=np.int64), ncols)
         cols = np.tile(cols_all[:ncols], nrows)
         t = time.perf_counter()
-        O.gemm(p.M, p.N, p.K, p.alpha, A, data["lda"], ma, B, data["ldb"], mb, p.beta, C, p.N,
-               code, rows, cols, threads=threads, a_dtype=a_code, b_dtype=b_code)
+        if p.scale_codes is not None:
+            O.gemm_mx(p.M, p.N, p.K, p.alpha, A, data["lda"], a_code, data["SFA"].numpy(), data["ld_sf"],
+                      B, data["ldb"], b_code, data["SFB"].numpy(), data["ld_sf"], p.beta, C, p.N, code,
+                      rows, cols, threads=threads)
+        else:
+            O.gemm(p.M, p.N, p.K, p.alpha, A, data["lda"], ma, B, data["ldb"], mb, p.beta, C, p.N,
+                   code, rows, cols, threads=threads, a_dtype=a_code, b_dtype=b_code)
         return time.perf_counter() - t
 
     # probe with a slice of one row, then size the sample to the time budget
@@ -243,7 +249,8 @@ def run_reference(args):
         secs += last["seconds"]
     value = flops / secs / 1e12
     line = {
-        "impl": "reference", "metric": METRIC_FP8 if p.a_fmt else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": (METRIC_MX if p.scale_codes else METRIC_FP8) if p.a_fmt else METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(p),
@@ -291,10 +298,14 @@ def run_gb300(args):
     from layout_algebra_gb300 import workloads as W
     p = problem_of(args.workload)
     f8 = p.a_fmt is not None
+    mx = p.scale_codes is not None
     out_dt = W.torch_dtype(p.dtype)
     data = W.make(p)
     A, B = data["A"].to(dev), data["B"].to(dev)
     C = data["C"].to(dev) if data["C"] is not None else None
+    if mx:   # scales packed once, outside the timed region
+        sfa = G.mx_pack_scales(0, p.M, p.K, data["SFA"].to(dev), data["ld_sf"])
+        sfb = G.mx_pack_scales(1, p.N, p.K, data["SFB"].to(dev), data["ld_sf"])
     D = torch.empty(p.M * p.N, dtype=out_dt, device=dev)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
@@ -316,7 +327,14 @@ def run_gb300(args):
     dcode = 1 if out_dt == torch.bfloat16 else 0
 
     def launch():
-        if f8:
+        if mx:
+            st = G.lib().gb_gemm_mxfp8(G.fp8_format(p.a_fmt), G.fp8_format(p.b_fmt), dcode, p.M, p.N, p.K,
+                                       p.alpha, A.data_ptr(), lda, sfa.data_ptr(), B.data_ptr(), ldb,
+                                       sfb.data_ptr(), p.beta, cptr, D.data_ptr(),
+                                       ctypes.byref(epi) if epi is not None else None,
+                                       ws.data_ptr() if ws is not None else None,
+                                       ws.numel() if ws is not None else 0, sh)
+        elif f8:
             st = G.lib().gb_gemm_fp8(G.fp8_format(p.a_fmt), G.fp8_format(p.b_fmt), dcode, p.M, p.N,
                                      p.K, p.alpha, A.data_ptr(), lda, B.data_ptr(), ldb, p.beta,
                                      cptr, D.data_ptr(),
@@ -379,8 +397,21 @@ def run_gb300(args):
     C_h = data["C"].pin_memory() if data["C"] is not None else None
     D_h = torch.empty(p.M * p.N, dtype=out_dt, pin_memory=True)
 
+    if mx:
+        SFA_h, SFB_h = data["SFA"].pin_memory(), data["SFB"].pin_memory()
+
     def public_call():
-        if f8:
+        if mx:
+            # host operands and plain scales in, D out: copies, packing and the GEMM
+            Ad, Bd = A_h.to(dev, non_blocking=True), B_h.to(dev, non_blocking=True)
+            Cd = C_h.to(dev, non_blocking=True) if C_h is not None else None
+            pa = G.mx_pack_scales(0, p.M, p.K, SFA_h.to(dev, non_blocking=True), data["ld_sf"])
+            pb = G.mx_pack_scales(1, p.N, p.K, SFB_h.to(dev, non_blocking=True), data["ld_sf"])
+            Dd = G.gemm_mxfp8(Ad, Bd, p.M, p.N, p.K, lda=lda, ldb=ldb, sfa=pa, sfb=pb, a_format=p.a_fmt,
+                              b_format=p.b_fmt, out_dtype=out_dt, alpha=p.alpha, beta=p.beta, C=Cd,
+                              workspace=ws)
+            D_h.copy_(Dd, non_blocking=True)
+        elif f8:
             G.gemm_fp8(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, a_format=p.a_fmt,
                        b_format=p.b_fmt, out_dtype=out_dt, alpha=p.alpha, beta=p.beta, C=C_h,
                        D=D_h, workspace=ws)
@@ -403,7 +434,8 @@ def run_gb300(args):
     torch.cuda.synchronize()
     barrier(world, local)
     e2e_s, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, float(p.flops) * e2e_steps, world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (data["A"], data["B"], data["C"]) if t is not None)
+    h2d = sum(t.numel() * t.element_size()
+              for t in (data["A"], data["B"], data["C"], data.get("SFA"), data.get("SFB")) if t is not None)
     d2h = p.M * p.N * 2
     st, detail = G.last_device_status()
     if st != 0:
@@ -440,7 +472,11 @@ def run_gb300(args):
     }
     line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
                                      if ws is not None else "gb_gemm_%s" % p.dtype)
-    if f8:
+    if mx:
+        line["config"]["entry_point"] = "gb_gemm_mxfp8" + (" (workspace)" if ws is not None else "")
+        line["config"]["scales"] = "E8M0 per 32 K elements of each row of A and column of B, codes %d..%d" % p.scale_codes
+        line["metric"] = METRIC_MX
+    elif f8:
         line["config"]["entry_point"] = "gb_gemm_fp8" + (" (workspace)" if ws is not None else "")
     elif epi is not None:
         line["config"]["entry_point"] = "gb_gemm_ex"

@@ -155,6 +155,40 @@ gb_status gb_gemm_fp8(int a_format, int b_format, int out_dtype, int64_t M, int6
                       float beta, const void* C, void* D, const gb_epilogue* epi,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Block-scaled FP8 GEMM ("MX": the per-block scale factors of "CUTLASS, in depth" —
+   "Epilogue fusion" and "Numerics", read as the OCP Microscaling format).  Every 32
+   consecutive K elements of a row of A, and of a column of B, share one E8M0 scale
+   2^(e - 127) (e = 255 is NaN):
+     D = epilogue(alpha * sum_k (2^(sa(i,k/32)-127) A(i,k)) (2^(sb(j,k/32)-127) B(k,j)) + beta*C)
+   computed on the tensor cores (kind::mxf8f6f4, fp32 accumulation).  A and B are as for
+   gb_gemm_fp8 (K-major FP8 codes of a_format / b_format, lda and ldb multiples of 16).
+   sfa and sfb are the scales packed by gb_mx_pack_scales (operand 0 for A with M rows,
+   operand 1 for B with N rows), 16-byte aligned device buffers.  C, D, epi, workspace and
+   stream as for gb_gemm_fp8.  Errors as for gb_gemm_fp8, plus GB_ERR_INVALID_ARG for a
+   missing scale buffer when K > 0.  Uses the single-CTA kernel for M <= 128 and the
+   CTA-pair kernel otherwise (variant 3 runs as variant 2). */
+gb_status gb_gemm_mxfp8(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K,
+                        float alpha, const void* A, int64_t lda, const void* sfa,
+                        const void* B, int64_t ldb, const void* sfb,
+                        float beta, const void* C, void* D, const gb_epilogue* epi,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Packed scale factors for gb_gemm_mxfp8.  The kernels read scales in 512-byte atoms, each
+   covering 128 rows (or columns) and one k-block of 128 elements (4 scales per row): scale
+   (row 32j + i, scale kk of the k-block) at byte 16i + 4j + kk of the atom, i.e. the layout
+   ((32,4),4):((16,4),1) from (row, scale) to bytes.  Operand 0 (A, rows = M): one atom per
+   (128 rows, k-block), atom (rb, kb) at byte (rb * ceil(K/128) + kb) * 512.  Operand 1 (B,
+   rows = N): 1024 bytes per (224 columns, k-block) at (nb * ceil(K/128) + kb) * 1024, the
+   seven 32-column groups g of the block in atom g / 4, slot g % 4 (the eighth slot is
+   padding).  Padding holds 127 (a scale of 1).
+   gb_mx_scales_bytes: size of the packed buffer.  gb_mx_pack_scales: fill `dst` (device,
+   that size) from `src` (device, rows x ceil(K/32) E8M0 bytes, row pitch ld_src >=
+   ceil(K/32)), asynchronously on `stream`.  GB_ERR_INVALID_ARG for a bad operand, negative
+   sizes or a short pitch. */
+gb_status gb_mx_scales_bytes(int operand, int64_t rows, int64_t K, size_t* bytes);
+gb_status gb_mx_pack_scales(int operand, int64_t rows, int64_t K, const void* src, int64_t ld_src,
+                            void* dst, void* stream);
+
 /* Allocation-free GEMM (no counterpart on the pages: an addition for callers that may not
    allocate device memory).  Some callers cannot call cudaMalloc at the point where they
    run a GEMM: code inside a runtime that owns every byte of device memory (a serving

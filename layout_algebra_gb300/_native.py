@@ -14,7 +14,8 @@ GEMM_SYMBOLS = [
     "gb_gemm_make_plan", "gb_set_wait_timeout_ns", "gb_debug_skip_k_block",
     "gb_debug_epilogue_map", "gb_debug_stage_bytes", "gb_set_kernel_variant",
     "gb_gemm_f16_ws", "gb_gemm_bf16_ws", "gb_gemm_workspace_bytes", "gb_set_schedule",
-    "gb_gemm_noalloc", "gb_gemm_ex", "gb_gemm_fp8",
+    "gb_gemm_noalloc", "gb_gemm_ex", "gb_gemm_fp8", "gb_gemm_mxfp8", "gb_mx_scales_bytes",
+    "gb_mx_pack_scales",
 ]
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
@@ -75,6 +76,13 @@ def lib():
     L.gb_gemm_fp8.restype = ci
     L.gb_gemm_fp8.argtypes = [ci, ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, vp,
                               ctypes.POINTER(Epilogue), vp, sz, vp]
+    L.gb_gemm_mxfp8.restype = ci
+    L.gb_gemm_mxfp8.argtypes = [ci, ci, ci, i64, i64, i64, f32, vp, i64, vp, vp, i64, vp, f32, vp, vp,
+                                ctypes.POINTER(Epilogue), vp, sz, vp]
+    L.gb_mx_scales_bytes.restype = ci
+    L.gb_mx_scales_bytes.argtypes = [ci, i64, i64, ctypes.POINTER(sz)]
+    L.gb_mx_pack_scales.restype = ci
+    L.gb_mx_pack_scales.argtypes = [ci, i64, i64, vp, i64, vp, vp]
     L.gb_gemm_noalloc.restype = ci
     L.gb_gemm_noalloc.argtypes = [ci, i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp]
     L.gb_gemm_workspace_bytes.restype = ci

@@ -175,6 +175,50 @@ def gemm_fp8(A, B, M, N, K, *, lda, ldb, a_format=None, b_format=None, out_dtype
     return D
 
 
+def mx_scales_bytes(operand, rows, K):
+    """Bytes of the packed scale buffer of operand 0 (A, rows = M) or 1 (B, rows = N)."""
+    n = ctypes.c_size_t()
+    st = lib().gb_mx_scales_bytes(int(operand), rows, K, ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "mx_scales_bytes")
+    return n.value
+
+
+def mx_pack_scales(operand, rows, K, scales, ld=None, stream=None):
+    """Pack rows x ceil(K/32) E8M0 scales (a uint8 device tensor, row pitch ld) for
+    gemm_mxfp8; returns the packed uint8 device tensor."""
+    ld = -(-K // 32) if ld is None else ld
+    out = torch.empty(mx_scales_bytes(operand, rows, K), dtype=torch.uint8, device=scales.device)
+    st = lib().gb_mx_pack_scales(int(operand), rows, K, _ptr(scales), ld, _ptr(out),
+                                 _stream_handle(stream))
+    if st != 0:
+        raise GemmError(st, "mx_pack_scales")
+    return out
+
+
+def gemm_mxfp8(A, B, M, N, K, *, lda, ldb, sfa, sfb, a_format=None, b_format=None,
+               out_dtype=torch.bfloat16, alpha=1.0, beta=0.0, C=None, bias=None, activation="none",
+               amax=None, out_format="input", out_scale=1.0, D=None, workspace=None, stream=None):
+    """Block-scaled FP8 GEMM through gb_gemm_mxfp8 (device tensors).  A, B as for gemm_fp8;
+    sfa / sfb are packed scales from mx_pack_scales (operand 0 with M rows, 1 with N rows)."""
+    fa = fp8_format(a_format if a_format is not None else A.dtype)
+    fb = fp8_format(b_format if b_format is not None else B.dtype)
+    od = dtype_code(out_dtype)
+    fmt = OUT_FORMATS[out_format]
+    if D is None:
+        dd = {0: out_dtype, 1: torch.float8_e4m3fn, 2: torch.float8_e5m2}[fmt]
+        D = torch.empty(M * N, dtype=dd, device=A.device)
+    epi = Epilogue(_ptr(bias), ACTIVATIONS[activation], _ptr(amax), fmt, float(out_scale))
+    st = lib().gb_gemm_mxfp8(fa, fb, od, M, N, K, float(alpha), _ptr(A), lda, _ptr(sfa), _ptr(B), ldb,
+                             _ptr(sfb), float(beta), _ptr(C), _ptr(D), ctypes.byref(epi),
+                             _ptr(workspace),
+                             0 if workspace is None else workspace.numel() * workspace.element_size(),
+                             _stream_handle(stream))
+    if st != 0:
+        raise GemmError(st, "gemm_mxfp8")
+    return D
+
+
 def raw_call(dtype, M, N, K, alpha, A_ptr, lda, majorA, B_ptr, ldb, majorB, beta, C_ptr, D_ptr,
              stream_handle):
     """Direct C-ABI call with integer pointers; returns the status code."""

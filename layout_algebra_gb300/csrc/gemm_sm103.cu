@@ -70,32 +70,49 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 //         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
 //         the copy side's time did not drop with the 25 % fewer bytes (it follows the count
 //         of pipeline stages), so 256-column tiles with the overlapped epilogue stay.
-template <bool kPair>
+// Input kinds: 16-bit (fp16/bf16, kind::f16), FP8 (kind::f8f6f4) and block-scaled FP8
+// (kind::mxf8f6f4 with one E8M0 scale per 32 K elements of each row of A and column of B).
+enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
+
+// Block-scaled FP8 uses 224-column tiles: two accumulators (at TMEM columns 0 and 256) and,
+// in the 32 columns behind each, one slot of scale factors (4 columns for A's 128 rows, 8
+// for B's columns), so the epilogue still overlaps the next tile.
+constexpr int kMxTileN = 224;
+constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
+
+template <bool kPair, int kIn = kIn16>
 struct Cfg {
+  static constexpr bool kMx = kIn == kInMx;
   static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kTileN = kPair ? kPairTileN : kBN;
-  static constexpr int kNSub = kTileN / kBN;                  // MMAs per K step (along N)
-  static constexpr int kRowsBSub = kPair ? kBN / 2 : kBN;    // B rows a CTA stages per MMA
-  static constexpr int kRowsB = kRowsBSub * kNSub;          // B rows a CTA stages per k-block
-  static constexpr int kAccBufs = kTmemCols / kTileN;       // accumulators in TMEM
-  static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1; // 64-wide k-blocks per stage
+  static constexpr int kTileN = kMx ? kMxTileN : (kPair ? kPairTileN : kBN);
+  static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
+  static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
+  static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
+  static constexpr int kRowsB = kRowsBSub * kNSub;                // B rows a CTA stages per k-block
+  static constexpr int kAccBufs = kMx ? 2 : kTmemCols / kTileN;   // accumulators in TMEM
+  static constexpr int kAccStride = kMx ? 256 : kTileN;           // TMEM columns between them
+  static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1;       // k-blocks per stage
   static constexpr int kStages = (kPair && kNSub == 1) ? 3 : 4;
   static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;      // producer, MMA, epilogue warps
-  static constexpr int kAHalf = kRowsA * kBK * 2;          // one k-block of A (bytes)
-  static constexpr int kBSub = kRowsBSub * kBK * 2;        // one k-block of one MMA's B rows
-  static constexpr int kBHalf = kRowsB * kBK * 2;          // one k-block of B (bytes)
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;            // producer, MMA, epilogue warps
+  static constexpr int kAHalf = kRowsA * kBK * 2;                // one k-block of A (bytes)
+  static constexpr int kBSub = kRowsBSub * kBK * 2;              // one k-block of one MMA's B rows
+  static constexpr int kBHalf = kRowsB * kBK * 2;                // one k-block of B (bytes)
+  static constexpr int kSfBytes = kMx ? kMxSfBytes : 0;          // one k-block's scale factors
   static constexpr int kAStage = kAHalf * kKB;
   static constexpr int kBStage = kBHalf * kKB;
-  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kSfOff = kAStage + kBStage;               // scale factors after A and B
+  // stage bases stay 1024-byte aligned (the swizzle atom)
+  static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
   // bytes one k-block adds to the (even CTA's) full barrier: both CTAs' copies in a pair
-  static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf) * (kPair ? 2 : 1);
+  static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf + kSfBytes) * (kPair ? 2 : 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
   static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
   static_assert(kStages <= kMaxStages, "control block");
-  static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kBN == 0, "TMEM accumulators");
+  static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kNSub == 0, "TMEM accumulators");
+  static_assert(!kMx || (kTileN <= 224 && kTileN % 32 == 0 && kBSub % 1024 == 0), "MX tile");
 };
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -370,10 +387,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k
   return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
 }
 
-template <bool kPair, bool kMc>
-__device__ void run_producer(const Params& p, const void* tmA, const void* tmB, uint8_t* smem,
-                             Ctl* ctl, uint32_t rank, uint32_t cluster, uint32_t nclusters) {
-  using C = Cfg<kPair>;
+template <bool kPair, int kIn, bool kMc>
+__device__ void run_producer(const Params& p, const void* tmA, const void* tmB, const void* tmSFA,
+                             const void* tmSFB, uint8_t* smem, Ctl* ctl, uint32_t rank, uint32_t cluster,
+                             uint32_t nclusters) {
+  using C = Cfg<kPair, kIn>;
+  static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
   // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
   int stage = 0;
@@ -420,7 +439,22 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
 #pragma unroll
             for (int j = 0; j < C::kNSub; ++j)
               issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
-                                   full_tgt, b_row0 + j * kBN, C::kRowsBSub, kb, p.bk_elems);
+                                   full_tgt, b_row0 + j * C::kMmaN, C::kRowsBSub, kb, p.bk_elems);
+          }
+          if constexpr (C::kMx) {
+            // scale factors, packed in 512-byte atoms (two 256-byte rows of the scale maps):
+            // A's atom of this CTA's 128 rows, then B's two atoms of the tile's columns
+            // (every CTA of a pair holds all of them)
+            const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
+            const int32_t rb = a_row0 / kRowsA;
+            const int32_t ya = 2 * (rb * p.k_blocks + kb), yb = 4 * (nt * p.k_blocks + kb);
+            if constexpr (kPair) {
+              tma_load_2d_pair(sf, tmSFA, full_tgt, 0, ya);
+              tma_load_2d_pair(sf + 512, tmSFB, full_tgt, 0, yb);
+            } else {
+              tma_load_2d(sf, tmSFA, full_tgt, 0, ya);
+              tma_load_2d(sf + 512, tmSFB, full_tgt, 0, yb);
+            }
           }
         }
         issued |= 1u << stage;
@@ -455,10 +489,11 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   }
 }
 
-template <bool kPair, bool kF8, bool kMc>
+template <bool kPair, int kIn, bool kMc>
 __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
                         uint32_t cluster, uint32_t nclusters) {
-  using C = Cfg<kPair>;
+  using C = Cfg<kPair, kIn>;
+  uint32_t kbc = 0;                        // k-blocks issued: selects the scale-factor slot
   if (kPair && (rank & 1u) != 0) return;   // the even CTA issues for the pair
   // a stage is free once every pair reading it has finished: with B multicast the other
   // pair's copies land in this pair's stages too, so releases go to all four CTAs
@@ -480,7 +515,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       break;
     }
     tc_fence_after_sync();
-    const uint32_t d_tmem = tmem_base + buf * C::kTileN;
+    const uint32_t d_tmem = tmem_base + buf * C::kAccStride;
     for (int32_t sbk = item.sb0; sbk < item.sb1; ++sbk) {
       if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
         ok = false;
@@ -496,24 +531,51 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       const uint32_t ka = p.majorA == 0 ? (kUmmaK * 2) >> 4 : (kUmmaK * 128) >> 4;
       const uint32_t kb_ = p.majorB == 0 ? (kUmmaK * 2) >> 4 : (kUmmaK * 128) >> 4;
       for (int h = 0; h < nkb; ++h) {
+        uint32_t sfa = 0, sfb = 0;
+        if constexpr (C::kMx) {
+          // this k-block's scale factors into a TMEM slot behind an accumulator (two slots
+          // alternate; copies and MMAs of one thread execute in issue order)
+          const uint32_t slot = tmem_base + C::kTileN + (kbc & 1u) * C::kAccStride;
+          const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
+          sfa = slot;
+          sfb = slot + 4;
+          if constexpr (kPair) {
+            tc_cp_32x128b_x4_pair(sfa, smem_desc_plain(sf, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb, smem_desc_plain(sf + 512, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+          } else {
+            tc_cp_32x128b_x4(sfa, smem_desc_plain(sf, 0, 128));
+            tc_cp_32x128b_x4(sfb, smem_desc_plain(sf + 512, 0, 128));
+            tc_cp_32x128b_x4(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+          }
+        }
+        ++kbc;
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k) {
           const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
           const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
-          // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and 256
-          // columns; the N sub-tiles share the A slice
+          // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and up to
+          // 256 columns; the N sub-tiles share the A slice
 #pragma unroll
           for (int j = 0; j < C::kNSub; ++j) {
             const uint64_t db = db0 + ((h * C::kBHalf + j * C::kBSub) >> 4) + k * kb_;
-            const uint32_t dt = d_tmem + j * kBN;
-            if constexpr (kPair && kF8)
+            const uint32_t dt = d_tmem + j * C::kMmaN;
+            if constexpr (C::kMx) {
+              // the k-th 32-element slice takes scale byte k of each 32-bit scale cell
+              const uint32_t id = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+              if constexpr (kPair)
+                tc_mma_mx_pair(dt, da, db, id, sfa, sfb, acc);
+              else
+                tc_mma_mx(dt, da, db, id, sfa, sfb, acc);
+            } else if constexpr (kPair && kIn == kIn8) {
               tc_mma_f8_pair(dt, da, db, p.idesc, acc);
-            else if constexpr (kPair)
+            } else if constexpr (kPair) {
               tc_mma_f16_pair(dt, da, db, p.idesc, acc);
-            else if constexpr (kF8)
+            } else if constexpr (kIn == kIn8) {
               tc_mma_f8(dt, da, db, p.idesc, acc);
-            else
+            } else {
               tc_mma_f16(dt, da, db, p.idesc, acc);
+            }
           }
         }
       }
@@ -712,10 +774,10 @@ __device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl
   return ok != 0;
 }
 
-template <bool kBF16, bool kPair, bool kMc>
+template <bool kBF16, bool kPair, int kIn, bool kMc>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters) {
-  using C = Cfg<kPair>;
+  using C = Cfg<kPair, kIn>;
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
@@ -771,7 +833,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       const bool vec_run = cvec && c0 + 32 <= cend;
       const bool next_vec = cvec && c0 + 64 <= cend;
       if (p.k_blocks > 0)
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kTileN + c0, acc);
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
       if (next_vec) {   // issued while the TMEM load is in flight
         const uint4* src = reinterpret_cast<const uint4*>(p.C + base + c0 + 32);
 #pragma unroll
@@ -837,11 +899,12 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <bool kBF16, bool kPair, bool kF8, bool kMc = false>
-__global__ void __launch_bounds__(Cfg<kPair>::kThreads, 1)
+template <bool kBF16, bool kPair, int kIn, bool kMc = false>
+__global__ void __launch_bounds__(Cfg<kPair, kIn>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const Params p) {
-  using C = Cfg<kPair>;
+  using C = Cfg<kPair, kIn>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStages * C::kStageBytes);
@@ -867,6 +930,10 @@ __global__ void __launch_bounds__(Cfg<kPair>::kThreads, 1)
     if (p.k_blocks > 0) {
       prefetch_tensormap(&tmA);
       prefetch_tensormap(&tmB);
+      if constexpr (C::kMx) {
+        prefetch_tensormap(&tmSFA);
+        prefetch_tensormap(&tmSFB);
+      }
     }
   }
   if (warp == 1) {
@@ -885,13 +952,14 @@ __global__ void __launch_bounds__(Cfg<kPair>::kThreads, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<kPair, kMc>(p, &tmA, &tmB, smem, ctl, rank, cluster, nclusters);
+    if (lane == 0)
+      run_producer<kPair, kIn, kMc>(p, &tmA, &tmB, &tmSFA, &tmSFB, smem, ctl, rank, cluster, nclusters);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<kPair, kF8, kMc>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
+    if (lane == 0) run_mma<kPair, kIn, kMc>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
-    run_epilogue<kBF16, kPair, kMc>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
+    run_epilogue<kBF16, kPair, kIn, kMc>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
   }
 
   tc_fence_before_sync();
@@ -904,6 +972,37 @@ __global__ void __launch_bounds__(Cfg<kPair>::kThreads, 1)
     else
       tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// ------------------------------------------------------------------ scale-factor packing
+// Block-scaled FP8 reads its E8M0 scales in 512-byte atoms, each holding 4 k-slices of 32
+// elements (one k-block of 128) for 128 rows: scale (row 32 j + i, slice kk) at byte
+// 16 i + 4 j + kk, the layout ((32,4),4):((16,4),1) from (row, slice) to bytes.  A packs one
+// atom per (128 rows, k-block), atom (rb, kb) at (rb * KB + kb) * 512; B packs two atoms per
+// (224 columns, k-block) at (nb * KB + kb) * 1024, its 32-column groups g = 0..6 in atom
+// g / 4, group slot g % 4 (slot 3 of the second atom is padding).  Padding holds 127 (1.0).
+__global__ void mx_pack_kernel(int operand, int64_t rows, int64_t K, const uint8_t* src, int64_t ld,
+                               uint8_t* dst, int64_t total) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total) return;
+  const int64_t kbs = (K + 127) / 128, nsf = (K + 31) / 32;
+  const int64_t atom_bytes = operand == 0 ? 512 : 1024;
+  const int64_t blk = idx / atom_bytes, w = idx % atom_bytes;
+  const int64_t rb = blk / kbs, kb = blk % kbs;
+  const int64_t w2 = w % 512;
+  const int64_t i = w2 / 16, slot = (w2 / 4) % 4, kk = w2 % 4;
+  int64_t r;
+  bool valid;
+  if (operand == 0) {
+    r = rb * 128 + 32 * slot + i;
+    valid = true;
+  } else {
+    const int64_t g = (w / 512) * 4 + slot;
+    r = rb * kMxTileN + 32 * g + i;
+    valid = g < kMxTileN / 32;
+  }
+  const int64_t sfi = kb * 4 + kk;
+  dst[idx] = (valid && r < rows && sfi < nsf) ? src[r * ld + sfi] : static_cast<uint8_t>(127);
 }
 
 // ------------------------------------------------------------------ test kernels
@@ -969,9 +1068,9 @@ bool is_pair(int variant) { return variant == kVariantPair || variant == kVarian
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
-  bool attr_single[2][2] = {{false, false}, {false, false}};   // [bf16 out][fp8 in]
-  bool attr_pair[2][2] = {{false, false}, {false, false}};
-  bool attr_mc[2][2] = {{false, false}, {false, false}};
+  bool attr_single[2][3] = {};   // [bf16 out][input kind]
+  bool attr_pair[2][3] = {};
+  bool attr_mc[2][3] = {};
   int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
   int mc_clusters = 0;     // co-resident 4-CTA clusters of the multicast kernel
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
@@ -1007,10 +1106,22 @@ struct InType {
   int a_fmt, b_fmt;   // instruction-descriptor formats: 0 fp16 / E4M3, 1 bf16 / E5M2
   bool f8;
   int bytes;          // 2 or 1
+  bool mx = false;    // block-scaled FP8 (E8M0 scales per 32 K elements)
   int bk() const { return 128 / bytes; }
+  int kind() const { return mx ? gb::kInMx : (f8 ? gb::kIn8 : gb::kIn16); }
 };
 
-InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false, 2}; }
+InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false, 2, false}; }
+
+// Tile width and the B rows one copy stages per CTA, per variant and input kind.
+int64_t tile_n_of(bool pair, const InType& in) {
+  if (in.mx) return gb::kMxTileN;
+  return pair ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
+}
+int64_t mma_n_of(bool pair, const InType& in) {
+  if (in.mx) return gb::kMxTileN;
+  return pair ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
+}
 
 gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t tile_rows,
                        int64_t cta_rows, OperandPlan* o, const InType& in) {
@@ -1058,14 +1169,17 @@ gb_status validate_sizes(int64_t M, int64_t N, int64_t K, int64_t lda, int major
   return GB_OK;
 }
 
-uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m) {
+uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mma_n) {
   uint32_t d = 0;
-  d |= 1u << 4;                                        // accumulator format: fp32
+  if (in.mx)
+    d |= 1u << 23;                                     // scale factors: E8M0 (bits 4-5, 29-30: ids)
+  else
+    d |= 1u << 4;                                      // accumulator format: fp32
   d |= static_cast<uint32_t>(in.a_fmt) << 7;           // A format: 0 fp16/E4M3, 1 bf16/E5M2
   d |= static_cast<uint32_t>(in.b_fmt) << 10;          // B format
   d |= static_cast<uint32_t>(majorA) << 15;            // A: 0 K-major, 1 MN-major
   d |= static_cast<uint32_t>(majorB) << 16;            // B: 0 K-major, 1 MN-major
-  d |= static_cast<uint32_t>(gb::kBN >> 3) << 17;      // N / 8
+  d |= static_cast<uint32_t>(mma_n >> 3) << 17;        // N / 8
   d |= static_cast<uint32_t>(tile_m >> 4) << 24;       // M / 16 (256 for a CTA pair)
   return d;
 }
@@ -1089,9 +1203,11 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   if (variant != kVariantSingle && !is_pair(variant)) return GB_ERR_INVALID_ARG;
   const bool pair = is_pair(variant);
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
-  const int64_t tile_n = pair ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
-  // B rows one copy stages: with multicast each CTA copies a quarter of the pair's 256
-  int64_t rows_b = pair ? gb::Cfg<true>::kRowsBSub : gb::Cfg<false>::kRowsBSub;
+  if (in.mx && variant == kVariantPairMc) return GB_ERR_INVALID_ARG;
+  const int64_t tile_n = tile_n_of(pair, in);
+  // B rows one copy stages: one CTA's share of one MMA's columns; with multicast each CTA
+  // copies a quarter of the pair's 256
+  int64_t rows_b = pair ? mma_n_of(pair, in) / 2 : mma_n_of(pair, in);
   if (variant == kVariantPairMc) rows_b = gb::kSwz;
   std::memset(pl, 0, sizeof(*pl));
   pl->variant = variant;
@@ -1137,14 +1253,14 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   } catch (const la::Error&) {
     return GB_ERR_INVALID_ARG;
   }
-  pl->instr_desc = make_idesc(in, majorA, majorB, static_cast<int>(tile_m));
+  pl->instr_desc = make_idesc(in, majorA, majorB, static_cast<int>(tile_m), static_cast<int>(mma_n_of(pair, in)));
   return GB_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
-                     const int64_t box[2], int dtype, bool f8 = false) {
+                     const int64_t box[2], int dtype, bool f8 = false, bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return GB_ERR_LAUNCH;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(dim[0]), static_cast<cuuint64_t>(dim[1])};
@@ -1156,7 +1272,8 @@ gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], i
                                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
   CUresult r = fn(map, t,
                   2, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
 }
@@ -1213,27 +1330,31 @@ void fill_params(const gb_gemm_plan& pl, int64_t M, int64_t N, int64_t K, float 
   p->skip_kb = g_skip_kb;
 }
 
-template <bool kBF16, bool kF8>
-gb_status launch_single(DeviceState* dev, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                        int grid, cudaStream_t s) {
-  using C = gb::Cfg<false>;
-  if (!dev->attr_single[kBF16][kF8]) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+// The tensor maps of one call: A, B and, for block-scaled inputs, the packed scale factors.
+struct Maps {
+  CUtensorMap a, b, sfa, sfb;
+};
+
+template <bool kBF16, int kIn>
+gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s) {
+  using C = gb::Cfg<false, kIn>;
+  if (!dev->attr_single[kBF16][kIn]) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    dev->attr_single[kBF16][kF8] = true;
+    dev->attr_single[kBF16][kIn] = true;
   }
-  gb::gemm_kernel<kBF16, false, kF8><<<grid, C::kThreads, C::kSmemBytes, s>>>(tmA, tmB, p);
+  gb::gemm_kernel<kBF16, false, kIn><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
-template <bool kBF16, bool kF8, bool kMc>
+template <bool kBF16, int kIn, bool kMc>
 gb_status prepare_pair(DeviceState* dev) {
-  using C = gb::Cfg<true>;
+  using C = gb::Cfg<true, kIn>;
   constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
-  bool& attr = kMc ? dev->attr_mc[kBF16][kF8] : dev->attr_pair[kBF16][kF8];
+  bool& attr = kMc ? dev->attr_mc[kBF16][kIn] : dev->attr_pair[kBF16][kIn];
   if (!attr) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kF8, kMc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kMc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
     attr = true;
@@ -1253,7 +1374,7 @@ gb_status prepare_pair(DeviceState* dev) {
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(kCl * (dev->sms / kCl), 1, 1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kF8, kMc>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kMc>, &cfg) != cudaSuccess ||
         n <= 0)
       n = dev->sms / kCl;
     clusters = std::min(n, dev->sms / kCl);
@@ -1261,10 +1382,9 @@ gb_status prepare_pair(DeviceState* dev) {
   return GB_OK;
 }
 
-template <bool kBF16, bool kF8, bool kMc>
-gb_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p, int clusters,
-                      cudaStream_t s) {
-  using C = gb::Cfg<true>;
+template <bool kBF16, int kIn, bool kMc>
+gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s) {
+  using C = gb::Cfg<true, kIn>;
   constexpr int kCl = kMc ? 4 : 2;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1278,26 +1398,33 @@ gb_status launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const Para
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(kCl * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kF8, kMc>, tmA, tmB, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kMc>, m.a, m.b, m.sfa, m.sfb, p) != cudaSuccess)
     return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
-// Dispatch on the output type and the two pair kernels.
-template <bool kF8>
-gb_status prepare_pair_any(bool bf, bool mc, DeviceState* dev) {
-  if (mc) return bf ? prepare_pair<true, kF8, true>(dev) : prepare_pair<false, kF8, true>(dev);
-  return bf ? prepare_pair<true, kF8, false>(dev) : prepare_pair<false, kF8, false>(dev);
+// Dispatch on the output type, the input kind and the two pair kernels (the multicast
+// pair takes 16-bit and FP8 inputs).
+template <bool kBF16>
+gb_status prepare_pair_any(int kin, bool mc, DeviceState* dev) {
+  if (mc) return kin == gb::kIn8 ? prepare_pair<kBF16, gb::kIn8, true>(dev) : prepare_pair<kBF16, gb::kIn16, true>(dev);
+  if (kin == gb::kInMx) return prepare_pair<kBF16, gb::kInMx, false>(dev);
+  return kin == gb::kIn8 ? prepare_pair<kBF16, gb::kIn8, false>(dev) : prepare_pair<kBF16, gb::kIn16, false>(dev);
 }
 
-template <bool kF8>
-gb_status launch_pair_any(bool bf, bool mc, const CUtensorMap& tmA, const CUtensorMap& tmB, const Params& p,
-                          int clusters, cudaStream_t s) {
-  if (mc)
-    return bf ? launch_pair<true, kF8, true>(tmA, tmB, p, clusters, s)
-              : launch_pair<false, kF8, true>(tmA, tmB, p, clusters, s);
-  return bf ? launch_pair<true, kF8, false>(tmA, tmB, p, clusters, s)
-            : launch_pair<false, kF8, false>(tmA, tmB, p, clusters, s);
+template <bool kBF16>
+gb_status launch_any(bool pair, int kin, bool mc, DeviceState* dev, const Maps& m, const Params& p, int G,
+                     cudaStream_t s) {
+  if (!pair) {
+    if (kin == gb::kInMx) return launch_single<kBF16, gb::kInMx>(dev, m, p, G, s);
+    return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8>(dev, m, p, G, s)
+                           : launch_single<kBF16, gb::kIn16>(dev, m, p, G, s);
+  }
+  if (mc) return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, true>(m, p, G, s)
+                                 : launch_pair<kBF16, gb::kIn16, true>(m, p, G, s);
+  if (kin == gb::kInMx) return launch_pair<kBF16, gb::kInMx, false>(m, p, G, s);
+  return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, false>(m, p, G, s)
+                         : launch_pair<kBF16, gb::kIn16, false>(m, p, G, s);
 }
 
 // Workspace layout: one 32-bit flag per CTA (padded to 256 B), then one 128 x 256 fp32
@@ -1310,12 +1437,14 @@ int64_t workspace_bytes_for(int sms) {
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
                      void* workspace, size_t workspace_size, void* stream, const gb_epilogue* epi = nullptr,
-                     const InType* in_f8 = nullptr) {
+                     const InType* in_f8 = nullptr, const void* sfa = nullptr, const void* sfb = nullptr) {
   // dtype names the 16-bit type of C, D and the bias; the inputs share it unless in_f8 names
-  // 8-bit input formats
+  // 8-bit input formats (with packed scale factors sfa / sfb when block-scaled)
   const InType in = in_f8 ? *in_f8 : in16(dtype);
+  int variant = choose_variant(M);
+  if (in.mx && variant == kVariantPairMc) variant = kVariantPair;   // no multicast form
   gb_gemm_plan pl;
-  gb_status st = make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, &pl, &in);
+  gb_status st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in);
   if (st != GB_OK) return st;
   if (M == 0 || N == 0) return GB_OK;
   if (D == nullptr) return GB_ERR_INVALID_ARG;
@@ -1337,12 +1466,23 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
 
-  CUtensorMap tmA, tmB;
-  std::memset(&tmA, 0, sizeof(tmA));
-  std::memset(&tmB, 0, sizeof(tmB));
+  Maps maps;
+  std::memset(&maps, 0, sizeof(maps));
   if (K > 0) {
-    if ((st = encode_map(&tmA, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
-    if ((st = encode_map(&tmB, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
+    if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
+    if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
+    if (in.mx) {
+      if (sfa == nullptr || sfb == nullptr) return GB_ERR_INVALID_ARG;
+      if (!aligned16(sfa) || !aligned16(sfb)) return GB_ERR_MISALIGNED;
+      // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
+      // k-block), two atoms of B per (224 columns, k-block)
+      const int64_t a_rows = 2 * ((M + 127) / 128) * pl.k_blocks;
+      const int64_t b_rows = 4 * pl.n_tiles * pl.k_blocks;
+      const int64_t a_dim[2] = {256, a_rows}, b_dim[2] = {256, b_rows};
+      const int64_t a_box[2] = {256, 2}, b_box[2] = {256, 4};
+      if ((st = encode_map(&maps.sfa, sfa, a_dim, 256, a_box, dtype, true, false)) != GB_OK) return st;
+      if ((st = encode_map(&maps.sfb, sfb, b_dim, 256, b_box, dtype, true, false)) != GB_OK) return st;
+    }
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
@@ -1360,7 +1500,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   const bool mc = pl.variant == kVariantPairMc;
   const bool bf = dtype == GB_BF16;
   if (pair) {
-    st = in.f8 ? prepare_pair_any<true>(bf, mc, dev) : prepare_pair_any<false>(bf, mc, dev);
+    st = bf ? prepare_pair_any<true>(in.kind(), mc, dev) : prepare_pair_any<false>(in.kind(), mc, dev);
     if (st != GB_OK) return st;
   }
   // CTAs (clusters) that can run at once
@@ -1373,7 +1513,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     std::lock_guard<std::mutex> lk(g_mu);
     sched = g_force_schedule;
   }
-  const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
+  const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;   // the same for every input kind
   p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   bool sk = !mc && workspace != nullptr && p.nsb > 0 && sched != 1;   // multicast: whole tiles
   if (sk && sched == 0) sk = p.num_tiles % slots != 0;
@@ -1392,10 +1532,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.dp_tiles = p.num_tiles;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (pair)
-    return in.f8 ? launch_pair_any<true>(bf, mc, tmA, tmB, p, G, s) : launch_pair_any<false>(bf, mc, tmA, tmB, p, G, s);
-  if (in.f8) return bf ? launch_single<true, true>(dev, tmA, tmB, p, G, s) : launch_single<false, true>(dev, tmA, tmB, p, G, s);
-  return bf ? launch_single<true, false>(dev, tmA, tmB, p, G, s) : launch_single<false, false>(dev, tmA, tmB, p, G, s);
+  return bf ? launch_any<true>(pair, in.kind(), mc, dev, maps, p, G, s)
+            : launch_any<false>(pair, in.kind(), mc, dev, maps, p, G, s);
 }
 
 }  // namespace
@@ -1439,6 +1577,44 @@ gb_status gb_gemm_fp8(int a_format, int b_format, int out_dtype, int64_t M, int6
   const InType in{a_format, b_format, true, 1};
   return gemm_entry(out_dtype, M, N, K, alpha, A, lda, GB_K_MAJOR, B, ldb, GB_K_MAJOR, beta, C, D, workspace,
                     workspace_bytes, stream, epi, &in);
+}
+
+gb_status gb_mx_scales_bytes(int operand, int64_t rows, int64_t K, size_t* bytes) {
+  if (!bytes || rows < 0 || K < 0 || (operand != 0 && operand != 1)) return GB_ERR_INVALID_ARG;
+  const int64_t kbs = (K + 127) / 128;
+  const int64_t blocks = operand == 0 ? (rows + 127) / 128 : (rows + gb::kMxTileN - 1) / gb::kMxTileN;
+  *bytes = static_cast<size_t>(blocks * kbs * (operand == 0 ? 512 : 1024));
+  return GB_OK;
+}
+
+gb_status gb_mx_pack_scales(int operand, int64_t rows, int64_t K, const void* src, int64_t ld_src, void* dst,
+                            void* stream) {
+  size_t bytes = 0;
+  gb_status st = gb_mx_scales_bytes(operand, rows, K, &bytes);
+  if (st != GB_OK) return st;
+  if (bytes == 0) return GB_OK;
+  if (!src || !dst || ld_src < (K + 31) / 32) return GB_ERR_INVALID_ARG;
+  DeviceState* dev;
+  if ((st = device_state(&dev)) != GB_OK) return st;
+  const int64_t total = static_cast<int64_t>(bytes);
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 0x7fffffff) return GB_ERR_INVALID_ARG;
+  gb::mx_pack_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      operand, rows, K, static_cast<const uint8_t*>(src), ld_src, static_cast<uint8_t*>(dst), total);
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+gb_status gb_gemm_mxfp8(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K, float alpha,
+                        const void* A, int64_t lda, const void* sfa, const void* B, int64_t ldb, const void* sfb,
+                        float beta, const void* C, void* D, const gb_epilogue* epi, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (a_format != GB_FP8_E4M3 && a_format != GB_FP8_E5M2) return GB_ERR_INVALID_ARG;
+  if (b_format != GB_FP8_E4M3 && b_format != GB_FP8_E5M2) return GB_ERR_INVALID_ARG;
+  if (out_dtype != GB_F16 && out_dtype != GB_BF16) return GB_ERR_INVALID_ARG;
+  const InType in{a_format, b_format, true, 1, true};
+  return gemm_entry(out_dtype, M, N, K, alpha, A, lda, GB_K_MAJOR, B, ldb, GB_K_MAJOR, beta, C, D, workspace,
+                    workspace_bytes, stream, epi, &in, sfa, sfb);
 }
 
 gb_status gb_gemm_ex(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,

@@ -12,6 +12,8 @@ Generation recipe (the same for every problem):
   * cast once to fp16/bf16 (round to nearest even), or, for FP8 inputs (a_fmt / b_fmt
     "e4m3" / "e5m2"), cast A and B once to that format with torch's conversion and keep
     their one-byte codes (C stays in the 16-bit dtype);
+  * block-scaled FP8 problems then draw E8M0 scale codes, uniform integers in
+    ``scale_codes`` = (lo, hi): SFA (M x ceil(K/32)) and then SFB (N x ceil(K/32)), row-major;
   * store in the requested major.  The values never depend on the major:
       A K-major : A[m*lda + k]      A M-major : A[m + k*lda]
       B K-major : B[n*ldb + k]      B N-major : B[k*ldb + n]
@@ -49,6 +51,7 @@ class Problem:
     ldb: Optional[int] = None
     a_fmt: Optional[str] = None  # None: A in dtype; "e4m3" | "e5m2": one-byte FP8 codes
     b_fmt: Optional[str] = None
+    scale_codes: Optional[tuple] = None   # block-scaled FP8: E8M0 codes drawn from [lo, hi]
 
     @property
     def in_bytes(self) -> int:
@@ -91,6 +94,12 @@ FP8_WORKLOADS = {
                                     sigma=1.0, c_dist="normal", c_sigma=1.0, seed=5,
                                     a_fmt="e4m3", b_fmt="e4m3"),
 }
+# Block-scaled (MX) FP8: the same square problem with one E8M0 scale per 32 K elements,
+# scales between 2^-4 and 2^4.
+FP8_WORKLOADS["gemm8192_mxfp8_bf16_c"] = Problem("gemm8192_mxfp8_bf16_c", 8192, 8192, 8192, "bf16",
+                                                 has_c=True, alpha=1.25, beta=0.5, dist="normal",
+                                                 sigma=1.0, c_dist="normal", c_sigma=1.0, seed=6,
+                                                 a_fmt="e4m3", b_fmt="e4m3", scale_codes=(123, 131))
 FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
@@ -169,6 +178,12 @@ def make(p: Problem, logical: bool = False):
         "ldb": ldb,
         "C": c.reshape(-1).clone() if c is not None else None,
     }
+    if p.scale_codes is not None:
+        lo, hi = p.scale_codes
+        nsf = -(-p.K // 32)
+        out["SFA"] = torch.randint(lo, hi + 1, (p.M, nsf), generator=g).to(torch.uint8).reshape(-1)
+        out["SFB"] = torch.randint(lo, hi + 1, (p.N, nsf), generator=g).to(torch.uint8).reshape(-1)
+        out["ld_sf"] = nsf
     if logical:
         out.update(a=a, b=b, c=c)
     return out

@@ -251,7 +251,9 @@ def test_wait_timeout_is_reported_and_context_survives(variant):
         G.debug_skip_k_block(-1)
         G.set_wait_timeout_ns(0)
     assert st == 5
-    assert detail & 0xff in (1, 2, 4)
+    # the first wait to run out: the MMA on the missing k-block (2), the epilogue behind it
+    # (4), a copy stage waiting for a slot (1) or for the last releases before exit (6)
+    assert detail & 0xff in (1, 2, 4, 6)
     assert G.last_device_status() == (0, 0)   # record cleared
     check(p, data, run(p, data), exact=True)  # the context still works
 
