@@ -72,6 +72,16 @@ int la_zipped_divide(const char* layout, const char* tiler, char* out, size_t ca
 int la_local_tile(const char* layout, const char* tiler, const int64_t* grid, int ngrid,
                   int64_t* origin, char* out, size_t cap);
 
+/* local_tile with a projection ("Layouts as Algebra" — "The kernel, in three lines": the
+   block tiler (BM, BN, BK) is applied to A, B and C with a step that keeps the modes each
+   one has).  tiler names n tile modes; step[i] != 0 keeps mode i (the kept modes must number
+   the layout's rank); grid[i] is the tile coordinate along mode i, or -1 to keep that grid
+   mode whole as a trailing mode of the result.  Writes the layout (tile modes, then the kept
+   grid modes) to out and the offset of the fixed coordinates to *origin.  LA_ERR_ARG for a
+   rank mismatch, LA_ERR_RANGE for a coordinate off the grid. */
+int la_local_tile_proj(const char* layout, const char* tiler, const int64_t* grid, const int* step, int n,
+                       int64_t* origin, char* out, size_t cap);
+
 /* Thread `tid` of thread layout `thr`: its elements of `layout` (the rest layout in
    `out`) and the offset of its first element in *origin. */
 int la_local_partition(const char* layout, const char* thr, int64_t tid, int64_t* origin,

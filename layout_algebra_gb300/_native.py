@@ -21,7 +21,7 @@ LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
     "la_composition", "la_complement", "la_logical_divide", "la_zipped_divide",
     "la_local_tile", "la_local_partition", "la_print_layout", "la_logical_product",
-    "la_swizzle",
+    "la_swizzle", "la_local_tile_proj",
 ]
 
 
@@ -126,6 +126,8 @@ def lib():
     L.la_complement.argtypes = [cp, i64, cp, sz]
     L.la_local_tile.restype = ci
     L.la_local_tile.argtypes = [cp, cp, vp, ci, ctypes.POINTER(i64), cp, sz]
+    L.la_local_tile_proj.restype = ci
+    L.la_local_tile_proj.argtypes = [cp, cp, vp, vp, ci, ctypes.POINTER(i64), cp, sz]
     L.la_local_partition.restype = ci
     L.la_local_partition.argtypes = [cp, cp, i64, ctypes.POINTER(i64), cp, sz]
     L.la_logical_product.restype = ci

@@ -422,6 +422,39 @@ Layout local_tile(const Layout& a, const Tiler& t, const std::vector<int64_t>& g
   return z.mode(0);
 }
 
+Layout local_tile_proj(const Layout& a, const Tiler& t, const std::vector<int64_t>& grid_coord,
+                       const std::vector<int>& step, int64_t* origin) {
+  if (t.whole) throw Error(LA_ERR_ARG, "a projected tiler names one tile per mode");
+  const size_t n = t.modes.size();
+  if (step.size() != n || grid_coord.size() != n) throw Error(LA_ERR_ARG, "tiler, coordinate and step ranks differ");
+  Tiler kept;
+  std::vector<int64_t> coord;
+  for (size_t i = 0; i < n; ++i)
+    if (step[i] != 0) {
+      kept.modes.push_back(t.modes[i]);
+      coord.push_back(grid_coord[i]);
+    }
+  if (static_cast<int>(kept.modes.size()) != a.rank())
+    throw Error(LA_ERR_ARG, "the projection keeps a different number of modes than the layout has");
+  Layout z = zipped_divide(a, kept);
+  Layout tile = z.mode(0), grid = z.mode(1);
+  if (grid.rank() != a.rank()) throw Error(LA_ERR_ARG, "grid rank");
+  int64_t off = 0;
+  std::vector<Layout> out;
+  for (int i = 0; i < tile.rank(); ++i) out.push_back(tile.mode(i));
+  for (int i = 0; i < grid.rank(); ++i) {
+    Layout g = grid.mode(i);
+    if (coord[i] < 0) {
+      out.push_back(g);
+    } else {
+      if (coord[i] >= size(g)) throw Error(LA_ERR_RANGE, "grid coordinate out of range");
+      off += eval(g, coord[i]);
+    }
+  }
+  if (origin) *origin = off;
+  return tuple_layout(out);
+}
+
 Layout local_partition(const Layout& a, const Layout& thr, int64_t tid, int64_t* origin) {
   // the thread's coordinate inside thr: the x with thr(x) == tid, unravelled
   int64_t n = size(thr);

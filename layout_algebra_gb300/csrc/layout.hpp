@@ -107,6 +107,13 @@ int64_t swizzle(int bits, int base, int shift, int64_t x);
 // (one index per grid leaf).  Returns the tile layout and its origin offset.
 Layout local_tile(const Layout& a, const Tiler& t, const std::vector<int64_t>& grid_coord,
                   int64_t* origin);
+// local_tile with a projection: the tiler and coordinate name more modes than `a` has (the
+// (BM, BN, BK) tiler of a GEMM, say) and step[i] != 0 keeps mode i of them for `a` (CuTe's
+// Step<_1, X, _1> for A).  A coordinate of -1 keeps that grid mode whole, as a trailing mode
+// of the result over its tiles.  Returns (tile modes..., kept grid modes...) and the
+// offset of the fixed coordinates.
+Layout local_tile_proj(const Layout& a, const Tiler& t, const std::vector<int64_t>& grid_coord,
+                       const std::vector<int>& step, int64_t* origin);
 // local_partition: thread `tid` of thread layout `thr` takes, from every thr-shaped
 // block of `a`, the element at its own coordinate.  Returns the rest layout and the
 // offset of the thread's first element.

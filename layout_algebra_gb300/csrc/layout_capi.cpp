@@ -127,6 +127,17 @@ int la_local_tile(const char* layout, const char* tiler, const int64_t* grid, in
   });
 }
 
+int la_local_tile_proj(const char* layout, const char* tiler, const int64_t* grid, const int* step, int n,
+                       int64_t* origin, char* out, size_t cap) {
+  if (!layout || !tiler || !origin || n <= 0 || !grid || !step) return LA_ERR_ARG;
+  return guarded([&] {
+    std::vector<int64_t> g(grid, grid + n);
+    std::vector<int> st(step, step + n);
+    la::Layout t = la::local_tile_proj(la::parse_layout(layout), la::parse_tiler(tiler), g, st, origin);
+    return put(la::to_string(t), out, cap);
+  });
+}
+
 int la_local_partition(const char* layout, const char* thr, int64_t tid, int64_t* origin,
                        char* out, size_t cap) {
   if (!layout || !thr || !origin) return LA_ERR_ARG;

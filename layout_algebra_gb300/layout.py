@@ -94,6 +94,21 @@ def local_tile(layout, tiler, grid_coord):
     return origin.value, s
 
 
+def local_tile_proj(layout, tiler, grid_coord, step):
+    """local_tile with a projection step: grid_coord entries of None keep that grid mode
+    (every tile along it) as a trailing mode; step entries of 0 (or None) drop a tiler mode.
+    Returns (origin, layout)."""
+    n = len(step)
+    g = np.ascontiguousarray([-1 if c is None else int(c) for c in grid_coord], dtype=np.int64)
+    st = np.ascontiguousarray([0 if x in (None, 0) else 1 for x in step], dtype=np.int32)
+    if g.size != n:
+        raise ValueError("grid_coord and step must have the same length")
+    origin = ctypes.c_int64()
+    s = _text(lib().la_local_tile_proj, _b(layout), _b(tiler), g.ctypes.data, st.ctypes.data, n,
+              ctypes.byref(origin))
+    return origin.value, s
+
+
 def local_partition(layout, thr, tid):
     origin = ctypes.c_int64()
     s = _text(lib().la_local_partition, _b(layout), _b(thr), int(tid), ctypes.byref(origin))

@@ -85,3 +85,48 @@ def test_print_layout_cli():
     assert r.returncode == 0, r.stderr
     rows = [line for line in r.stdout.splitlines() if "|" in line]
     assert [[int(v) for v in line.split("|")[1:-1]] for line in rows] == [[0, 1, 2], [3, 4, 5]]
+
+
+# ------------------------------------------------------------------ local_tile with a projection
+# "Layouts as Algebra", "The kernel, in three lines": one block tiler (BM, BN, BK) serves A, B
+# and C, each keeping the modes it has; A keeps (BM, BK) and every k-tile, giving the
+# (BLK_M, BLK_K, k) shape of the sgemm example.
+
+@pytest.mark.parametrize("M,N,K,BM,BN,BK,m,n", [(512, 384, 256, 128, 64, 32, 2, 3),
+                                                 (256, 256, 128, 128, 128, 64, 1, 0)])
+def test_projected_tiles_of_a_gemm(M, N, K, BM, BN, BK, m, n):
+    tiler = "(%d,%d,%d)" % (BM, BN, BK)
+    # A (M,K) row-major, step (1, X, 1), all k-tiles kept
+    oa, la = L.local_tile_proj("(%d,%d):(%d,1)" % (M, K, K), tiler, [m, n, None], [1, 0, 1])
+    assert R.parse(la)[0] == (BM, BK, K // BK)
+    for i in range(0, BM, 7):
+        for k in range(0, BK, 5):
+            for kt in range(K // BK):
+                assert oa + R.evaluate_coord(R.parse(la), [i, k, kt]) == (m * BM + i) * K + kt * BK + k
+    # B (N,K) K-major, step (X, 1, 1)
+    ob, lb = L.local_tile_proj("(%d,%d):(%d,1)" % (N, K, K), tiler, [m, n, None], [0, 1, 1])
+    assert R.parse(lb)[0] == (BN, BK, K // BK)
+    for j in range(0, BN, 3):
+        for kt in range(K // BK):
+            assert ob + R.evaluate_coord(R.parse(lb), [j, 1, kt]) == (n * BN + j) * K + kt * BK + 1
+    # C (M,N) row-major, step (1, 1, X): one tile, no trailing mode
+    oc, lc = L.local_tile_proj("(%d,%d):(%d,1)" % (M, N, N), tiler, [m, n, None], [1, 1, 0])
+    assert R.parse(lc)[0] == (BM, BN)
+    for i in range(0, BM, 11):
+        for j in range(0, BN, 13):
+            assert oc + R.evaluate_coord(R.parse(lc), [i, j]) == (m * BM + i) * N + n * BN + j
+
+
+def test_projection_matches_plain_local_tile():
+    # with every mode kept and every coordinate fixed it is local_tile itself
+    for coord in ([0, 0], [3, 1], [1, 2]):
+        o1, l1 = L.local_tile("(64,48):(1,64)", "(16,16)", coord)
+        o2, l2 = L.local_tile_proj("(64,48):(1,64)", "(16,16)", coord, [1, 1])
+        assert (o1, R.table(R.parse(l1))) == (o2, R.table(R.parse(l2)))
+
+
+def test_projection_errors():
+    with pytest.raises(L.LayoutError):    # keeps three modes of a rank-2 layout
+        L.local_tile_proj("(64,48):(48,1)", "(16,16,8)", [0, 0, 0], [1, 1, 1])
+    with pytest.raises(L.LayoutError):    # coordinate beyond the grid
+        L.local_tile_proj("(64,48):(48,1)", "(16,16,8)", [4, 0, None], [1, 0, 1])
