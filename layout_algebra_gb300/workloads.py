@@ -102,6 +102,13 @@ FP8_WORKLOADS["gemm8192_mxfp8_bf16_c"] = Problem("gemm8192_mxfp8_bf16_c", 8192, 
                                                  a_fmt="e4m3", b_fmt="e4m3", scale_codes=(123, 131))
 FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
+# A decode-like problem with few output tiles (N = 16): K is split across CTAs (stream-K,
+# through a workspace) so that every SM has work.  Bound by reading A from HBM.
+EXTRA_WORKLOADS = {
+    "gemm4096x16x4096_decode_bf16": Problem("gemm4096x16x4096_decode_bf16", 4096, 16, 4096, "bf16",
+                                            dist="normal", sigma=1.0, seed=7),
+}
+
 
 def torch_dtype(name: str) -> torch.dtype:
     return {"f16": torch.float16, "bf16": torch.bfloat16}[name]

@@ -44,7 +44,7 @@ def run_ws(p, data, ws, D=None):
     return out
 
 
-@pytest.mark.parametrize("shape", [(256, 512, 4096), (300, 520, 1000), (128, 256, 2048),
+@pytest.mark.parametrize("shape", [(256, 512, 4096), (300, 520, 1000), (128, 256, 2048), (4096, 16, 4096),
                                    (1000, 1000, 777), (64, 64, 64)])
 def test_split_tiles_match_oracle(variant, schedule, workspace, shape):
     """Few tiles and forced splitting: many CTAs add partials into one tile."""
