@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--epilogue", default="plain", choices=["plain", "bias-gelu", "bias-gelu-e4m3"],
                     help="fused epilogue to time (gb_gemm_ex): bias + GELU, optionally with amax "
                          "and a scaled E4M3 output")
+    ap.add_argument("--graph", action="store_true",
+                    help="launch the timed steps from one captured CUDA graph (for GEMMs shorter "
+                         "than the host's per-call work); kernel time = graph time / steps")
     ap.add_argument("--workspace", action="store_true",
                     help="time the workspace entry point (stream-K schedule where it helps)")
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -329,6 +332,7 @@ def run_gb300(args):
     dcode = 1 if out_dt == torch.bfloat16 else 0
 
     def launch():
+        sh = torch.cuda.current_stream().cuda_stream   # the capture stream inside a graph capture
         if mx:
             st = G.lib().gb_gemm_mxfp8(G.fp8_format(p.a_fmt), G.fp8_format(p.b_fmt), dcode, p.M, p.N, p.K,
                                        p.alpha, A.data_ptr(), lda, sfa.data_ptr(), B.data_ptr(), ldb,
@@ -370,15 +374,31 @@ def run_gb300(args):
     sampler = ClockSampler(phys)
     time.sleep(0.3)
 
+    graph = None
+    if args.graph:
+        # the launches of the timed region recorded once; the host's per-call work (planning,
+        # tensor maps) happens at capture time, outside the timed region
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                launch()
+        torch.cuda.synchronize()
+        graph.replay()                      # one untimed replay
+        torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world, local)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(args.steps):
-        starts[i].record(stream)
-        launch()
-        ends[i].record(stream)
+    if graph is not None:
+        starts[0].record(stream)
+        graph.replay()
+        ends[-1].record(stream)
+    else:
+        for i in range(args.steps):
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     barrier(world, local)
@@ -388,8 +408,11 @@ def run_gb300(args):
     if st != 0:
         raise RuntimeError("device status %d (%#x) in the timed region" % (st, detail))
     total_ms = starts[0].elapsed_time(ends[-1])
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    if graph is not None:
+        kernel_ms = total_ms / args.steps
+    else:
+        per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
     elapsed_s, total_flops = aggregate(total_ms / 1e3, float(p.flops) * args.steps, world, dev)
     value = total_flops / elapsed_s / 1e12
     clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
@@ -494,6 +517,8 @@ def run_gb300(args):
     }
     line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
                                      if ws is not None else "gb_gemm_%s" % p.dtype)
+    if graph is not None:
+        line["config"]["launch"] = "one CUDA graph of %d launches" % args.steps
     if mx:
         line["config"]["entry_point"] = "gb_gemm_mxfp8" + (" (workspace)" if ws is not None else "")
         line["config"]["scales"] = "E8M0 per 32 K elements of each row of A and column of B, codes %d..%d" % p.scale_codes

@@ -10,7 +10,8 @@
  * in depth" — "The problem CUTLASS solves", tiling); tile and element addressing come
  * from shape:stride layouts divided into (tile, grid) modes ("Day 84: CUTLASS and CuTe
  * layouts" — "A layout is a shape and a stride").  The pair variant is used when
- * M > 128, the single-CTA variant otherwise (gb_set_kernel_variant overrides this).
+ * M > 128, the single-CTA variant otherwise, and narrow single-CTA tiles when N <= 64
+ * (gb_set_kernel_variant overrides this).
  *
  * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
  * "One notation, and no more transposes"):
@@ -248,10 +249,13 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
 gb_status gb_set_wait_timeout_ns(uint64_t ns);
 gb_status gb_debug_skip_k_block(int64_t k_block);
 
-/* Kernel variant for later calls (process-wide): 0 chooses by shape (the default), 1 the
-   single-CTA 128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 3 the CTA-pair kernel in
-   clusters of two pairs that share each B tile through multicast copies (whole tiles only:
-   the *_ws calls do not use stream-K with it).  GB_ERR_INVALID_ARG for other values. */
+/* Kernel variant for later calls (process-wide): 0 chooses by shape (the default: 4 when N
+   <= 64, else 2 when M > 128, else 1), 1 the single-CTA 128 x 256 kernel, 2 the CTA-pair
+   256 x 256 kernel, 3 the CTA-pair kernel in clusters of two pairs that share each B tile
+   through multicast copies (whole tiles only: the *_ws calls do not use stream-K with it),
+   4 the single-CTA kernel with narrow 128 x 64 tiles and eight 24 KiB stages (for outputs
+   with few columns; with a workspace, stream-K spreads K over the SMs).  Block-scaled FP8
+   has no form 3 or 4 and runs as 2 (M > 128) or 1.  GB_ERR_INVALID_ARG for other values. */
 gb_status gb_set_kernel_variant(int variant);
 
 /* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2 or

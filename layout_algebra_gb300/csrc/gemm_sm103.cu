@@ -54,7 +54,7 @@ constexpr int kSwz = 64;             // elements per 128-byte swizzle span
 constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
 constexpr int kTmemCols = 512;       // all of Tensor Memory: accumulators of 512 fp32 columns
 constexpr int kCtlBytes = 256;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 // Two variants share all code:
@@ -80,19 +80,26 @@ enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
 constexpr int kMxTileN = 224;
 constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
 
-template <bool kPair, int kIn = kIn16>
+// Kernel shapes: the standard tiles, the CTA pair in clusters of two pairs sharing B by
+// multicast, and narrow single-CTA tiles (128 x 64) for problems with few output columns.
+enum : int { kShapeStd = 0, kShapeMc = 1, kShapeNarrow = 2 };
+constexpr int kNarrowTileN = 64;
+
+template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
 struct Cfg {
   static constexpr bool kMx = kIn == kInMx;
+  static constexpr bool kNarrow = kShape == kShapeNarrow;
   static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kTileN = kMx ? kMxTileN : (kPair ? kPairTileN : kBN);
+  static constexpr int kTileN = kNarrow ? kNarrowTileN : (kMx ? kMxTileN : (kPair ? kPairTileN : kBN));
   static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
   static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
   static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
   static constexpr int kRowsB = kRowsBSub * kNSub;                // B rows a CTA stages per k-block
-  static constexpr int kAccBufs = kMx ? 2 : kTmemCols / kTileN;   // accumulators in TMEM
+  static constexpr int kAccBufs = (kMx || kTmemCols / kTileN >= 2) ? 2 : 1;   // accumulators in TMEM
   static constexpr int kAccStride = kMx ? 256 : kTileN;           // TMEM columns between them
   static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1;       // k-blocks per stage
-  static constexpr int kStages = (kPair && kNSub == 1) ? 3 : 4;
+  // narrow tiles: 24 KiB k-blocks, eight in flight
+  static constexpr int kStages = kNarrow ? 8 : ((kPair && kNSub == 1) ? 3 : 4);
   static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;            // producer, MMA, epilogue warps
   static constexpr int kAHalf = kRowsA * kBK * 2;                // one k-block of A (bytes)
@@ -113,6 +120,7 @@ struct Cfg {
   static_assert(kStages <= kMaxStages, "control block");
   static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kNSub == 0, "TMEM accumulators");
   static_assert(!kMx || (kTileN <= 224 && kTileN % 32 == 0 && kBSub % 1024 == 0), "MX tile");
+  static_assert(!kNarrow || (!kPair && !kMx), "narrow tiles: single CTA, 16-bit or FP8 inputs");
 };
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -158,6 +166,7 @@ struct Ctl {
   uint64_t acc_empty[2];
   uint64_t drain;
   uint64_t part_done;         // epilogue warps finished writing a stream-K partial
+  uint64_t fix_done;          // epilogue warps finished reading other CTAs' partials
   uint32_t tmem_base;
   int32_t abort;
 };
@@ -387,11 +396,12 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k
   return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
 }
 
-template <bool kPair, int kIn, bool kMc>
+template <bool kPair, int kIn, int kShape>
 __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, const void* tmSFA,
                              const void* tmSFB, uint8_t* smem, Ctl* ctl, uint32_t rank, uint32_t cluster,
                              uint32_t nclusters) {
-  using C = Cfg<kPair, kIn>;
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
   static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
   // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
@@ -489,10 +499,11 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   }
 }
 
-template <bool kPair, int kIn, bool kMc>
+template <bool kPair, int kIn, int kShape>
 __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
                         uint32_t cluster, uint32_t nclusters) {
-  using C = Cfg<kPair, kIn>;
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
   uint32_t kbc = 0;                        // k-blocks issued: selects the scale-factor slot
   if (kPair && (rank & 1u) != 0) return;   // the even CTA issues for the pair
   // a stage is free once every pair reading it has finished: with B multicast the other
@@ -774,10 +785,11 @@ __device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl
   return ok != 0;
 }
 
-template <bool kBF16, bool kPair, int kIn, bool kMc>
+template <bool kBF16, bool kPair, int kIn, int kShape>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters) {
-  using C = Cfg<kPair, kIn>;
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
@@ -797,12 +809,22 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const int32_t cols_left = p.N - nt * C::kTileN;
     const int64_t base = d_offset(p, mt, nt, r, 0);
     const int cend = min(cbeg + kCols, static_cast<int>(min(cols_left, C::kTileN)));
-    // C in 16-byte words when rows are contiguous and aligned (vec_ok); the tile's C rows
-    // are pulled into L2 while the main loop still runs, and each 32-column run is loaded
-    // one run ahead of its use
+    // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
+    // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
+    // still runs; each later run is loaded kAhead runs before its use
     const bool cvec = p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
+    constexpr int kRuns = kCols / 32;
+    constexpr int kAhead = C::kAccBufs == 1 ? 4 : 2;
+    uint4 cr[kAhead][4];
     if (cvec && cend > cbeg)
       prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a)
+      if (cvec && cbeg + 32 * a + 32 <= cend) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg + 32 * a);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cr[a][j] = __ldg(src + j);
+      }
     const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
     const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
     if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
@@ -822,24 +844,14 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       if (!ok) break;
     }
     float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
-    uint4 cw[4], cn[4];
-    if (cvec && cbeg + 32 <= cend) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) cw[j] = __ldg(src + j);
-    }
-    for (int c0 = cbeg; c0 < cend; c0 += 32) {
+    for (int run = 0; run < kRuns; ++run) {
+      const int c0 = cbeg + 32 * run;
+      if (c0 >= cend) break;
       uint32_t acc[32];
       const bool vec_run = cvec && c0 + 32 <= cend;
-      const bool next_vec = cvec && c0 + 64 <= cend;
-      if (p.k_blocks > 0)
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
-      if (next_vec) {   // issued while the TMEM load is in flight
-        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + c0 + 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) cn[j] = __ldg(src + j);
-      }
       if (p.k_blocks > 0) {
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -848,21 +860,24 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       if (contributor) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
-        continue;
-      }
-      for (uint32_t c = c_lo; c <= c_hi; ++c) {
-        if (!sk_has_units(p, nclusters, c)) continue;
-        const float* part = part_slot<kPair>(p, c, rank);
+      } else {
+        for (uint32_t c = c_lo; c <= c_hi; ++c) {
+          if (!sk_has_units(p, nclusters, c)) continue;
+          const float* part = part_slot<kPair>(p, c, rank);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+          for (int i = 0; i < 32; ++i)
+            acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+        }
+        if (row_ok)
+          store_run<kBF16>(p, base + c0 * p.d_col, vec_run ? cr[run % kAhead] : nullptr, acc,
+                           min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
       }
-      if (row_ok)
-        store_run<kBF16>(p, base + c0 * p.d_col, vec_run ? cw : nullptr, acc, min(32, cols_left - c0),
-                         static_cast<int64_t>(nt) * C::kTileN + c0, amax);
-      if (next_vec) {
+      // refill this run's registers with the run kAhead further on
+      const int cn0 = c0 + 32 * kAhead;
+      if (cvec && cn0 + 32 <= cend) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cw[j] = cn[j];
+        for (int j = 0; j < 4; ++j) cr[run % kAhead][j] = __ldg(src + j);
       }
     }
     if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
@@ -875,6 +890,17 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       else
         mbar_arrive(ae);
       if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
+      if (owner_with_parts) mbar_arrive(smem_addr(&ctl->fix_done));
+    }
+    if (owner_with_parts && warp == 2) {
+      // the partials this CTA added are consumed: clear their flags, so that a later launch
+      // with the same launch number (a replayed CUDA graph) waits for fresh ones.  A CTA
+      // owns at most one split tile per launch, so fix_done completes phase 0 once.
+      if (!wait_warp<kPair>(smem_addr(&ctl->fix_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
+      if (lane == 0)
+        for (uint32_t c = c_lo; c <= c_hi; ++c)
+          if (sk_has_units(p, nclusters, c)) st_release_gpu(part_flag<kPair>(p, c, rank), 0u);
+      __syncwarp();
     }
     if (contributor && warp == 2) {
       // a CTA contributes at most one partial per launch: part_done completes phase 0 once
@@ -899,12 +925,13 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <bool kBF16, bool kPair, int kIn, bool kMc = false>
-__global__ void __launch_bounds__(Cfg<kPair, kIn>::kThreads, 1)
+template <bool kBF16, bool kPair, int kIn, int kShape = kShapeStd>
+__global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const Params p) {
-  using C = Cfg<kPair, kIn>;
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStages * C::kStageBytes);
@@ -925,6 +952,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn>::kThreads, 1)
     }
     mbar_init(smem_addr(&ctl->drain), 1);
     mbar_init(smem_addr(&ctl->part_done), C::kEpiWarps);
+    mbar_init(smem_addr(&ctl->fix_done), C::kEpiWarps);
     ctl->abort = 0;
     fence_barrier_init();
     if (p.k_blocks > 0) {
@@ -953,13 +981,13 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn>::kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      run_producer<kPair, kIn, kMc>(p, &tmA, &tmB, &tmSFA, &tmSFB, smem, ctl, rank, cluster, nclusters);
+      run_producer<kPair, kIn, kShape>(p, &tmA, &tmB, &tmSFA, &tmSFB, smem, ctl, rank, cluster, nclusters);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<kPair, kIn, kMc>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
+    if (lane == 0) run_mma<kPair, kIn, kShape>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
-    run_epilogue<kBF16, kPair, kIn, kMc>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
+    run_epilogue<kBF16, kPair, kIn, kShape>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
   }
 
   tc_fence_before_sync();
@@ -1055,20 +1083,22 @@ using gb::Params;
 std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
-int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast
+int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast;
+                           // 4: single CTA with narrow tiles
 int g_force_schedule = 0;  // 0: stream-K when a workspace is given and tiles leave a ragged
                            // last wave; 1: data-parallel only; 2: stream-K whenever possible
 
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
 constexpr int kVariantPairMc = 3;   // clusters of two pairs sharing B tiles by multicast
+constexpr int kVariantNarrow = 4;   // single CTA, 128 x 64 tiles (few output columns)
 
 bool is_pair(int variant) { return variant == kVariantPair || variant == kVariantPairMc; }
 
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
-  bool attr_single[2][3] = {};   // [bf16 out][input kind]
+  bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
   bool attr_pair[2][3] = {};
   bool attr_mc[2][3] = {};
   int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
@@ -1114,13 +1144,15 @@ struct InType {
 InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false, 2, false}; }
 
 // Tile width and the B rows one copy stages per CTA, per variant and input kind.
-int64_t tile_n_of(bool pair, const InType& in) {
+int64_t tile_n_of(int variant, const InType& in) {
+  if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx) return gb::kMxTileN;
-  return pair ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
+  return is_pair(variant) ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
 }
-int64_t mma_n_of(bool pair, const InType& in) {
+int64_t mma_n_of(int variant, const InType& in) {
+  if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx) return gb::kMxTileN;
-  return pair ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
+  return is_pair(variant) ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
 }
 
 gb_status plan_operand(int64_t rows, int64_t K, int64_t ld, int major, int64_t tile_rows,
@@ -1184,14 +1216,25 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
   return d;
 }
 
-int choose_variant(int64_t M) {
+// Kernel for a problem: a forced variant, else narrow tiles when the output has at most 64
+// columns, the CTA pair when it has more than 128 rows, the single CTA otherwise.  Block-
+// scaled inputs have no multicast or narrow form and take the pair or the single CTA.
+int choose_variant(int64_t M, int64_t N, const InType& in) {
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);
     forced = g_force_variant;
   }
-  if (forced == kVariantSingle || is_pair(forced)) return forced;
-  return M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+  int v;
+  if (forced != 0)
+    v = forced;
+  else if (N <= gb::kNarrowTileN)
+    v = kVariantNarrow;
+  else
+    v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+  if (in.mx && v == kVariantPairMc) v = kVariantPair;
+  if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+  return v;
 }
 
 gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
@@ -1200,14 +1243,14 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB, in.bytes);
   if (st != GB_OK) return st;
   if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
-  if (variant != kVariantSingle && !is_pair(variant)) return GB_ERR_INVALID_ARG;
+  if (variant != kVariantSingle && variant != kVariantNarrow && !is_pair(variant)) return GB_ERR_INVALID_ARG;
   const bool pair = is_pair(variant);
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
-  if (in.mx && variant == kVariantPairMc) return GB_ERR_INVALID_ARG;
-  const int64_t tile_n = tile_n_of(pair, in);
+  if (in.mx && (variant == kVariantPairMc || variant == kVariantNarrow)) return GB_ERR_INVALID_ARG;
+  const int64_t tile_n = tile_n_of(variant, in);
   // B rows one copy stages: one CTA's share of one MMA's columns; with multicast each CTA
   // copies a quarter of the pair's 256
-  int64_t rows_b = pair ? mma_n_of(pair, in) / 2 : mma_n_of(pair, in);
+  int64_t rows_b = pair ? mma_n_of(variant, in) / 2 : mma_n_of(variant, in);
   if (variant == kVariantPairMc) rows_b = gb::kSwz;
   std::memset(pl, 0, sizeof(*pl));
   pl->variant = variant;
@@ -1253,7 +1296,7 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   } catch (const la::Error&) {
     return GB_ERR_INVALID_ARG;
   }
-  pl->instr_desc = make_idesc(in, majorA, majorB, static_cast<int>(tile_m), static_cast<int>(mma_n_of(pair, in)));
+  pl->instr_desc = make_idesc(in, majorA, majorB, static_cast<int>(tile_m), static_cast<int>(mma_n_of(variant, in)));
   return GB_OK;
 }
 
@@ -1335,16 +1378,17 @@ struct Maps {
   CUtensorMap a, b, sfa, sfb;
 };
 
-template <bool kBF16, int kIn>
+template <bool kBF16, int kIn, int kShape>
 gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s) {
-  using C = gb::Cfg<false, kIn>;
-  if (!dev->attr_single[kBF16][kIn]) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using C = gb::Cfg<false, kIn, kShape>;
+  bool& attr = dev->attr_single[kBF16][kIn][kShape == gb::kShapeNarrow];
+  if (!attr) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kIn, kShape>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    dev->attr_single[kBF16][kIn] = true;
+    attr = true;
   }
-  gb::gemm_kernel<kBF16, false, kIn><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, p);
+  gb::gemm_kernel<kBF16, false, kIn, kShape><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
@@ -1354,7 +1398,7 @@ gb_status prepare_pair(DeviceState* dev) {
   constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
   bool& attr = kMc ? dev->attr_mc[kBF16][kIn] : dev->attr_pair[kBF16][kIn];
   if (!attr) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kMc>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
     attr = true;
@@ -1374,7 +1418,7 @@ gb_status prepare_pair(DeviceState* dev) {
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(kCl * (dev->sms / kCl), 1, 1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kMc>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, &cfg) != cudaSuccess ||
         n <= 0)
       n = dev->sms / kCl;
     clusters = std::min(n, dev->sms / kCl);
@@ -1398,7 +1442,7 @@ gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(kCl * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kMc>, m.a, m.b, m.sfa, m.sfb, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, m.a, m.b, m.sfa, m.sfb, p) != cudaSuccess)
     return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
@@ -1413,12 +1457,15 @@ gb_status prepare_pair_any(int kin, bool mc, DeviceState* dev) {
 }
 
 template <bool kBF16>
-gb_status launch_any(bool pair, int kin, bool mc, DeviceState* dev, const Maps& m, const Params& p, int G,
-                     cudaStream_t s) {
+gb_status launch_any(bool pair, int kin, bool mc, bool narrow, DeviceState* dev, const Maps& m, const Params& p,
+                     int G, cudaStream_t s) {
   if (!pair) {
-    if (kin == gb::kInMx) return launch_single<kBF16, gb::kInMx>(dev, m, p, G, s);
-    return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8>(dev, m, p, G, s)
-                           : launch_single<kBF16, gb::kIn16>(dev, m, p, G, s);
+    if (narrow)
+      return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeNarrow>(dev, m, p, G, s)
+                             : launch_single<kBF16, gb::kIn16, gb::kShapeNarrow>(dev, m, p, G, s);
+    if (kin == gb::kInMx) return launch_single<kBF16, gb::kInMx, gb::kShapeStd>(dev, m, p, G, s);
+    return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeStd>(dev, m, p, G, s)
+                           : launch_single<kBF16, gb::kIn16, gb::kShapeStd>(dev, m, p, G, s);
   }
   if (mc) return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, true>(m, p, G, s)
                                  : launch_pair<kBF16, gb::kIn16, true>(m, p, G, s);
@@ -1434,6 +1481,50 @@ int64_t workspace_bytes_for(int sms) {
   return flags + static_cast<int64_t>(sms) * gb::kSlotFloats * 4;
 }
 
+// Plans and tensor maps of recent calls.  Building them (the layout algebra and four map
+// encodings) costs tens of microseconds on the host, more than a small GEMM takes on the
+// GPU; a repeated call with the same operands and shape reuses them.
+struct PlanKey {
+  int device, dtype, kind, a_fmt, b_fmt, variant, majorA, majorB;
+  int64_t M, N, K, lda, ldb;
+  const void *A, *B, *sfa, *sfb;
+  bool operator==(const PlanKey& o) const {
+    return device == o.device && dtype == o.dtype && kind == o.kind && a_fmt == o.a_fmt && b_fmt == o.b_fmt &&
+           variant == o.variant && majorA == o.majorA && majorB == o.majorB && M == o.M && N == o.N &&
+           K == o.K && lda == o.lda && ldb == o.ldb && A == o.A && B == o.B && sfa == o.sfa && sfb == o.sfb;
+  }
+};
+struct PlanEntry {
+  bool valid = false;
+  PlanKey key;
+  gb_gemm_plan pl;
+  Maps maps;
+};
+constexpr int kPlanCacheSize = 16;
+PlanEntry g_plan_cache[kPlanCacheSize];
+int g_plan_next = 0;
+
+bool plan_cache_get(const PlanKey& k, gb_gemm_plan* pl, Maps* maps) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const PlanEntry& e : g_plan_cache)
+    if (e.valid && e.key == k) {
+      *pl = e.pl;
+      *maps = e.maps;
+      return true;
+    }
+  return false;
+}
+
+void plan_cache_put(const PlanKey& k, const gb_gemm_plan& pl, const Maps& maps) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  PlanEntry& e = g_plan_cache[g_plan_next];
+  g_plan_next = (g_plan_next + 1) % kPlanCacheSize;
+  e.valid = true;
+  e.key = k;
+  e.pl = pl;
+  e.maps = maps;
+}
+
 gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, const void* A, int64_t lda,
                      int majorA, const void* B, int64_t ldb, int majorB, float beta, const void* C, void* D,
                      void* workspace, size_t workspace_size, void* stream, const gb_epilogue* epi = nullptr,
@@ -1441,17 +1532,20 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   // dtype names the 16-bit type of C, D and the bias; the inputs share it unless in_f8 names
   // 8-bit input formats (with packed scale factors sfa / sfb when block-scaled)
   const InType in = in_f8 ? *in_f8 : in16(dtype);
-  int variant = choose_variant(M);
-  if (in.mx && variant == kVariantPairMc) variant = kVariantPair;   // no multicast form
-  gb_gemm_plan pl;
-  gb_status st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in);
+  const int variant = choose_variant(M, N, in);
+  gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB, in.bytes);
   if (st != GB_OK) return st;
+  if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GB_OK;
   if (D == nullptr) return GB_ERR_INVALID_ARG;
   if (beta != 0.0f && C == nullptr) return GB_ERR_INVALID_ARG;
   if (K > 0 && (A == nullptr || B == nullptr)) return GB_ERR_INVALID_ARG;
   if (!aligned16(D) || (C && !aligned16(C))) return GB_ERR_MISALIGNED;
   if (K > 0 && (!aligned16(A) || !aligned16(B))) return GB_ERR_MISALIGNED;
+  if (K > 0 && in.mx) {
+    if (sfa == nullptr || sfb == nullptr) return GB_ERR_INVALID_ARG;
+    if (!aligned16(sfa) || !aligned16(sfb)) return GB_ERR_MISALIGNED;
+  }
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GB_ERR_MISALIGNED;
   if (epi) {
     if (epi->activation < GB_ACT_NONE || epi->activation > GB_ACT_GELU) return GB_ERR_INVALID_ARG;
@@ -1465,24 +1559,31 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
+  const PlanKey key{device, dtype, in.kind(), in.a_fmt, in.b_fmt, variant, majorA, majorB, M, N, K, lda, ldb,
+                    K > 0 ? A : nullptr, K > 0 ? B : nullptr, in.mx ? sfa : nullptr, in.mx ? sfb : nullptr};
+  gb_gemm_plan pl;
   Maps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  if (K > 0) {
-    if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
-    if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
-    if (in.mx) {
-      if (sfa == nullptr || sfb == nullptr) return GB_ERR_INVALID_ARG;
-      if (!aligned16(sfa) || !aligned16(sfb)) return GB_ERR_MISALIGNED;
-      // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
-      // k-block), two atoms of B per (224 columns, k-block)
-      const int64_t a_rows = 2 * ((M + 127) / 128) * pl.k_blocks;
-      const int64_t b_rows = 4 * pl.n_tiles * pl.k_blocks;
-      const int64_t a_dim[2] = {256, a_rows}, b_dim[2] = {256, b_rows};
-      const int64_t a_box[2] = {256, 2}, b_box[2] = {256, 4};
-      if ((st = encode_map(&maps.sfa, sfa, a_dim, 256, a_box, dtype, true, false)) != GB_OK) return st;
-      if ((st = encode_map(&maps.sfb, sfb, b_dim, 256, b_box, dtype, true, false)) != GB_OK) return st;
+  if (!plan_cache_get(key, &pl, &maps)) {
+    if ((st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in)) != GB_OK) return st;
+    std::memset(&maps, 0, sizeof(maps));
+    if (K > 0) {
+      if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
+      if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
+      if (in.mx) {
+        // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
+        // k-block), two atoms of B per (224 columns, k-block)
+        const int64_t a_rows = 2 * ((M + 127) / 128) * pl.k_blocks;
+        const int64_t b_rows = 4 * pl.n_tiles * pl.k_blocks;
+        const int64_t a_dim[2] = {256, a_rows}, b_dim[2] = {256, b_rows};
+        const int64_t a_box[2] = {256, 2}, b_box[2] = {256, 4};
+        if ((st = encode_map(&maps.sfa, sfa, a_dim, 256, a_box, dtype, true, false)) != GB_OK) return st;
+        if ((st = encode_map(&maps.sfb, sfb, b_dim, 256, b_box, dtype, true, false)) != GB_OK) return st;
+      }
     }
+    plan_cache_put(key, pl, maps);
   }
   Params p;
   fill_params(pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
@@ -1532,8 +1633,9 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.dp_tiles = p.num_tiles;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return bf ? launch_any<true>(pair, in.kind(), mc, dev, maps, p, G, s)
-            : launch_any<false>(pair, in.kind(), mc, dev, maps, p, G, s);
+  const bool narrow = pl.variant == kVariantNarrow;
+  return bf ? launch_any<true>(pair, in.kind(), mc, narrow, dev, maps, p, G, s)
+            : launch_any<false>(pair, in.kind(), mc, narrow, dev, maps, p, G, s);
 }
 
 }  // namespace
@@ -1668,7 +1770,7 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
                             int majorB, gb_gemm_plan* plan) {
   if (!plan) return GB_ERR_INVALID_ARG;
   if (M < 0) return GB_ERR_INVALID_ARG;
-  return make_plan(dtype, choose_variant(M), M, N, K, lda, majorA, ldb, majorB, plan);
+  return make_plan(dtype, choose_variant(M, N, in16(dtype)), M, N, K, lda, majorA, ldb, majorB, plan);
 }
 
 gb_status gb_set_wait_timeout_ns(uint64_t ns) {
@@ -1684,7 +1786,8 @@ gb_status gb_debug_skip_k_block(int64_t k_block) {
 }
 
 gb_status gb_set_kernel_variant(int variant) {
-  if (variant != 0 && variant != kVariantSingle && !is_pair(variant)) return GB_ERR_INVALID_ARG;
+  if (variant != 0 && variant != kVariantSingle && variant != kVariantNarrow && !is_pair(variant))
+    return GB_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   g_force_variant = variant;
   return GB_OK;

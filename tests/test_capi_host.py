@@ -87,8 +87,13 @@ def test_variant_choice_by_shape():
     G.set_kernel_variant(0)
     assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 1
     assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 2
+    # at most 64 output columns: narrow 128 x 64 tiles
+    p = G.plan("f16", 4096, 16, 4096, 4096, "K", 4096, "K")
+    assert p["variant"] == 4 and (p["tile_m"], p["tile_n"]) == (128, 64)
+    assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 1, 64)
+    assert p["b_box"] == [64, 64] and (p["instr_desc"] >> 17) & 63 == 64 >> 3
     with pytest.raises(G.GemmError):
-        G.set_kernel_variant(4)
+        G.set_kernel_variant(5)
 
 
 def test_plan_bf16_descriptor_and_scalar_epilogue(variant):

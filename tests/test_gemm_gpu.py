@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["single", "pair", "pair_mc"])
+@pytest.fixture(params=[1, 2, 3, 4], ids=["single", "pair", "pair_mc", "narrow"])
 def variant(request):
     """Run a test with the single-CTA kernel and with the CTA-pair kernel."""
     G.set_kernel_variant(request.param)
@@ -261,17 +261,17 @@ def test_wait_timeout_is_reported_and_context_survives(variant):
 # --------------------------------------------------------------------------- device-side maps
 
 
-@pytest.mark.parametrize("var", [1, 2, 3])
+@pytest.mark.parametrize("var", [1, 2, 3, 4])
 @pytest.mark.parametrize("M,N,tile", [(5000, 3000, (19, 11)), (5000, 3000, (0, 0)),
                                       (256, 128, (0, 0)), (8192, 8192, (17, 30))])
 def test_epilogue_map_matches_host_layout(var, M, N, tile):
     """The device evaluation of the C/D tile map equals the host layout library's."""
-    tm = 128 if var == 1 else 256
     G.set_kernel_variant(var)
     try:
-        tn = int(G.plan("f16", M, N, 64, 64, "K", 64, "K")["tile_n"])
+        plan = G.plan("f16", M, N, 64, 64, "K", 64, "K")
     finally:
         G.set_kernel_variant(0)
+    tm, tn = int(plan["tile_m"]), int(plan["tile_n"])
     # the last tile along a mode when the index is beyond this variant's grid
     tile = (min(tile[0], (M + tm - 1) // tm - 1), min(tile[1], (N + tn - 1) // tn - 1))
     out = torch.empty(tm * tn, dtype=torch.int64, device=DEV)

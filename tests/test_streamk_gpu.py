@@ -20,7 +20,7 @@ def workspace():
     return G.make_workspace(DEV)
 
 
-@pytest.fixture(params=[1, 2], ids=["single", "pair"])
+@pytest.fixture(params=[1, 2, 4], ids=["single", "pair", "narrow"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param
@@ -130,5 +130,36 @@ def test_split_timeout_path_reports_and_recovers(workspace):
     assert st == 5 and (detail & 0xff) in (1, 2, 4, 7)
     try:
         check(p, data, run_ws(p, data, workspace), exact=True)
+    finally:
+        G.set_schedule(0)
+
+
+def test_stream_k_graph_replay(workspace):
+    """A captured stream-K GEMM replays correctly: owners clear the partial-ready flags they
+    consumed, so a replay (same launch number) waits for fresh partials."""
+    G.set_schedule(2)
+    try:
+        p = W.Problem("skg", 512, 768, 4096, "f16", dist="int2", seed=12)
+        data = W.make(p)
+        A, B = data["A"].to(DEV), data["B"].to(DEV)
+        D = torch.empty(p.M * p.N, dtype=torch.float16, device=DEV)
+
+        def call():
+            G.gemm(A, B, p.M, p.N, p.K, lda=data["lda"], ldb=data["ldb"], D=D, workspace=workspace)
+
+        call()                                   # first use: attributes, occupancy, plan
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        gen = torch.Generator().manual_seed(13)
+        for trial in range(4):
+            a = torch.randint(-2, 3, (p.M, p.K), generator=gen).to(torch.float16)
+            A.copy_(a.reshape(-1).to(DEV))
+            graph.replay()
+            torch.cuda.synchronize()
+            assert G.last_device_status() == (0, 0)
+            q = dict(data, A=a.reshape(-1))
+            check(p, q, D.cpu(), exact=True)
     finally:
         G.set_schedule(0)
