@@ -35,7 +35,9 @@ DEFAULT_WORKLOAD = "gemm8192_bf16_c"
 METRIC_MX = "GEMM TFLOP/s (2MNK/s) at 8192^3 block-scaled (MX) e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 METRIC_FP8 = "GEMM TFLOP/s (2MNK/s) at 8192^3 e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/gemm_kernel.cuh",
+                  "layout_algebra_gb300/csrc/gemm_launch.cuh", "layout_algebra_gb300/csrc/gemm_inst.cu",
+                  "layout_algebra_gb300/csrc/ptx.cuh"]
 
 
 def parse_args(argv=None):

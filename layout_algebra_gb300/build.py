@@ -1,7 +1,8 @@
 """Build the native library ``libgb300gemm.so`` in-tree.
 
 One shared library holds the host layout library (C++17), the sm_103a kernels and both
-C ABIs (include/gb300_gemm.h, include/layout_algebra.h).  Objects compile in parallel;
+C ABIs (include/gb300_gemm.h, include/layout_algebra.h).  Objects compile in parallel
+(the kernel instances in INST_GROUPS compilations of gemm_inst.cu);
 the CUDA runtime is linked statically and the driver's tensor-map encoder is looked up
 at run time, so the library loads on hosts without a GPU driver.
 """
@@ -16,8 +17,9 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgb300gemm.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["layout.cpp", "layout_capi.cpp", "gemm_sm103.cu"]
-HEADERS = ["layout.hpp", "ptx.cuh"]
+SOURCES = ["layout.cpp", "layout_capi.cpp", "gemm_sm103.cu", "gemm_inst.cu"]
+HEADERS = ["layout.hpp", "ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh"]
+INST_GROUPS = 10   # GB_INST_GROUP values of gemm_inst.cu
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -42,8 +44,19 @@ def up_to_date():
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _jobs():
+    """(source, object name, extra flags) of every object of the library."""
+    jobs = []
+    for s in SOURCES:
+        if s == "gemm_inst.cu":
+            jobs += [(s, "gemm_inst_%d.o" % g, ["-DGB_INST_GROUP=%d" % g]) for g in range(INST_GROUPS)]
+        else:
+            jobs.append((s, s + ".o", []))
+    return jobs
+
+
+def _compile(src, name, extra):
+    obj = os.path.join(BUILD, name)
     cmd = [nvcc(), *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
            "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj, *extra]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,9 +69,12 @@ def build(force=False, verbose=False, ptxas_info=False):
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
-    with ThreadPoolExecutor(len(SOURCES)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra if s.endswith(".cu") else []), SOURCES))
+    info = ["-Xptxas", "-v"] if ptxas_info else []
+    jobs = _jobs()
+    workers = max(1, min(len(jobs), os.cpu_count() or 1))
+    with ThreadPoolExecutor(workers) as ex:
+        results = list(ex.map(lambda j: _compile(j[0], j[1], j[2] + (info if j[0].endswith(".cu") else [])),
+                              jobs))
     if verbose or ptxas_info:
         for _, err in results:
             if err:

@@ -1,0 +1,53 @@
+// Kernel instances of the persistent GEMM, one group per compilation of this file
+// (GB_INST_GROUP = 0 .. kInstGroups - 1, set by the build), so that the instances compile
+// in parallel.  Every launcher the host dispatch (gemm_sm103.cu) calls is instantiated in
+// exactly one group.
+#include "gemm_launch.cuh"
+
+#ifndef GB_INST_GROUP
+#error "GB_INST_GROUP must be defined (0..9)"
+#endif
+
+namespace gb {
+
+#define GB_PAIR(BF, IN, MC)                                                                  \
+  template gb_status prepare_pair<BF, IN, MC>(DeviceState*);                                 \
+  template gb_status launch_pair<BF, IN, MC>(const Maps&, const Params&, int, cudaStream_t);
+#define GB_SINGLE(BF, IN, SHAPE) \
+  template gb_status launch_single<BF, IN, SHAPE>(DeviceState*, const Maps&, const Params&, int, cudaStream_t);
+
+#if GB_INST_GROUP == 0      // the 16-bit CTA-pair kernels (the large-problem path)
+GB_PAIR(true, kIn16, false)
+#elif GB_INST_GROUP == 1
+GB_PAIR(false, kIn16, false)
+#elif GB_INST_GROUP == 2    // CTA pairs sharing B by multicast
+GB_PAIR(true, kIn16, true)
+GB_PAIR(false, kIn16, true)
+#elif GB_INST_GROUP == 3    // FP8 inputs, CTA pairs
+GB_PAIR(true, kIn8, false)
+GB_PAIR(false, kIn8, false)
+#elif GB_INST_GROUP == 4
+GB_PAIR(true, kIn8, true)
+GB_PAIR(false, kIn8, true)
+#elif GB_INST_GROUP == 5    // block-scaled FP8
+GB_PAIR(true, kInMx, false)
+GB_PAIR(false, kInMx, false)
+#elif GB_INST_GROUP == 6
+GB_SINGLE(true, kInMx, kShapeStd)
+GB_SINGLE(false, kInMx, kShapeStd)
+#elif GB_INST_GROUP == 7    // single-CTA kernels, 128 x 256 tiles
+GB_SINGLE(true, kIn16, kShapeStd)
+GB_SINGLE(false, kIn16, kShapeStd)
+#elif GB_INST_GROUP == 8
+GB_SINGLE(true, kIn8, kShapeStd)
+GB_SINGLE(false, kIn8, kShapeStd)
+#elif GB_INST_GROUP == 9    // single-CTA kernels, 128 x 64 tiles (few output columns)
+GB_SINGLE(true, kIn16, kShapeNarrow)
+GB_SINGLE(false, kIn16, kShapeNarrow)
+GB_SINGLE(true, kIn8, kShapeNarrow)
+GB_SINGLE(false, kIn8, kShapeNarrow)
+#else
+#error "GB_INST_GROUP out of range"
+#endif
+
+}  // namespace gb

@@ -1,0 +1,1011 @@
+// Device side of the persistent tcgen05 GEMM: configuration, shared-memory control
+// block, bounded waits, the copy / MMA / epilogue roles and the kernel template, plus
+// the host launchers' declarations.  Kernel instances are compiled in separate
+// translation units (gemm_inst.cu) so that the build runs in parallel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gb300_gemm.h"
+#include "layout.hpp"
+#include "ptx.cuh"
+
+namespace gb {
+
+constexpr int kBN = 256;             // N of one MMA instruction (and the single variant's tile)
+constexpr int kPairTileN = 256;      // output tile columns of the pair variant (256 or 512)
+constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
+constexpr int kRowsA = 128;          // A rows staged per CTA (one MMA's M per SM)
+constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
+constexpr int kSwz = 64;             // elements per 128-byte swizzle span
+constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
+constexpr int kTmemCols = 512;       // all of Tensor Memory: accumulators of 512 fp32 columns
+constexpr int kCtlBytes = 256;
+constexpr int kMaxStages = 8;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// Two variants share all code:
+//  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64,
+//         two 256-column accumulators in TMEM (the epilogue of one tile overlaps the main
+//         loop of the next);
+//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x kPairTileN tile; the
+//         even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256) reading both CTAs'
+//         shared memory, and each CTA's TMEM holds its own 128 rows of the accumulator.
+//         Each CTA stages its 128 A rows and, per 256-column MMA, its 128 of the 256 B rows.
+//         A 512-column tile (kPairTileN = 512) feeds two MMAs from one k-block of A; the
+//         accumulator then fills TMEM, the epilogue no longer overlaps the next tile, and
+//         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
+//         the copy side's time did not drop with the 25 % fewer bytes (it follows the count
+//         of pipeline stages), so 256-column tiles with the overlapped epilogue stay.
+// Input kinds: 16-bit (fp16/bf16, kind::f16), FP8 (kind::f8f6f4) and block-scaled FP8
+// (kind::mxf8f6f4 with one E8M0 scale per 32 K elements of each row of A and column of B).
+enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
+
+// Block-scaled FP8 uses 224-column tiles: two accumulators (at TMEM columns 0 and 256) and,
+// in the 32 columns behind each, one slot of scale factors (4 columns for A's 128 rows, 8
+// for B's columns), so the epilogue still overlaps the next tile.
+constexpr int kMxTileN = 224;
+constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
+
+// Kernel shapes: the standard tiles, the CTA pair in clusters of two pairs sharing B by
+// multicast, and narrow single-CTA tiles (128 x 64) for problems with few output columns.
+enum : int { kShapeStd = 0, kShapeMc = 1, kShapeNarrow = 2 };
+constexpr int kNarrowTileN = 64;
+
+template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
+struct Cfg {
+  static constexpr bool kMx = kIn == kInMx;
+  static constexpr bool kNarrow = kShape == kShapeNarrow;
+  static constexpr int kTileM = kPair ? 256 : 128;
+  static constexpr int kTileN = kNarrow ? kNarrowTileN : (kMx ? kMxTileN : (kPair ? kPairTileN : kBN));
+  static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
+  static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
+  static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
+  static constexpr int kRowsB = kRowsBSub * kNSub;                // B rows a CTA stages per k-block
+  static constexpr int kAccBufs = (kMx || kTmemCols / kTileN >= 2) ? 2 : 1;   // accumulators in TMEM
+  static constexpr int kAccStride = kMx ? 256 : kTileN;           // TMEM columns between them
+  static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1;       // k-blocks per stage
+  // narrow tiles: 24 KiB k-blocks, eight in flight
+  static constexpr int kStages = kNarrow ? 8 : ((kPair && kNSub == 1) ? 3 : 4);
+  static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;            // producer, MMA, epilogue warps
+  static constexpr int kAHalf = kRowsA * kBK * 2;                // one k-block of A (bytes)
+  static constexpr int kBSub = kRowsBSub * kBK * 2;              // one k-block of one MMA's B rows
+  static constexpr int kBHalf = kRowsB * kBK * 2;                // one k-block of B (bytes)
+  static constexpr int kSfBytes = kMx ? kMxSfBytes : 0;          // one k-block's scale factors
+  static constexpr int kAStage = kAHalf * kKB;
+  static constexpr int kBStage = kBHalf * kKB;
+  static constexpr int kSfOff = kAStage + kBStage;               // scale factors after A and B
+  // stage bases stay 1024-byte aligned (the swizzle atom)
+  static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
+  // bytes one k-block adds to the (even CTA's) full barrier: both CTAs' copies in a pair
+  static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf + kSfBytes) * (kPair ? 2 : 1);
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+  static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
+  static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
+  static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
+  static_assert(kStages <= kMaxStages, "control block");
+  static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kNSub == 0, "TMEM accumulators");
+  static_assert(!kMx || (kTileN <= 224 && kTileN % 32 == 0 && kBSub % 1024 == 0), "MX tile");
+  static_assert(!kNarrow || (!kPair && !kMx), "narrow tiles: single CTA, 16-bit or FP8 inputs");
+};
+static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
+
+struct Params {
+  int32_t M, N, K;
+  int32_t m_tiles, n_tiles, k_blocks, num_tiles, group_m;
+  int32_t majorA, majorB;     // 0: K-major, 1: MN-major
+  float alpha, beta;
+  const uint16_t* C;
+  uint16_t* D;
+  int64_t d_grid_m, d_grid_n; // D/C offset per tile step (grid mode of the divide)
+  int64_t d_row, d_col;       // D/C offset per element step (tile mode of the divide)
+  uint32_t idesc;
+  int32_t vec_ok, has_c;
+  uint64_t timeout_ns;
+  int64_t skip_kb;
+  // stream-K schedule: each CTA (pair) first runs data-parallel tiles t = c, c + G, ... <
+  // dp_tiles, then an even, contiguous share of the remaining (tile, stage-block) units.
+  int32_t nsb;                // stage-blocks per tile
+  int32_t dp_tiles;           // tiles run whole; == num_tiles when stream-K is off
+  uint32_t epoch;             // launch number, written to the partial-ready flags
+  float* ws_part;             // per CTA slot: one 128 x 256 fp32 partial accumulator
+  uint32_t* ws_flags;         // per CTA slot: epoch of the last partial written
+  // fused epilogue ("CUTLASS, in depth" — "Epilogue fusion"): v = alpha*acc + beta*c,
+  // v += bias[column], v = act(v), amax = max |v|, D = v (16-bit) or sat_fp8(v * out_scale)
+  int32_t fused;              // 0: plain alpha/beta epilogue
+  const uint16_t* bias;       // N values of the input type, or null
+  int32_t act;                // 0 none, 1 ReLU, 2 GELU (erf form)
+  float* amax;                // device float receiving max |v| (by atomic max), or null
+  int32_t out_fmt;            // 0 same 16-bit type as the inputs, 1 FP8 E4M3, 2 FP8 E5M2
+  float out_scale;
+  int32_t vec8_ok;            // 16-byte FP8 stores legal (N % 16 == 0)
+  int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
+  uint32_t* status;           // device status word: first failing wait, 0 if none
+};
+
+// Largest stream-K slot of any variant (floats): sizes the workspace.
+constexpr int kSlotFloats = kRowsA * (kPairTileN > kBN ? kPairTileN : kBN);
+
+struct Ctl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint64_t part_done;         // epilogue warps finished writing a stream-K partial
+  uint64_t fix_done;          // epilogue warps finished reading other CTAs' partials
+  uint32_t tmem_base;
+  int32_t abort;
+  uint32_t* status;           // copy of Params::status for the wait helpers
+};
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+
+enum : uint32_t {
+  kSiteEmpty = 1,     // copy stage waiting for a free ring slot
+  kSiteFull = 2,      // MMA waiting for a k-block to land
+  kSiteAccEmpty = 3,  // MMA waiting for the epilogue to free an accumulator
+  kSiteAccFull = 4,   // epilogue waiting for a finished accumulator
+  kSiteDrain = 5,     // abort path: waiting for own operations in flight
+  kSiteTail = 6,      // copy stage waiting for the last releases before exit
+  kSiteFixup = 7,     // tile owner waiting for another CTA's stream-K partial
+};
+
+// Record the first failing wait, and stop this CTA (and its peer, in a pair).
+template <bool kPair>
+__device__ __forceinline__ void raise_status(Ctl* ctl, uint32_t site) {
+  atomicCAS(ctl->status, 0u, site | (blockIdx.x << 8));
+  *reinterpret_cast<volatile int32_t*>(&ctl->abort) = 1;
+  if constexpr (kPair) {
+    const uint32_t me = cluster_ctarank(), n = cluster_nctarank();
+    for (uint32_t c = 0; c < n; ++c)
+      if (c != me) st_cluster_u32(map_to_cta(smem_addr(&ctl->abort), c), 1u);
+  }
+}
+
+__device__ __forceinline__ bool aborted(Ctl* ctl) {
+  return *reinterpret_cast<volatile int32_t*>(&ctl->abort) != 0;
+}
+
+template <bool kCluster>
+__device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity) {
+  if constexpr (kCluster)
+    return mbar_try_wait_cluster(bar, parity);
+  else
+    return mbar_try_wait(bar, parity);
+}
+
+// Single-thread bounded wait; gives up on the abort flag or the time limit.  kCluster
+// selects a cluster-scope acquire: needed only where the arrivals are plain thread
+// arrivals from the peer CTA; barriers completed by copies or tcgen05.commit are
+// waited at CTA scope.
+template <bool kPair, bool kCluster = false>
+__device__ __noinline__ bool wait_one_slow(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
+                                           uint32_t site) {
+  if (probe<kCluster>(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (probe<kCluster>(bar, parity)) return true;
+    if ((n & 7) == 0) {
+      if (aborted(ctl)) return false;
+      if (global_timer_ns() - t0 > limit) {
+        raise_status<kPair>(ctl, site);
+        return false;
+      }
+    }
+  }
+}
+
+// The common case (already complete) stays inline: one probe, no call.  Measured: the
+// per-stage hand-off cost of the call alone was ~5 % of an 8192^3 GEMM.
+template <bool kPair, bool kCluster = false>
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
+                                         uint32_t site) {
+  if (probe<kCluster>(bar, parity)) return true;
+  return wait_one_slow<kPair, kCluster>(bar, parity, ctl, limit, site);
+}
+
+// Bounded wait that ignores the abort flag (used to drain own work after an abort).
+static __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64_t limit, uint32_t* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit) {
+      atomicCAS(status, 0u, kSiteDrain | (blockIdx.x << 8));
+      return false;
+    }
+  }
+  return true;
+}
+
+// Warp-collective bounded wait with a warp-uniform outcome.
+template <bool kPair>
+__device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, uint64_t limit,
+                                       uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    const bool ok = probe<false>(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((n & 7) == 7) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (aborted(ctl)) {
+          stop = 1;
+        } else if (global_timer_ns() - t0 > limit) {
+          raise_status<kPair>(ctl, site);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+// Grouped raster order: runs of group_m M-tiles, walked down M first, then across N,
+// so that CTAs working at the same time share A rows and B columns in L2 ("CUTLASS, in
+// depth" — "Kernel schedules", rasterisation).
+__device__ __forceinline__ void raster(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
+                                       int32_t& mt, int32_t& nt) {
+  const int32_t per_group = group_m * n_tiles;
+  const int32_t g = t / per_group;
+  const int32_t first_m = g * group_m;
+  const int32_t gm = min(m_tiles - first_m, group_m);
+  const int32_t local = t - g * per_group;
+  mt = first_m + local % gm;
+  nt = local / gm;
+}
+
+__device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t& mt, int32_t& nt) {
+  raster(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
+}
+
+// Tile of work item t for pair `pidx` of its cluster.  With B multicast (kMc) a work item
+// is a super-tile of two M-tiles over one column of B tiles: pair 0 takes M-tile 2s,
+// pair 1 takes 2s + 1 (past the last M-tile when m_tiles is odd: its rows are all out of
+// range, and it still loads its share of B for pair 0).
+template <bool kMc>
+__device__ __forceinline__ void item_coords(const Params& p, int32_t t, uint32_t pidx, int32_t& mt,
+                                            int32_t& nt) {
+  if constexpr (kMc) {
+    int32_t sm;
+    raster(t, (p.m_tiles + 1) / 2, p.n_tiles, max(1, p.group_m / 2), sm, nt);
+    mt = 2 * sm + static_cast<int32_t>(pidx);
+  } else {
+    tile_coords(p, t, mt, nt);
+  }
+}
+
+// One unit of work: stage-blocks [sb0, sb1) of tile `tile`.
+struct Item {
+  int32_t tile, sb0, sb1;
+};
+
+// The work list of one CTA (or pair), walked identically by the copy, MMA and epilogue
+// roles.  Stream-K part: the U = (num_tiles - dp_tiles) * nsb remaining units are cut
+// into G contiguous ranges [c*U/G, (c+1)*U/G); an item never crosses a tile boundary.
+struct Sched {
+  int32_t dp_next;
+  int64_t u, u_end;
+  __device__ __forceinline__ void init(const Params& p, uint32_t c, uint32_t G) {
+    dp_next = static_cast<int32_t>(c);
+    const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+    u = U * c / G;
+    u_end = U * (c + 1) / G;
+  }
+  __device__ __forceinline__ bool next(const Params& p, uint32_t G, Item& it) {
+    if (dp_next < p.dp_tiles) {
+      it.tile = dp_next;
+      it.sb0 = 0;
+      it.sb1 = p.nsb;
+      dp_next += static_cast<int32_t>(G);
+      return true;
+    }
+    if (u >= u_end) return false;
+    const int64_t gu = static_cast<int64_t>(p.dp_tiles) * p.nsb + u;
+    it.tile = static_cast<int32_t>(gu / p.nsb);
+    it.sb0 = static_cast<int32_t>(gu % p.nsb);
+    const int64_t span = u_end - u, room = p.nsb - it.sb0;
+    it.sb1 = it.sb0 + static_cast<int32_t>(span < room ? span : room);
+    u += it.sb1 - it.sb0;
+    return true;
+  }
+};
+
+// The CTA (pair) whose stream-K range holds unit index `gu` (counted over all tiles).
+__device__ __forceinline__ uint32_t sk_owner_of(const Params& p, uint32_t G, int64_t gu) {
+  const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+  const int64_t v = gu - static_cast<int64_t>(p.dp_tiles) * p.nsb;
+  return static_cast<uint32_t>(((v + 1) * G + U - 1) / U - 1);
+}
+
+// True when CTA (pair) c's stream-K range holds at least one unit (with fewer units than
+// CTAs some ranges are empty, and those CTAs hand nothing over).
+__device__ __forceinline__ bool sk_has_units(const Params& p, uint32_t G, uint32_t c) {
+  const int64_t U = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.nsb;
+  return U * (c + 1) / G > U * c / G;
+}
+
+// C/D offset of in-tile element (r, c) of tile (mt, nt): the divided layout evaluated.
+__device__ __forceinline__ int64_t d_offset(const Params& p, int32_t mt, int32_t nt, int32_t r,
+                                            int32_t c) {
+  return mt * p.d_grid_m + nt * p.d_grid_n + r * p.d_row + c * p.d_col;
+}
+
+// Copies of one k-block of one operand, `rows` rows starting at row0.  K-major: one box of
+// 64 (K) x rows.  MN-major: rows/64 boxes of 64 (M or N) x 64 (K), 8 KiB each, back to back.
+template <bool kPair>
+__device__ __forceinline__ void issue_operand(int major, const void* tm, uint32_t dst, uint32_t bar,
+                                              int32_t row0, int rows, int32_t kb, int32_t bk_elems) {
+  if (major == 0) {
+    // a K-major k-block is one 128-byte swizzle row per operand row: 64 16-bit or 128
+    // 8-bit elements
+    if constexpr (kPair)
+      tma_load_2d_pair(dst, tm, bar, kb * bk_elems, row0);
+    else
+      tma_load_2d(dst, tm, bar, kb * bk_elems, row0);
+  } else {
+    for (int j = 0; j < rows / kSwz; ++j) {
+      if constexpr (kPair)
+        tma_load_2d_pair(dst + j * kChunkBytes, tm, bar, row0 + j * kSwz, kb * kBK);
+      else
+        tma_load_2d(dst + j * kChunkBytes, tm, bar, row0 + j * kSwz, kb * kBK);
+    }
+  }
+}
+
+// Shared-memory descriptor of the k-th K=16 slice of a stage operand.
+//  K-major, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (stride offset);
+//    the leading offset is unused; the k-th slice starts 32 B further along the row.
+//  MN-major, 128-byte swizzle: 64-element MN chunks one box (8 KiB) apart (leading
+//    offset), 8-row K groups 1024 B apart (stride offset); the k-th slice starts 16 rows
+//    (2 KiB) further down.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k) {
+  if (major == 0) return smem_desc_sw128(base + k * (kUmmaK * 2), 16, 1024);
+  return smem_desc_sw128(base + k * (kUmmaK * 128), kChunkBytes, 1024);
+}
+
+template <bool kPair, int kIn, int kShape>
+__device__ void run_producer(const Params& p, const void* tmA, const void* tmB, const void* tmSFA,
+                             const void* tmSFB, uint8_t* smem, Ctl* ctl, uint32_t rank, uint32_t cluster,
+                             uint32_t nclusters) {
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
+  static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
+  // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
+  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
+  int stage = 0;
+  uint32_t phase = 0;
+  int64_t gkb = 0;
+  uint32_t issued = 0, issued_parity = 0;
+  bool ok = true;
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  while (ok && sched.next(p, nclusters, item)) {
+    int32_t mt, nt;
+    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA;
+    const int32_t b_row0 = nt * C::kTileN + static_cast<int32_t>(prank) * C::kRowsBSub;
+    for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
+      if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
+        ok = false;
+        break;
+      }
+      if (gkb != p.skip_kb) {
+        const uint32_t full = smem_addr(&ctl->full[stage]);
+        // in a pair both CTAs' copies are counted on the even CTA's barrier
+        const uint32_t full_tgt = kPair ? map_to_cta(full, leader) : full;
+        const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
+        // the last stage of a tile may hold fewer k-blocks: copy and count only those
+        const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
+        if (!kPair || prank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
+        for (int h = 0; h < nkb; ++h) {
+          const int32_t kb = sb * C::kKB + h;
+          issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
+                               p.bk_elems);
+          if constexpr (kMc) {
+            // both pairs need the same B rows: this CTA copies its pair's quarter of them
+            // (64 rows) into itself and the same-rank CTA of the other pair
+            const uint32_t dst = sa + C::kAStage + h * C::kBHalf + pidx * kChunkBytes;
+            const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+            if (p.majorB == 0)
+              tma_load_2d_pair_mc(dst, tmB, full_tgt, kb * p.bk_elems, b_row0 + pidx * kSwz, mask);
+            else
+              tma_load_2d_pair_mc(dst, tmB, full_tgt, b_row0 + pidx * kSwz, kb * kBK, mask);
+          } else {
+            // per MMA along N: this CTA's rows of that MMA's 256 tile columns
+#pragma unroll
+            for (int j = 0; j < C::kNSub; ++j)
+              issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
+                                   full_tgt, b_row0 + j * C::kMmaN, C::kRowsBSub, kb, p.bk_elems);
+          }
+          if constexpr (C::kMx) {
+            // scale factors, packed in 512-byte atoms (two 256-byte rows of the scale maps):
+            // A's atom of this CTA's 128 rows, then B's two atoms of the tile's columns
+            // (every CTA of a pair holds all of them)
+            const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
+            const int32_t rb = a_row0 / kRowsA;
+            const int32_t ya = 2 * (rb * p.k_blocks + kb), yb = 4 * (nt * p.k_blocks + kb);
+            if constexpr (kPair) {
+              tma_load_2d_pair(sf, tmSFA, full_tgt, 0, ya);
+              tma_load_2d_pair(sf + 512, tmSFB, full_tgt, 0, yb);
+            } else {
+              tma_load_2d(sf, tmSFA, full_tgt, 0, ya);
+              tma_load_2d(sf + 512, tmSFB, full_tgt, 0, yb);
+            }
+          }
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+      } else {
+        issued &= ~(1u << stage);
+      }
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (ok) {
+    // The consumer releases stages through asynchronous arrivals; wait for the last
+    // kStages releases so that none lands after this CTA's shared memory is gone.
+    for (int i = 0; i < C::kStages; ++i) {
+      if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteTail)) break;
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  } else if (!kPair || prank == 0) {
+    for (int s = 0; s < C::kStages; ++s)
+      if (issued & (1u << s))
+        wait_drain(smem_addr(&ctl->full[s]), (issued_parity >> s) & 1u, p.timeout_ns, p.status);
+  } else {
+    // the odd CTA's copies complete on the even CTA's barrier, which it cannot observe;
+    // a stage of 64 KiB lands in microseconds
+    __nanosleep(200000);
+  }
+}
+
+template <bool kPair, int kIn, int kShape>
+__device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
+                        uint32_t cluster, uint32_t nclusters) {
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
+  uint32_t kbc = 0;                        // k-blocks issued: selects the scale-factor slot
+  if (kPair && (rank & 1u) != 0) return;   // the even CTA issues for the pair
+  // a stage is free once every pair reading it has finished: with B multicast the other
+  // pair's copies land in this pair's stages too, so releases go to all four CTAs
+  const uint16_t release_mask = kMc ? 0xF : 0x3;
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true, issued_any = false;
+  int32_t it = 0;
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  for (; ok && sched.next(p, nclusters, item); ++it) {
+    const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+    const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+    if (!wait_one<kPair, kPair>(smem_addr(&ctl->acc_empty[buf]), use ^ 1u, ctl, p.timeout_ns,
+                                kSiteAccEmpty)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t d_tmem = tmem_base + buf * C::kAccStride;
+    for (int32_t sbk = item.sb0; sbk < item.sb1; ++sbk) {
+      if (!wait_one<kPair>(smem_addr(&ctl->full[stage]), phase, ctl, p.timeout_ns, kSiteFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
+      const uint32_t sb = sa + C::kAStage;
+      const int nkb = min(C::kKB, p.k_blocks - sbk * C::kKB);
+      // descriptors differ only in the start-address field (bits 0-13, bytes >> 4), which
+      // never carries for shared-memory addresses: build one per operand, then add offsets
+      const uint64_t da0 = operand_desc(sa, p.majorA, 0), db0 = operand_desc(sb, p.majorB, 0);
+      const uint32_t ka = p.majorA == 0 ? (kUmmaK * 2) >> 4 : (kUmmaK * 128) >> 4;
+      const uint32_t kb_ = p.majorB == 0 ? (kUmmaK * 2) >> 4 : (kUmmaK * 128) >> 4;
+      for (int h = 0; h < nkb; ++h) {
+        uint32_t sfa = 0, sfb = 0;
+        if constexpr (C::kMx) {
+          // this k-block's scale factors into a TMEM slot behind an accumulator (two slots
+          // alternate; copies and MMAs of one thread execute in issue order)
+          const uint32_t slot = tmem_base + C::kTileN + (kbc & 1u) * C::kAccStride;
+          const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
+          sfa = slot;
+          sfb = slot + 4;
+          if constexpr (kPair) {
+            tc_cp_32x128b_x4_pair(sfa, smem_desc_plain(sf, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb, smem_desc_plain(sf + 512, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+          } else {
+            tc_cp_32x128b_x4(sfa, smem_desc_plain(sf, 0, 128));
+            tc_cp_32x128b_x4(sfb, smem_desc_plain(sf + 512, 0, 128));
+            tc_cp_32x128b_x4(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+          }
+        }
+        ++kbc;
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k) {
+          const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
+          const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
+          // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and up to
+          // 256 columns; the N sub-tiles share the A slice
+#pragma unroll
+          for (int j = 0; j < C::kNSub; ++j) {
+            const uint64_t db = db0 + ((h * C::kBHalf + j * C::kBSub) >> 4) + k * kb_;
+            const uint32_t dt = d_tmem + j * C::kMmaN;
+            if constexpr (C::kMx) {
+              // the k-th 32-element slice takes scale byte k of each 32-bit scale cell
+              const uint32_t id = p.idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+              if constexpr (kPair)
+                tc_mma_mx_pair(dt, da, db, id, sfa, sfb, acc);
+              else
+                tc_mma_mx(dt, da, db, id, sfa, sfb, acc);
+            } else if constexpr (kPair && kIn == kIn8) {
+              tc_mma_f8_pair(dt, da, db, p.idesc, acc);
+            } else if constexpr (kPair) {
+              tc_mma_f16_pair(dt, da, db, p.idesc, acc);
+            } else if constexpr (kIn == kIn8) {
+              tc_mma_f8(dt, da, db, p.idesc, acc);
+            } else {
+              tc_mma_f16(dt, da, db, p.idesc, acc);
+            }
+          }
+        }
+      }
+      issued_any = true;
+      if constexpr (kPair)
+        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), release_mask);
+      else
+        tc_commit(smem_addr(&ctl->empty[stage]));
+      if (++stage == C::kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    const uint32_t af = smem_addr(&ctl->acc_full[buf]);
+    if (p.k_blocks == 0) {
+      mbar_arrive(af);
+      if constexpr (kPair) mbar_arrive_cluster(map_to_cta(af, rank + 1));
+    } else {
+      if constexpr (kPair)
+        tc_commit_pair_mc(af, pair_mask);
+      else
+        tc_commit(af);
+    }
+  }
+  if (!ok && issued_any) {
+    if constexpr (kPair)
+      tc_commit_pair(smem_addr(&ctl->drain));
+    else
+      tc_commit(smem_addr(&ctl->drain));
+    wait_drain(smem_addr(&ctl->drain), 0u, p.timeout_ns, p.status);
+    __nanosleep(20000);   // let the arrivals of earlier commits land
+  }
+}
+
+template <bool kBF16>
+__device__ __forceinline__ float to_f32(uint16_t b) {
+  if constexpr (kBF16)
+    return __bfloat162float(__ushort_as_bfloat16(b));
+  else
+    return __half2float(__ushort_as_half(b));
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint16_t from_f32(float v) {
+  if constexpr (kBF16)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else
+    return __half_as_ushort(__float2half_rn(v));
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return static_cast<uint32_t>(from_f32<kBF16>(lo)) |
+         (static_cast<uint32_t>(from_f32<kBF16>(hi)) << 16);
+}
+
+// 32 consecutive outputs of one row: v = alpha*acc (+ beta*c) in fp32.
+template <bool kBF16>
+__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, const uint4* cw,
+                                                const uint32_t (&acc)[32],
+                                                int valid, float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
+  if (!p.has_c) return;
+  if (cw != nullptr) {
+    // 32 C values loaded ahead as four 16-byte words
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
+                                v[8 * j + 2 * e]);
+        v[8 * j + 2 * e + 1] =
+            fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[off + i * p.d_col]), v[i]);
+  }
+}
+
+// Round v to the 16-bit output type and store it (16-byte stores when legal).
+template <bool kBF16>
+__device__ __forceinline__ void store_16(const Params& p, int64_t off, const float (&v)[32], int valid) {
+  if (p.vec_ok && valid == 32) {
+    uint4* dst = reinterpret_cast<uint4*>(p.D + off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 u;
+      u.x = pack2<kBF16>(v[8 * j + 0], v[8 * j + 1]);
+      u.y = pack2<kBF16>(v[8 * j + 2], v[8 * j + 3]);
+      u.z = pack2<kBF16>(v[8 * j + 4], v[8 * j + 5]);
+      u.w = pack2<kBF16>(v[8 * j + 6], v[8 * j + 7]);
+      dst[j] = u;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) p.D[off + i * p.d_col] = from_f32<kBF16>(v[i]);
+  }
+}
+
+// v * out_scale to FP8 with saturation to the largest finite value (round to nearest even).
+__device__ __forceinline__ uint32_t to_fp8(float x, int fmt) {
+  return fmt == 1 ? static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3))
+                  : static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2));
+}
+
+__device__ __forceinline__ void store_fp8(const Params& p, int64_t off, const float (&v)[32], int valid) {
+  uint8_t* d8 = reinterpret_cast<uint8_t*>(p.D);
+  if (p.vec8_ok && valid == 32) {
+    uint4* dst = reinterpret_cast<uint4*>(d8 + off);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int b = 16 * j + 4 * e;
+        w[e] = to_fp8(v[b] * p.out_scale, p.out_fmt) | (to_fp8(v[b + 1] * p.out_scale, p.out_fmt) << 8) |
+               (to_fp8(v[b + 2] * p.out_scale, p.out_fmt) << 16) |
+               (to_fp8(v[b + 3] * p.out_scale, p.out_fmt) << 24);
+      }
+      dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < valid) d8[off + i * p.d_col] = static_cast<uint8_t>(to_fp8(v[i] * p.out_scale, p.out_fmt));
+  }
+}
+
+// The epilogue of 32 consecutive outputs of one row (columns col0 .. col0+31).
+template <bool kBF16>
+__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint4* cw,
+                                          const uint32_t (&acc)[32], int valid, int64_t col0, float& amax) {
+  float v[32];
+  epilogue_values<kBF16>(p, off, cw, acc, valid, v);
+  if (!p.fused) {
+    store_16<kBF16>(p, off, v, valid);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (p.bias != nullptr && i < valid) v[i] += to_f32<kBF16>(__ldg(p.bias + col0 + i));
+    if (p.act == 1) v[i] = fmaxf(v[i], 0.0f);
+    if (p.act == 2) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
+    if (i < valid) amax = fmaxf(amax, fabsf(v[i]));
+  }
+  if (p.out_fmt == 0)
+    store_16<kBF16>(p, off, v, valid);
+  else
+    store_fp8(p, off, v, valid);
+}
+
+// Stream-K workspace slot of CTA (cluster c, rank r): a 128 x 256 fp32 partial stored
+// column-major ([column][row]) so that a warp's 32 rows form one 128-byte access.
+template <bool kPair>
+__device__ __forceinline__ float* part_slot(const Params& p, uint32_t c, uint32_t rank) {
+  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * Cfg<kPair>::kSlotFloats;
+}
+
+template <bool kPair>
+__device__ __forceinline__ uint32_t* part_flag(const Params& p, uint32_t c, uint32_t rank) {
+  return p.ws_flags + static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank;
+}
+
+// Warp-collective bounded wait until a partial-ready flag carries this launch's epoch.
+template <bool kPair>
+__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl* ctl, uint64_t limit) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t n = 0;; ++n) {
+      if (ld_acquire_gpu(flag) == epoch) {
+        ok = 1;
+        break;
+      }
+      if ((n & 63) == 63) {
+        if (aborted(ctl)) break;
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > limit) {
+          raise_status<kPair>(ctl, kSiteFixup);
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ld_acquire_gpu(flag);   // every lane acquires before reading the partial
+  return ok != 0;
+}
+
+template <bool kBF16, bool kPair, int kIn, int kShape>
+__device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
+                             uint32_t rank, uint32_t cluster, uint32_t nclusters) {
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
+  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
+  const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
+  const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
+  // with eight epilogue warps two share a lane quarter and split the columns
+  constexpr int kCols = C::kTileN / (C::kEpiWarps / 4);
+  const int cbeg = ((warp - 2) >> 2) * kCols;
+  const int r = static_cast<int>(prank) * kRowsA + lrow;   // row within the tile
+  int32_t it = 0;
+  float amax = 0.0f;                 // this thread's max |v| (fused epilogue)
+  Sched sched;
+  sched.init(p, cluster, nclusters);
+  Item item;
+  for (; sched.next(p, nclusters, item); ++it) {
+    int32_t mt, nt;
+    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
+    const int32_t cols_left = p.N - nt * C::kTileN;
+    const int64_t base = d_offset(p, mt, nt, r, 0);
+    const int cend = min(cbeg + kCols, static_cast<int>(min(cols_left, C::kTileN)));
+    // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
+    // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
+    // still runs; each later run is loaded kAhead runs before its use
+    const bool cvec = p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
+    constexpr int kRuns = kCols / 32;
+    constexpr int kAhead = C::kAccBufs == 1 ? 4 : 2;
+    uint4 cr[kAhead][4];
+    if (cvec && cend > cbeg)
+      prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a)
+      if (cvec && cbeg + 32 * a + 32 <= cend) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg + 32 * a);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cr[a][j] = __ldg(src + j);
+      }
+    const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
+    const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
+    if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
+    tc_fence_after_sync();
+    // stream-K roles: a contributor holds later k-units of a tile and hands its partial
+    // over; the owner (which holds k = 0) adds every contributor's partial.
+    const bool contributor = item.sb0 > 0;
+    const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
+    uint32_t c_lo = 1, c_hi = 0;
+    if (owner_with_parts) {
+      c_lo = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile) * p.nsb + item.sb1);
+      c_hi = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile + 1) * p.nsb - 1);
+      bool ok = true;
+      for (uint32_t c = c_lo; ok && c <= c_hi; ++c)
+        if (sk_has_units(p, nclusters, c))
+          ok = wait_flag<kPair>(part_flag<kPair>(p, c, rank), p.epoch, ctl, p.timeout_ns);
+      if (!ok) break;
+    }
+    float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
+#pragma unroll
+    for (int run = 0; run < kRuns; ++run) {
+      const int c0 = cbeg + 32 * run;
+      if (c0 >= cend) break;
+      uint32_t acc[32];
+      const bool vec_run = cvec && c0 + 32 <= cend;
+      if (p.k_blocks > 0) {
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0u;
+      }
+      if (contributor) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
+      } else {
+        for (uint32_t c = c_lo; c <= c_hi; ++c) {
+          if (!sk_has_units(p, nclusters, c)) continue;
+          const float* part = part_slot<kPair>(p, c, rank);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+        }
+        if (row_ok)
+          store_run<kBF16>(p, base + c0 * p.d_col, vec_run ? cr[run % kAhead] : nullptr, acc,
+                           min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
+      }
+      // refill this run's registers with the run kAhead further on
+      const int cn0 = c0 + 32 * kAhead;
+      if (cvec && cn0 + 32 <= cend) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cr[run % kAhead][j] = __ldg(src + j);
+      }
+    }
+    if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
+      if constexpr (kPair)
+        mbar_arrive_cluster(map_to_cta(ae, leader));
+      else
+        mbar_arrive(ae);
+      if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
+      if (owner_with_parts) mbar_arrive(smem_addr(&ctl->fix_done));
+    }
+    if (owner_with_parts && warp == 2) {
+      // the partials this CTA added are consumed: clear their flags, so that a later launch
+      // with the same launch number (a replayed CUDA graph) waits for fresh ones.  A CTA
+      // owns at most one split tile per launch, so fix_done completes phase 0 once.
+      if (!wait_warp<kPair>(smem_addr(&ctl->fix_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
+      if (lane == 0)
+        for (uint32_t c = c_lo; c <= c_hi; ++c)
+          if (sk_has_units(p, nclusters, c)) st_release_gpu(part_flag<kPair>(p, c, rank), 0u);
+      __syncwarp();
+    }
+    if (contributor && warp == 2) {
+      // a CTA contributes at most one partial per launch: part_done completes phase 0 once
+      // all epilogue warps have written theirs; then publish it at device scope
+      if (!wait_warp<kPair>(smem_addr(&ctl->part_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
+      if (lane == 0) {
+        fence_acq_rel_gpu();
+        st_release_gpu(part_flag<kPair>(p, cluster, rank), p.epoch);
+      }
+      __syncwarp();
+    }
+  }
+  if (p.fused && p.amax != nullptr) {
+    // one atomic per warp; |v| >= 0, so the float order equals the integer order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) atomicMax(reinterpret_cast<int*>(p.amax), __float_as_int(amax));
+  }
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <bool kBF16, bool kPair, int kIn, int kShape = kShapeStd>
+__global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                const Params p) {
+  using C = Cfg<kPair, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStages * C::kStageBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t cluster = kPair ? cluster_id_x() : blockIdx.x;
+  const uint32_t nclusters = kPair ? cluster_count_x() : gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_addr(&ctl->full[s]), 1);
+      mbar_init(smem_addr(&ctl->empty[s]), kMc ? 2 : 1);   // one release per pair reading it
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(smem_addr(&ctl->acc_full[b]), 1);
+      mbar_init(smem_addr(&ctl->acc_empty[b]), C::kAccEmptyArrivals);
+    }
+    mbar_init(smem_addr(&ctl->drain), 1);
+    mbar_init(smem_addr(&ctl->part_done), C::kEpiWarps);
+    mbar_init(smem_addr(&ctl->fix_done), C::kEpiWarps);
+    ctl->abort = 0;
+    ctl->status = p.status;
+    fence_barrier_init();
+    if (p.k_blocks > 0) {
+      prefetch_tensormap(&tmA);
+      prefetch_tensormap(&tmB);
+      if constexpr (C::kMx) {
+        prefetch_tensormap(&tmSFA);
+        prefetch_tensormap(&tmSFB);
+      }
+    }
+  }
+  if (warp == 1) {
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync();   // peer barriers initialised before any remote use
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0)
+      run_producer<kPair, kIn, kShape>(p, &tmA, &tmB, &tmSFA, &tmSFB, smem, ctl, rank, cluster, nclusters);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<kPair, kIn, kShape>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
+    __syncwarp();
+  } else {
+    run_epilogue<kBF16, kPair, kIn, kShape>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if constexpr (kPair) cluster_sync();   // no remote arrival or MMA targets a CTA that left
+  if (warp == 1) {
+    tc_fence_after_sync();
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host launch side
+// Per-device state the launchers keep (function attributes set, co-resident clusters).
+struct DeviceState {
+  bool probed = false;
+  int major = 0, minor = 0, sms = 0;
+  bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
+  bool attr_pair[2][3] = {};
+  bool attr_mc[2][3] = {};
+  int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
+  int mc_clusters = 0;     // co-resident 4-CTA clusters of the multicast kernel
+  uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
+  bool dbg_attr = false;
+  uint32_t* status = nullptr;   // device address of the status word
+};
+
+// The tensor maps of one call: A, B and, for block-scaled inputs, the packed scale factors.
+struct Maps {
+  CUtensorMap a, b, sfa, sfb;
+};
+
+// Defined in gemm_launch.cuh; instances come from gemm_inst.cu.
+template <bool kBF16, int kIn, int kShape>
+gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s);
+template <bool kBF16, int kIn, bool kMc>
+gb_status prepare_pair(DeviceState* dev);
+template <bool kBF16, int kIn, bool kMc>
+gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s);
+
+}  // namespace gb

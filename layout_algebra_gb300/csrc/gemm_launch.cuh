@@ -1,0 +1,77 @@
+// Host launchers of the GEMM kernel instances (included by gemm_inst.cu only).
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace gb {
+
+template <bool kBF16, int kIn, int kShape>
+gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s) {
+  using C = gb::Cfg<false, kIn, kShape>;
+  bool& attr = dev->attr_single[kBF16][kIn][kShape == gb::kShapeNarrow];
+  if (!attr) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kIn, kShape>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return GB_ERR_LAUNCH;
+    attr = true;
+  }
+  gb::gemm_kernel<kBF16, false, kIn, kShape><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, p);
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+template <bool kBF16, int kIn, bool kMc>
+gb_status prepare_pair(DeviceState* dev) {
+  using C = gb::Cfg<true, kIn>;
+  constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
+  bool& attr = kMc ? dev->attr_mc[kBF16][kIn] : dev->attr_pair[kBF16][kIn];
+  if (!attr) {
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes) != cudaSuccess)
+      return GB_ERR_LAUNCH;
+    attr = true;
+  }
+  int& clusters = kMc ? dev->mc_clusters : dev->pair_clusters;
+  if (clusters == 0) {
+    // a persistent grid must fit at once: ask how many clusters can be resident together
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCl;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(kCl * (dev->sms / kCl), 1, 1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, &cfg) != cudaSuccess ||
+        n <= 0)
+      n = dev->sms / kCl;
+    clusters = std::min(n, dev->sms / kCl);
+  }
+  return GB_OK;
+}
+
+template <bool kBF16, int kIn, bool kMc>
+gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s) {
+  using C = gb::Cfg<true, kIn>;
+  constexpr int kCl = kMc ? 4 : 2;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(kCl * clusters, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, m.a, m.b, m.sfa, m.sfb, p) != cudaSuccess)
+    return GB_ERR_LAUNCH;
+  return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
+}
+
+}  // namespace gb
