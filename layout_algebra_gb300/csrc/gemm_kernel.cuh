@@ -88,8 +88,6 @@ struct Cfg {
   static constexpr int kSfOff = kAStage + kBStage;               // scale factors after A and B
   // stage bases stay 1024-byte aligned (the swizzle atom)
   static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
-  // bytes one k-block adds to the (even CTA's) full barrier: both CTAs' copies in a pair
-  static constexpr uint32_t kTxPerKB = (kAHalf + kBHalf + kSfBytes) * (kPair ? 2 : 1);
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
   static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
   static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
@@ -132,6 +130,10 @@ struct Params {
   int32_t vec8_ok;            // 16-byte FP8 stores legal (N % 16 == 0)
   int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
   uint32_t* status;           // device status word: first failing wait, 0 if none
+  // bit 0 (A), bit 1 (B): the operand's tensor map is three-dimensional, (k-block elements,
+  // rows, k-blocks), and one copy moves all kKB k-blocks of a stage (CTA pair, K-major,
+  // K a multiple of the k-block); otherwise one two-dimensional copy per k-block
+  int32_t kb_boxes;
 };
 
 // Largest stream-K slot of any variant (floats): sizes the workspace.
@@ -382,6 +384,8 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
   // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
+  // stage-deep copies: CTA pairs without multicast, one 256-column MMA per k-block
+  constexpr bool kStageBoxes = kPair && !kMc && C::kNSub == 1 && C::kKB > 1;
   int stage = 0;
   uint32_t phase = 0;
   int64_t gkb = 0;
@@ -405,13 +409,28 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         // in a pair both CTAs' copies are counted on the even CTA's barrier
         const uint32_t full_tgt = kPair ? map_to_cta(full, leader) : full;
         const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
-        // the last stage of a tile may hold fewer k-blocks: copy and count only those
+        // the last stage of a tile may hold fewer k-blocks: copy and count only those (a
+        // stage-deep copy always lands whole, its k-blocks past K zero-filled)
         const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
-        if (!kPair || prank == 0) mbar_arrive_expect_tx(full, C::kTxPerKB * nkb);
+        bool a3 = false, b3 = false;
+        if constexpr (kStageBoxes) {
+          a3 = (p.kb_boxes & 1) != 0;
+          b3 = (p.kb_boxes & 2) != 0;
+        }
+        if (!kPair || prank == 0) {
+          const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * (b3 ? C::kKB : nkb) +
+                               C::kSfBytes * nkb) * (kPair ? 2u : 1u);
+          mbar_arrive_expect_tx(full, tx);
+        }
+        if constexpr (kStageBoxes) {
+          if (a3) tma_load_3d_pair(sa, tmA, full_tgt, 0, a_row0, sb * C::kKB);
+          if (b3) tma_load_3d_pair(sa + C::kAStage, tmB, full_tgt, 0, b_row0, sb * C::kKB);
+        }
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
-          issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
-                               p.bk_elems);
+          if (!a3)
+            issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
+                                 p.bk_elems);
           if constexpr (kMc) {
             // both pairs need the same B rows: this CTA copies its pair's quarter of them
             // (64 rows) into itself and the same-rank CTA of the other pair
@@ -421,7 +440,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
               tma_load_2d_pair_mc(dst, tmB, full_tgt, kb * p.bk_elems, b_row0 + pidx * kSwz, mask);
             else
               tma_load_2d_pair_mc(dst, tmB, full_tgt, b_row0 + pidx * kSwz, kb * kBK, mask);
-          } else {
+          } else if (!b3) {
             // per MMA along N: this CTA's rows of that MMA's 256 tile columns
 #pragma unroll
             for (int j = 0; j < C::kNSub; ++j)
@@ -998,6 +1017,7 @@ struct DeviceState {
 // The tensor maps of one call: A, B and, for block-scaled inputs, the packed scale factors.
 struct Maps {
   CUtensorMap a, b, sfa, sfb;
+  int32_t kb_boxes;   // Params::kb_boxes: which of a, b are stage-deep (three-dimensional) maps
 };
 
 // Defined in gemm_launch.cuh; instances come from gemm_inst.cu.

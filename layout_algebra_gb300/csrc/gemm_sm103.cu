@@ -365,6 +365,31 @@ gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], i
   return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
 }
 
+// Stage-deep map of a K-major operand described by the two-dimensional (K, rows) geometry of
+// plan_operand: the K mode divided by the k-block, (K):(1) -> (bk, K/bk):(1, bk), as in the
+// zipped_divide of the operand by (rows, bk), gives copy dimensions (bk, rows, k-blocks) with
+// byte strides (row_bytes, bk * bytes); the box takes `depth` k-blocks at once.  Used only
+// when K is a multiple of bk, so no row reads past its own K elements.
+gb_status encode_map_kblocks(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
+                             const int64_t box[2], int64_t depth, int dtype, bool f8) {
+  auto fn = encode_fn();
+  if (!fn) return GB_ERR_LAUNCH;
+  const int64_t bk = box[0], bytes = f8 ? 1 : 2;
+  if (dim[0] % bk != 0) return GB_ERR_INVALID_ARG;
+  cuuint64_t gdim[3] = {static_cast<cuuint64_t>(bk), static_cast<cuuint64_t>(dim[1]),
+                        static_cast<cuuint64_t>(dim[0] / bk)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(bk * bytes)};
+  cuuint32_t bdim[3] = {static_cast<cuuint32_t>(bk), static_cast<cuuint32_t>(box[1]),
+                        static_cast<cuuint32_t>(depth)};
+  cuuint32_t estride[3] = {1, 1, 1};
+  const CUtensorMapDataType t = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : (dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  CUresult r = fn(map, t, 3, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
+}
+
 gb_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
@@ -545,8 +570,27 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     if ((st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in)) != GB_OK) return st;
     std::memset(&maps, 0, sizeof(maps));
     if (K > 0) {
-      if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) return st;
-      if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
+      // CTA pairs without multicast copy a whole stage (kKB k-blocks) of a K-major operand
+      // with one three-dimensional copy when K is a multiple of the k-block: fewer, larger
+      // copies keep the per-SM copy rate up (the 128-row single k-block copies cost a fixed
+      // overhead each).  Other operands use one two-dimensional copy per k-block.
+      const int64_t depth = gb::Cfg<true>::kKB;
+      const bool stage_boxes = pl.variant == kVariantPair && gb::Cfg<true>::kNSub == 1 && depth > 1 &&
+                               K % in.bk() == 0;
+      if (stage_boxes && majorA == GB_K_MAJOR) {
+        if ((st = encode_map_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, depth, dtype, in.f8)) != GB_OK)
+          return st;
+        maps.kb_boxes |= 1;
+      } else if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) {
+        return st;
+      }
+      if (stage_boxes && majorB == GB_K_MAJOR) {
+        if ((st = encode_map_kblocks(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, depth, dtype, in.f8)) != GB_OK)
+          return st;
+        maps.kb_boxes |= 2;
+      } else if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) {
+        return st;
+      }
       if (in.mx) {
         // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
         // k-block), two atoms of B per (224 columns, k-block)
@@ -563,6 +607,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   Params p;
   fill_params(dev, pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
   p.bk_elems = in.bk();
+  p.kb_boxes = maps.kb_boxes;
   if (epi) {
     p.fused = 1;
     p.bias = static_cast<const uint16_t*>(epi->bias);

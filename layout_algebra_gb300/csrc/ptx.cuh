@@ -250,6 +250,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Three-dimensional form of the pair copy: the box spans (x, y, z) = (one k-block's elements,
+// rows, consecutive k-blocks), landing as z-many k-block slabs one after the other.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Pair copy multicast to the CTAs of `mask` (same shared-memory offset in each).  With
 // .cta_group::2 the bytes landing in a destination CTA are counted on the barrier at
 // `bar`'s offset in the even CTA of that destination's pair (`bar` names an even CTA).
