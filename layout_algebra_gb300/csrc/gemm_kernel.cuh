@@ -130,9 +130,10 @@ struct Params {
   int32_t vec8_ok;            // 16-byte FP8 stores legal (N % 16 == 0)
   int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
   uint32_t* status;           // device status word: first failing wait, 0 if none
-  // bit 0 (A), bit 1 (B): the operand's tensor map is three-dimensional, (k-block elements,
-  // rows, k-blocks), and one copy moves all kKB k-blocks of a stage (CTA pair, K-major,
-  // K a multiple of the k-block); otherwise one two-dimensional copy per k-block
+  // bit 0 (A), bit 1 (B): one copy moves all kKB k-blocks of the operand's stage (CTA pair,
+  // K a multiple of the k-block).  K-major: a three-dimensional map (k-block elements, rows,
+  // k-blocks); MN-major (rows a multiple of 64): four-dimensional (64 MN elements, K rows of
+  // a k-block, 64-wide MN chunks, k-blocks).  Otherwise one two-dimensional copy per k-block.
   int32_t kb_boxes;
 };
 
@@ -423,8 +424,18 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
           mbar_arrive_expect_tx(full, tx);
         }
         if constexpr (kStageBoxes) {
-          if (a3) tma_load_3d_pair(sa, tmA, full_tgt, 0, a_row0, sb * C::kKB);
-          if (b3) tma_load_3d_pair(sa + C::kAStage, tmB, full_tgt, 0, b_row0, sb * C::kKB);
+          if (a3) {
+            if (p.majorA == 0)
+              tma_load_3d_pair(sa, tmA, full_tgt, 0, a_row0, sb * C::kKB);
+            else
+              tma_load_4d_pair(sa, tmA, full_tgt, 0, 0, a_row0 / kSwz, sb * C::kKB);
+          }
+          if (b3) {
+            if (p.majorB == 0)
+              tma_load_3d_pair(sa + C::kAStage, tmB, full_tgt, 0, b_row0, sb * C::kKB);
+            else
+              tma_load_4d_pair(sa + C::kAStage, tmB, full_tgt, 0, 0, b_row0 / kSwz, sb * C::kKB);
+          }
         }
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;

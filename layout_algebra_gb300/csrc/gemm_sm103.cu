@@ -390,6 +390,32 @@ gb_status encode_map_kblocks(CUtensorMap* map, const void* base, const int64_t d
   return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
 }
 
+// Stage-deep map of an MN-major operand described by plan_operand's (rows, K) geometry (rows
+// contiguous, K rows `row_bytes` apart).  Dividing the row mode by 64 (one 128-byte swizzle
+// span) and the K mode by the k-block gives (64, chunks):(1, 64) and (bk, K/bk):(ld, bk ld);
+// ordered as the stage holds them, the copy dimensions are (64 MN elements, bk K rows,
+// MN chunks, k-blocks) with byte strides (row_bytes, 128, bk row_bytes).  The box takes
+// box_rows / 64 chunks and `depth` k-blocks.  Used only when rows and K are multiples of 64
+// and bk, so no copy reads an element outside the operand.
+gb_status encode_map_mn_kblocks(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
+                                int64_t box_rows, int64_t bk, int64_t depth, int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return GB_ERR_LAUNCH;
+  const int64_t span = gb::kSwz;
+  if (dim[0] % span != 0 || dim[1] % bk != 0 || box_rows % span != 0) return GB_ERR_INVALID_ARG;
+  cuuint64_t gdim[4] = {static_cast<cuuint64_t>(span), static_cast<cuuint64_t>(bk),
+                        static_cast<cuuint64_t>(dim[0] / span), static_cast<cuuint64_t>(dim[1] / bk)};
+  cuuint64_t gstride[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(span * 2),
+                           static_cast<cuuint64_t>(bk * row_bytes)};
+  cuuint32_t bdim[4] = {static_cast<cuuint32_t>(span), static_cast<cuuint32_t>(bk),
+                        static_cast<cuuint32_t>(box_rows / span), static_cast<cuuint32_t>(depth)};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, t, 4, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
+}
+
 gb_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
@@ -570,10 +596,10 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     if ((st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in)) != GB_OK) return st;
     std::memset(&maps, 0, sizeof(maps));
     if (K > 0) {
-      // CTA pairs without multicast copy a whole stage (kKB k-blocks) of a K-major operand
-      // with one three-dimensional copy when K is a multiple of the k-block: fewer, larger
-      // copies keep the per-SM copy rate up (the 128-row single k-block copies cost a fixed
-      // overhead each).  Other operands use one two-dimensional copy per k-block.
+      // CTA pairs without multicast copy a whole stage (kKB k-blocks) of an operand with one
+      // copy when K is a multiple of the k-block (and, MN-major, the operand's rows a multiple
+      // of 64): fewer, larger copies keep the per-SM copy rate up (each copy costs a fixed
+      // overhead).  Other operands use two-dimensional copies per k-block.
       const int64_t depth = gb::Cfg<true>::kKB;
       const bool stage_boxes = pl.variant == kVariantPair && gb::Cfg<true>::kNSub == 1 && depth > 1 &&
                                K % in.bk() == 0;
@@ -581,11 +607,21 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
         if ((st = encode_map_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, depth, dtype, in.f8)) != GB_OK)
           return st;
         maps.kb_boxes |= 1;
+      } else if (stage_boxes && !in.f8 && M % gb::kSwz == 0) {
+        if ((st = encode_map_mn_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, gb::kRowsA, in.bk(), depth, dtype)) !=
+            GB_OK)
+          return st;
+        maps.kb_boxes |= 1;
       } else if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) {
         return st;
       }
       if (stage_boxes && majorB == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, depth, dtype, in.f8)) != GB_OK)
+          return st;
+        maps.kb_boxes |= 2;
+      } else if (stage_boxes && !in.f8 && N % gb::kSwz == 0) {
+        if ((st = encode_map_mn_kblocks(&maps.b, B, pl.b_dim, pl.b_row_bytes, gb::Cfg<true>::kRowsBSub, in.bk(), depth,
+                                        dtype)) != GB_OK)
           return st;
         maps.kb_boxes |= 2;
       } else if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) {

@@ -261,6 +261,17 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Four-dimensional form of the pair copy (an MN-major operand's stage: 64-element MN runs,
+// K rows of a k-block, 64-wide MN chunks, consecutive k-blocks).
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, uint32_t bar,
+                                                 int32_t x, int32_t y, int32_t z, int32_t w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // Pair copy multicast to the CTAs of `mask` (same shared-memory offset in each).  With
 // .cta_group::2 the bytes landing in a destination CTA are counted on the barrier at
 // `bar`'s offset in the even CTA of that destination's pair (`bar` names an even CTA).

@@ -1,11 +1,12 @@
 """GPU parity of the stage-deep copies of the CTA-pair kernel.
 
-When an operand is K-major and K is a multiple of the k-block, the pair kernel copies both
-k-blocks of a stage with one three-dimensional tensor copy (k-block elements, rows,
-k-blocks); a last stage holding a single k-block still receives a whole box, its second
-k-block zero-filled past K.  These cases pin that path against the fp64 oracle: odd and
-even k-block counts, padded leading dimensions, one operand stage-deep and the other
-copied per k-block (MN-major), 16-bit and FP8 inputs.
+When K is a multiple of the k-block, the pair kernel copies both k-blocks of a stage with
+one tensor copy per operand: a K-major operand with a three-dimensional copy (k-block elements, rows,
+k-blocks), an MN-major one (rows a multiple of 64) with one four-dimensional copy; a last
+stage holding a single k-block still receives a whole box, its second k-block zero-filled
+past K.  These cases pin that path against the fp64 oracle: odd and even k-block counts,
+padded leading dimensions, mixed majors, rows that do and do not allow the MN-major stage
+copy, 16-bit and FP8 inputs.
 """
 import numpy as np
 import pytest
@@ -44,11 +45,15 @@ def ref16(p, data):
 
 
 @pytest.mark.parametrize("K", [64, 192, 320, 1024])
-@pytest.mark.parametrize("majors", [("K", "K"), ("K", "MN"), ("MN", "K")])
-def test_integer_exact_k_blocks(pair, K, majors):
-    M, N = 300, 520
-    lda = K + 16 if majors[0] == "K" else 304
-    ldb = K + 8 if majors[1] == "K" else 520
+@pytest.mark.parametrize("majors", [("K", "K"), ("K", "MN"), ("MN", "K"), ("MN", "MN")])
+@pytest.mark.parametrize("MN", [(300, 520), (320, 576)], ids=["rows_ragged", "rows_x64"])
+def test_integer_exact_k_blocks(pair, K, majors, MN):
+    # (300, 520): MN-major operands fall back to per-k-block copies (rows not a multiple of
+    # 64); (320, 576): they take the four-dimensional stage copies, with whole 64-row chunks
+    # past M and N zero-filled in the last tiles
+    M, N = MN
+    lda = K + 16 if majors[0] == "K" else -(-M // 8) * 8 + 8   # multiples of 8 elements
+    ldb = K + 8 if majors[1] == "K" else N
     p = W.Problem("sd", M, N, K, "f16", majorA=majors[0], majorB=majors[1], has_c=True,
                   alpha=1.0, beta=1.0, dist="int2", c_dist="int2", seed=K + 7, lda=lda, ldb=ldb)
     data = W.make(p)
