@@ -166,3 +166,17 @@ def test_argument_errors():
                                  0.0, None, A.data_ptr(), None, None, 0,
                                  torch.cuda.current_stream().cuda_stream)
         assert st == 1
+
+
+def test_host_operands_row_blocks():
+    """FP8 host operands through the row-block staging path equal one device call."""
+    p = W.Problem("h8", 2304, 272, 256, "bf16", has_c=True, alpha=0.75, beta=0.5, dist="uniform",
+                  c_dist="normal", seed=211, a_fmt="e4m3", b_fmt="e4m3")
+    data = W.make(p)
+    Dh = G.gemm_fp8(data["A"].pin_memory(), data["B"].pin_memory(), p.M, p.N, p.K,
+                    lda=data["lda"], ldb=data["ldb"], a_format=p.a_fmt, b_format=p.b_fmt,
+                    out_dtype=torch.bfloat16, alpha=p.alpha, beta=p.beta, C=data["C"].pin_memory())
+    torch.cuda.synchronize()
+    Dd = run(p, data)
+    assert not Dh.is_cuda
+    assert torch.equal(Dh.view(torch.int16), Dd.cpu().view(torch.int16))

@@ -227,6 +227,26 @@ def test_host_buffers_end_to_end():
     check(p, data, D)
 
 
+@pytest.mark.parametrize("dtype,M,majorA", [("bf16", 4096, "K"), ("f16", 5000, "K"), ("f16", 2304, "MN")])
+def test_host_buffers_row_blocks_match_device_call(dtype, M, majorA):
+    """Host operands go through the row-block staging path (A, C up and D down in blocks
+    overlapped with the GEMM); its result equals one device call over all rows."""
+    N, K = 520, 200
+    lda = K if majorA == "K" else M
+    p = W.Problem("e2eb", M, N, K, dtype, majorA=majorA, has_c=True, alpha=1.25, beta=0.5,
+                  dist="normal", c_dist="normal", seed=M + 3, lda=lda)
+    data = W.make(p)
+    assert len(G.row_blocks(M, majorA == "K")) == (1 if majorA == "MN" else min(8, M // 1024))
+    Dh = G.gemm(data["A"].pin_memory(), data["B"].pin_memory(), M, N, K, lda=lda,
+                ldb=data["ldb"], majorA=majorA, alpha=p.alpha, beta=p.beta,
+                C=data["C"].pin_memory())
+    torch.cuda.synchronize()
+    Dd = run(p, data)
+    assert not Dh.is_cuda
+    assert torch.equal(Dh.view(torch.int16), Dd.cpu().view(torch.int16))
+    check(p, data, Dh, *sample_entries(M, N, seed=5, n_random=4000))
+
+
 def test_device_misalignment_rejected():
     buf = torch.zeros(4096, dtype=torch.float16, device=DEV)
     s = torch.cuda.current_stream().cuda_stream
