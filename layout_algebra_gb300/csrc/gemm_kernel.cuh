@@ -30,7 +30,7 @@ constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
 constexpr int kSwz = 64;             // elements per 128-byte swizzle span
 constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
 constexpr int kTmemCols = 512;       // all of Tensor Memory: accumulators of 512 fp32 columns
-constexpr int kCtlBytes = 256;
+constexpr int kCtlBytes = 512;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -88,7 +88,14 @@ struct Cfg {
   static constexpr int kSfOff = kAStage + kBStage;               // scale factors after A and B
   // stage bases stay 1024-byte aligned (the swizzle atom)
   static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kCtlBytes;
+  // Tile-store epilogue: per epilogue warp two 32 x 32 staging tiles of D and two of C
+  // (16-bit, 64-byte rows), written back / read in by tensor copies; used when it fits
+  static constexpr int kEpiBufBytes = 32 * 64;
+  static constexpr int kEpiStageBytesFull = kEpiWarps * 4 * kEpiBufBytes;
+  static constexpr bool kEpiTma =
+      1024 + kStages * kStageBytes + kEpiStageBytesFull + kCtlBytes <= 227 * 1024;
+  static constexpr int kEpiStageBytes = kEpiTma ? kEpiStageBytesFull : 0;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiStageBytes + kCtlBytes;
   static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
   static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
@@ -135,6 +142,9 @@ struct Params {
   // k-blocks); MN-major (rows a multiple of 64): four-dimensional (64 MN elements, K rows of
   // a k-block, 64-wide MN chunks, k-blocks).  Otherwise one two-dimensional copy per k-block.
   int32_t kb_boxes;
+  // 1: the epilogue stages each 32 x 32 run of D in shared memory and writes it with a
+  // tensor copy (tmD), and reads C the same way (tmC); 16-bit D, row-major, N % 8 == 0
+  int32_t epi_tma;
 };
 
 // Largest stream-K slot of any variant (floats): sizes the workspace.
@@ -151,8 +161,10 @@ struct Ctl {
   uint32_t tmem_base;
   int32_t abort;
   uint32_t* status;           // copy of Params::status for the wait helpers
+  uint64_t c_full[8][2];      // tile-store epilogue: C staging tile landed (per warp, buffer)
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
+static_assert(kCtlBytes % 8 == 0, "control block alignment");
 
 enum : uint32_t {
   kSiteEmpty = 1,     // copy stage waiting for a free ring slot
@@ -162,6 +174,7 @@ enum : uint32_t {
   kSiteDrain = 5,     // abort path: waiting for own operations in flight
   kSiteTail = 6,      // copy stage waiting for the last releases before exit
   kSiteFixup = 7,     // tile owner waiting for another CTA's stream-K partial
+  kSiteEpiC = 8,      // epilogue waiting for a C tile copied into its staging buffer
 };
 
 // Record the first failing wait, and stop this CTA (and its peer, in a pair).
@@ -651,27 +664,31 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
          (static_cast<uint32_t>(from_f32<kBF16>(hi)) << 16);
 }
 
+// beta * c added to v from 32 C values held as four 16-byte words.
+template <bool kBF16>
+__device__ __forceinline__ void add_c_words(const Params& p, const uint4 (&cw)[4], float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t w[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)), v[8 * j + 2 * e]);
+      v[8 * j + 2 * e + 1] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
+    }
+  }
+}
+
 // 32 consecutive outputs of one row: v = alpha*acc (+ beta*c) in fp32.
 template <bool kBF16>
-__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, const uint4* cw,
+__device__ __forceinline__ void epilogue_values(const Params& p, int64_t off, bool have_cw, const uint4 (&cw)[4],
                                                 const uint32_t (&acc)[32],
                                                 int valid, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
   if (!p.has_c) return;
-  if (cw != nullptr) {
+  if (have_cw) {
     // 32 C values loaded ahead as four 16-byte words
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t w[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[8 * j + 2 * e] = fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] & 0xffffu)),
-                                v[8 * j + 2 * e]);
-        v[8 * j + 2 * e + 1] =
-            fmaf(p.beta, to_f32<kBF16>(static_cast<uint16_t>(w[e] >> 16)), v[8 * j + 2 * e + 1]);
-      }
-    }
+    add_c_words<kBF16>(p, cw, v);
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
@@ -729,16 +746,10 @@ __device__ __forceinline__ void store_fp8(const Params& p, int64_t off, const fl
   }
 }
 
-// The epilogue of 32 consecutive outputs of one row (columns col0 .. col0+31).
+// The fused nodes on 32 consecutive outputs of one row (columns col0 .. col0+31): bias,
+// activation, amax of the first `valid`.
 template <bool kBF16>
-__device__ __forceinline__ void store_run(const Params& p, int64_t off, const uint4* cw,
-                                          const uint32_t (&acc)[32], int valid, int64_t col0, float& amax) {
-  float v[32];
-  epilogue_values<kBF16>(p, off, cw, acc, valid, v);
-  if (!p.fused) {
-    store_16<kBF16>(p, off, v, valid);
-    return;
-  }
+__device__ __forceinline__ void fused_nodes(const Params& p, int valid, int64_t col0, float& amax, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     if (p.bias != nullptr && i < valid) v[i] += to_f32<kBF16>(__ldg(p.bias + col0 + i));
@@ -746,10 +757,27 @@ __device__ __forceinline__ void store_run(const Params& p, int64_t off, const ui
     if (p.act == 2) v[i] = 0.5f * v[i] * (1.0f + erff(v[i] * 0.70710678118654752f));
     if (i < valid) amax = fmaxf(amax, fabsf(v[i]));
   }
+}
+
+// The epilogue of 32 consecutive outputs of one row, stored by this thread.
+template <bool kBF16>
+__device__ __forceinline__ void store_run(const Params& p, int64_t off, bool have_cw, const uint4 (&cw)[4],
+                                          const uint32_t (&acc)[32], int valid, int64_t col0, float& amax) {
+  float v[32];
+  epilogue_values<kBF16>(p, off, have_cw, cw, acc, valid, v);
+  if (p.fused) fused_nodes<kBF16>(p, valid, col0, amax, v);
   if (p.out_fmt == 0)
     store_16<kBF16>(p, off, v, valid);
   else
     store_fp8(p, off, v, valid);
+}
+
+// Staging tiles of the tile-store epilogue: 32 rows of 64 bytes (32 16-bit values), in the
+// 64-byte swizzle of tensor copies: the 16-byte chunk j of row r sits at chunk
+// j ^ ((r >> 1) & 3), so a warp writing (or reading) one row per lane spreads each 16-byte
+// access over all banks.
+__device__ __forceinline__ uint32_t stage64_offset(int row, int chunk) {
+  return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
 // Stream-K workspace slot of CTA (cluster c, rank r): a 128 x 256 fp32 partial stored
@@ -792,9 +820,64 @@ __device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl
   return ok != 0;
 }
 
+// One 32-column run of the tile-store epilogue for this warp's 32 rows: C from its staging
+// tile (copied in two runs ahead), alpha/beta and the fused nodes, the 16-bit row written to
+// the D staging tile, one tensor copy of the 32 x 32 tile to D (clipped at M and N), and the
+// C staging tile refilled with the run two further on.  Returns false if a wait gave up.
+template <bool kBF16, bool kPair>
+__device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const uint32_t (&acc)[32], int ew,
+                                               int lane, uint32_t stg, uint32_t& gr, uint32_t& c_phase,
+                                               uint32_t& c_pending, bool tload_c, int run, int nruns, int32_t x0,
+                                               int32_t y0, int valid, int64_t col0, float& amax, const void* tmC,
+                                               const void* tmD) {
+  constexpr uint32_t kBuf = 32 * 64;
+  const uint32_t b = gr & 1u;
+  const uint32_t sd = stg + b * kBuf, sc = stg + (2 + b) * kBuf;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
+  if (tload_c) {
+    if (!wait_warp<kPair>(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, ctl, p.timeout_ns, kSiteEpiC))
+      return false;
+    c_phase ^= 1u << b;
+    c_pending &= ~(1u << b);
+    uint4 cw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cw[j] = ld_shared_u4(sc + stage64_offset(lane, j));
+    add_c_words<kBF16>(p, cw, v);
+  }
+  if (p.fused) fused_nodes<kBF16>(p, valid, col0, amax, v);
+  // the copy that last read this D staging tile (two runs back) must be done with it
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_u4(sd + stage64_offset(lane, j),
+                 make_uint4(pack2<kBF16>(v[8 * j + 0], v[8 * j + 1]), pack2<kBF16>(v[8 * j + 2], v[8 * j + 3]),
+                            pack2<kBF16>(v[8 * j + 4], v[8 * j + 5]), pack2<kBF16>(v[8 * j + 6], v[8 * j + 7])));
+  fence_proxy_async_smem();
+  __syncwarp();
+  const bool refill = tload_c && run + 2 < nruns;
+  if (lane == 0) {
+    tma_store_2d(tmD, sd, x0 + 32 * run, y0);
+    bulk_commit_group();
+    // this C tile is consumed (every lane passed the __syncwarp above): refill it with the
+    // run two further on
+    if (refill) {
+      const uint32_t bar = smem_addr(&ctl->c_full[ew][b]);
+      mbar_arrive_expect_tx(bar, kBuf);
+      tma_load_2d(sc, tmC, bar, x0 + 32 * (run + 2), y0);
+    }
+  }
+  if (refill) c_pending |= 1u << b;
+  ++gr;
+  return true;
+}
+
 template <bool kBF16, bool kPair, int kIn, int kShape>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
-                             uint32_t rank, uint32_t cluster, uint32_t nclusters) {
+                             uint32_t rank, uint32_t cluster, uint32_t nclusters, uint8_t* epi_smem,
+                             const void* tmC, const void* tmD) {
   using C = Cfg<kPair, kIn, kShape>;
   constexpr bool kMc = kShape == kShapeMc;
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
@@ -802,8 +885,18 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
   // with eight epilogue warps two share a lane quarter and split the columns
   constexpr int kCols = C::kTileN / (C::kEpiWarps / 4);
-  const int cbeg = ((warp - 2) >> 2) * kCols;
+  const int ew = warp - 2;           // epilogue warp index
+  const int cbeg = (ew >> 2) * kCols;
   const int r = static_cast<int>(prank) * kRowsA + lrow;   // row within the tile
+  constexpr int kRuns = kCols / 32;
+  // Tile-store epilogue (p.epi_tma): this warp's staging tiles D0, D1, C0, C1 and the
+  // barriers its C copies complete on.  Runs alternate between the two buffers by a count
+  // kept across tiles (gr), so a buffer is rewritten only once the copy that last read it
+  // (two runs earlier) has finished reading.
+  const bool tma = C::kEpiTma && p.epi_tma != 0;
+  const uint32_t stg = smem_addr(epi_smem) + static_cast<uint32_t>(ew) * 4u * C::kEpiBufBytes;
+  uint32_t gr = 0, c_phase = 0;
+  uint32_t c_pending = 0;            // staging buffers with a C copy issued, not yet waited for
   int32_t it = 0;
   float amax = 0.0f;                 // this thread's max |v| (fused epilogue)
   Sched sched;
@@ -816,11 +909,21 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const int32_t cols_left = p.N - nt * C::kTileN;
     const int64_t base = d_offset(p, mt, nt, r, 0);
     const int cend = min(cbeg + kCols, static_cast<int>(min(cols_left, C::kTileN)));
+    const int nruns = cend > cbeg ? (cend - cbeg + 31) / 32 : 0;
+    // stream-K roles: a contributor holds later k-units of a tile and hands its partial
+    // over; the owner (which holds k = 0) adds every contributor's partial.
+    const bool contributor = item.sb0 > 0;
+    const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
+    // tile-store path: the 32-row slab of this warp starts at row y0, its runs at x0 + 32 run
+    const bool tstore = tma && !contributor;
+    const bool tload_c = tstore && p.has_c;
+    const int32_t y0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA + q * 32;
+    const int32_t x0 = nt * C::kTileN + cbeg;
     // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
     // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
-    // still runs; each later run is loaded kAhead runs before its use
-    const bool cvec = p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
-    constexpr int kRuns = kCols / 32;
+    // still runs; each later run is loaded kAhead runs before its use.  On the tile-store
+    // path the first two runs of C are copied into the staging tiles instead.
+    const bool cvec = !tstore && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
     constexpr int kAhead = C::kAccBufs == 1 ? 4 : 2;
     uint4 cr[kAhead][4];
     if (cvec && cend > cbeg)
@@ -832,14 +935,21 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
         for (int j = 0; j < 4; ++j) cr[a][j] = __ldg(src + j);
       }
+    if constexpr (C::kEpiTma) {
+      if (tload_c && lane == 0) {
+        for (int a = 0; a < 2 && a < nruns; ++a) {
+          const uint32_t b = (gr + a) & 1u;
+          const uint32_t bar = smem_addr(&ctl->c_full[ew][b]);
+          mbar_arrive_expect_tx(bar, C::kEpiBufBytes);
+          tma_load_2d(stg + (2 + b) * C::kEpiBufBytes, tmC, bar, x0 + 32 * a, y0);
+        }
+      }
+      if (tload_c) c_pending |= (nruns > 0 ? 1u << (gr & 1u) : 0u) | (nruns > 1 ? 1u << ((gr + 1) & 1u) : 0u);
+    }
     const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
     const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
     if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
     tc_fence_after_sync();
-    // stream-K roles: a contributor holds later k-units of a tile and hands its partial
-    // over; the owner (which holds k = 0) adds every contributor's partial.
-    const bool contributor = item.sb0 > 0;
-    const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
     uint32_t c_lo = 1, c_hi = 0;
     if (owner_with_parts) {
       c_lo = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile) * p.nsb + item.sb1);
@@ -851,42 +961,53 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       if (!ok) break;
     }
     float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
+    bool ok = true;
 #pragma unroll
     for (int run = 0; run < kRuns; ++run) {
       const int c0 = cbeg + 32 * run;
-      if (c0 >= cend) break;
-      uint32_t acc[32];
-      const bool vec_run = cvec && c0 + 32 <= cend;
-      if (p.k_blocks > 0) {
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
-        tmem_ld_wait();
-      } else {
+      if (c0 < cend && ok) {
+        uint32_t acc[32];
+        if (p.k_blocks > 0) {
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * C::kAccStride + c0, acc);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0u;
-      }
-      if (contributor) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
-      } else {
-        for (uint32_t c = c_lo; c <= c_hi; ++c) {
-          if (!sk_has_units(p, nclusters, c)) continue;
-          const float* part = part_slot<kPair>(p, c, rank);
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+          for (int i = 0; i < 32; ++i) acc[i] = 0u;
         }
-        if (row_ok)
-          store_run<kBF16>(p, base + c0 * p.d_col, vec_run ? cr[run % kAhead] : nullptr, acc,
-                           min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
-      }
-      // refill this run's registers with the run kAhead further on
-      const int cn0 = c0 + 32 * kAhead;
-      if (cvec && cn0 + 32 <= cend) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
+        if (contributor) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cr[run % kAhead][j] = __ldg(src + j);
+          for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
+        } else {
+          for (uint32_t c = c_lo; c <= c_hi; ++c) {
+            if (!sk_has_units(p, nclusters, c)) continue;
+            const float* part = part_slot<kPair>(p, c, rank);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+          }
+          if (C::kEpiTma && tstore)
+            ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
+                                              nruns, x0, y0, row_ok ? min(32, cols_left - c0) : 0,
+                                              static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD);
+          else if (row_ok)
+            store_run<kBF16>(p, base + c0 * p.d_col, cvec && c0 + 32 <= cend, cr[0], acc,
+                             min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
+          // rotate the C registers (fixed indices keep them in registers) and load the run
+          // kAhead further on into the last slot
+#pragma unroll
+          for (int a = 0; a + 1 < kAhead; ++a)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cr[a][j] = cr[a + 1][j];
+          const int cn0 = c0 + 32 * kAhead;
+          if (cvec && cn0 + 32 <= cend) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cr[kAhead - 1][j] = __ldg(src + j);
+          }
+        }
       }
     }
+    if (!ok) break;
     if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
     tc_fence_before_sync();
     __syncwarp();
@@ -920,6 +1041,17 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       __syncwarp();
     }
   }
+  if constexpr (C::kEpiTma) {
+    // every tile store issued by this warp has written D, and every C copy into its staging
+    // tiles (outstanding only after an abort) has landed, before the CTA finishes
+    if (tma && lane == 0) {
+      bulk_wait_group<0>();
+      for (uint32_t b = 0; b < 2; ++b)
+        if (c_pending & (1u << b))
+          wait_drain(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, p.timeout_ns, p.status);
+    }
+    __syncwarp();
+  }
   if (p.fused && p.amax != nullptr) {
     // one atomic per warp; |v| >= 0, so the float order equals the integer order
 #pragma unroll
@@ -936,12 +1068,14 @@ template <bool kBF16, bool kPair, int kIn, int kShape = kShapeStd>
 __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const Params p) {
   using C = Cfg<kPair, kIn, kShape>;
   constexpr bool kMc = kShape == kShapeMc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + C::kStages * C::kStageBytes);
+  uint8_t* epi_smem = smem + C::kStages * C::kStageBytes;   // tile-store staging (1024-aligned)
+  Ctl* ctl = reinterpret_cast<Ctl*>(epi_smem + C::kEpiStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
@@ -960,6 +1094,11 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     mbar_init(smem_addr(&ctl->drain), 1);
     mbar_init(smem_addr(&ctl->part_done), C::kEpiWarps);
     mbar_init(smem_addr(&ctl->fix_done), C::kEpiWarps);
+    if constexpr (C::kEpiTma)
+      for (int w = 0; w < C::kEpiWarps; ++w) {
+        mbar_init(smem_addr(&ctl->c_full[w][0]), 1);
+        mbar_init(smem_addr(&ctl->c_full[w][1]), 1);
+      }
     ctl->abort = 0;
     ctl->status = p.status;
     fence_barrier_init();
@@ -970,6 +1109,10 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
         prefetch_tensormap(&tmSFA);
         prefetch_tensormap(&tmSFB);
       }
+    }
+    if (C::kEpiTma && p.epi_tma) {
+      if (p.has_c) prefetch_tensormap(&tmC);
+      prefetch_tensormap(&tmD);
     }
   }
   if (warp == 1) {
@@ -995,7 +1138,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     if (lane == 0) run_mma<kPair, kIn, kShape>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
     __syncwarp();
   } else {
-    run_epilogue<kBF16, kPair, kIn, kShape>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters);
+    run_epilogue<kBF16, kPair, kIn, kShape>(p, ctl, tmem_base, warp, lane, rank, cluster, nclusters, epi_smem,
+                                            &tmC, &tmD);
   }
 
   tc_fence_before_sync();
@@ -1028,6 +1172,8 @@ struct DeviceState {
 // The tensor maps of one call: A, B and, for block-scaled inputs, the packed scale factors.
 struct Maps {
   CUtensorMap a, b, sfa, sfb;
+  CUtensorMap c, d;   // tile-store epilogue: C and D as (N, M) tensors, 32 x 32 boxes
+  int32_t epi_tma;    // Params::epi_tma: c (when C is read) and d are encoded
   int32_t kb_boxes;   // Params::kb_boxes: which of a, b are stage-deep (three-dimensional) maps
 };
 

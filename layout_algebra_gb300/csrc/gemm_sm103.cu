@@ -416,6 +416,37 @@ gb_status encode_map_mn_kblocks(CUtensorMap* map, const void* base, const int64_
   return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
 }
 
+// Tensor map of a row-major 16-bit M x N matrix (C or D, leading dimension N) for the
+// tile-store epilogue: dimensions (N, M), 32 x 32 boxes in the 64-byte swizzle.  A store
+// writes only the box's elements inside (N, M); a load zero-fills the rest.
+gb_status encode_tile_map(CUtensorMap* map, const void* base, int64_t M, int64_t N, int dtype) {
+  auto fn = encode_fn();
+  if (!fn) return GB_ERR_LAUNCH;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(N * 2)};
+  cuuint32_t bdim[2] = {32, 32};
+  cuuint32_t estride[2] = {1, 1};
+  const CUtensorMapDataType t = dtype == GB_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(map, t, 2, const_cast<void*>(base), gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GB_OK : GB_ERR_LAUNCH;
+}
+
+// Whether the kernel instance of (variant, input kind) has shared memory for the tile-store
+// epilogue's staging tiles.
+bool epi_tma_fits(int variant, int kind) {
+  using namespace gb;
+  if (variant == kVariantNarrow)
+    return kind == kIn8 ? Cfg<false, kIn8, kShapeNarrow>::kEpiTma : Cfg<false, kIn16, kShapeNarrow>::kEpiTma;
+  if (variant == kVariantPairMc)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeMc>::kEpiTma : Cfg<true, kIn16, kShapeMc>::kEpiTma;
+  if (is_pair(variant))
+    return kind == kInMx ? Cfg<true, kInMx>::kEpiTma
+                         : (kind == kIn8 ? Cfg<true, kIn8>::kEpiTma : Cfg<true, kIn16>::kEpiTma);
+  return kind == kInMx ? Cfg<false, kInMx>::kEpiTma
+                       : (kind == kIn8 ? Cfg<false, kIn8>::kEpiTma : Cfg<false, kIn16>::kEpiTma);
+}
+
 gb_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
@@ -513,11 +544,13 @@ int64_t workspace_bytes_for(int sms) {
 struct PlanKey {
   int device, dtype, kind, a_fmt, b_fmt, variant, majorA, majorB;
   int64_t M, N, K, lda, ldb;
-  const void *A, *B, *sfa, *sfb;
+  const void *A, *B, *sfa, *sfb, *C, *D;
+  bool epi_tma;
   bool operator==(const PlanKey& o) const {
     return device == o.device && dtype == o.dtype && kind == o.kind && a_fmt == o.a_fmt && b_fmt == o.b_fmt &&
            variant == o.variant && majorA == o.majorA && majorB == o.majorB && M == o.M && N == o.N &&
-           K == o.K && lda == o.lda && ldb == o.ldb && A == o.A && B == o.B && sfa == o.sfa && sfb == o.sfb;
+           K == o.K && lda == o.lda && ldb == o.ldb && A == o.A && B == o.B && sfa == o.sfa && sfb == o.sfb &&
+           C == o.C && D == o.D && epi_tma == o.epi_tma;
   }
 };
 struct PlanEntry {
@@ -588,8 +621,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
+  // tile-store epilogue: 16-bit D stored by 32 x 32 tensor copies (row-major, N % 8 == 0; C
+  // read the same way); other outputs use per-thread stores
+  const bool epi_tma = (N % 8 == 0) && (!epi || epi->out_format == GB_OUT_INPUT_TYPE) &&
+                       epi_tma_fits(variant, in.kind());
+  const void* c_key = epi_tma && beta != 0.0f ? C : nullptr;
   const PlanKey key{device, dtype, in.kind(), in.a_fmt, in.b_fmt, variant, majorA, majorB, M, N, K, lda, ldb,
-                    K > 0 ? A : nullptr, K > 0 ? B : nullptr, in.mx ? sfa : nullptr, in.mx ? sfb : nullptr};
+                    K > 0 ? A : nullptr, K > 0 ? B : nullptr, in.mx ? sfa : nullptr, in.mx ? sfb : nullptr,
+                    c_key, epi_tma ? D : nullptr, epi_tma};
   gb_gemm_plan pl;
   Maps maps;
   if (!plan_cache_get(key, &pl, &maps)) {
@@ -638,12 +677,18 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
         if ((st = encode_map(&maps.sfb, sfb, b_dim, 256, b_box, dtype, true, false)) != GB_OK) return st;
       }
     }
+    if (epi_tma && pl.vector_epilogue) {
+      if ((st = encode_tile_map(&maps.d, D, M, N, dtype)) != GB_OK) return st;
+      if (c_key && (st = encode_tile_map(&maps.c, C, M, N, dtype)) != GB_OK) return st;
+      maps.epi_tma = 1;
+    }
     plan_cache_put(key, pl, maps);
   }
   Params p;
   fill_params(dev, pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
   p.bk_elems = in.bk();
   p.kb_boxes = maps.kb_boxes;
+  p.epi_tma = maps.epi_tma;
   if (epi) {
     p.fused = 1;
     p.bias = static_cast<const uint16_t*>(epi->bias);
