@@ -432,8 +432,9 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
           b3 = (p.kb_boxes & 2) != 0;
         }
         if (!kPair || prank == 0) {
+          // scale factors always arrive for the whole stage (one copy per operand)
           const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * (b3 ? C::kKB : nkb) +
-                               C::kSfBytes * nkb) * (kPair ? 2u : 1u);
+                               C::kSfBytes * C::kKB) * (kPair ? 2u : 1u);
           mbar_arrive_expect_tx(full, tx);
         }
         if constexpr (kStageBoxes) {
@@ -471,20 +472,22 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
               issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
                                    full_tgt, b_row0 + j * C::kMmaN, C::kRowsBSub, kb, p.bk_elems);
           }
-          if constexpr (C::kMx) {
-            // scale factors, packed in 512-byte atoms (two 256-byte rows of the scale maps):
-            // A's atom of this CTA's 128 rows, then B's two atoms of the tile's columns
-            // (every CTA of a pair holds all of them)
-            const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
-            const int32_t rb = a_row0 / kRowsA;
-            const int32_t ya = 2 * (rb * p.k_blocks + kb), yb = 4 * (nt * p.k_blocks + kb);
-            if constexpr (kPair) {
-              tma_load_2d_pair(sf, tmSFA, full_tgt, 0, ya);
-              tma_load_2d_pair(sf + 512, tmSFB, full_tgt, 0, yb);
-            } else {
-              tma_load_2d(sf, tmSFA, full_tgt, 0, ya);
-              tma_load_2d(sf + 512, tmSFB, full_tgt, 0, yb);
-            }
+        }
+        if constexpr (C::kMx) {
+          // scale factors, packed in 512-byte atoms (two 256-byte rows of the scale maps) that
+          // are consecutive in k-blocks: one copy of A's kKB atoms of this CTA's 128 rows, then
+          // one of B's 2 kKB atoms of the tile's columns (every CTA of a pair holds all of
+          // them); past a tile's last k-block the copy reads unused atoms (or zero fill)
+          const uint32_t sf = sa + C::kSfOff;
+          const int32_t kb0 = sb * C::kKB;
+          const int32_t rb = a_row0 / kRowsA;
+          const int32_t ya = 2 * (rb * p.k_blocks + kb0), yb = 4 * (nt * p.k_blocks + kb0);
+          if constexpr (kPair) {
+            tma_load_2d_pair(sf, tmSFA, full_tgt, 0, ya);
+            tma_load_2d_pair(sf + C::kKB * 512, tmSFB, full_tgt, 0, yb);
+          } else {
+            tma_load_2d(sf, tmSFA, full_tgt, 0, ya);
+            tma_load_2d(sf + C::kKB * 512, tmSFB, full_tgt, 0, yb);
           }
         }
         issued |= 1u << stage;
@@ -567,17 +570,19 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
           // this k-block's scale factors into a TMEM slot behind an accumulator (two slots
           // alternate; copies and MMAs of one thread execute in issue order)
           const uint32_t slot = tmem_base + C::kTileN + (kbc & 1u) * C::kAccStride;
-          const uint32_t sf = sa + C::kSfOff + h * C::kSfBytes;
+          // the stage holds A's kKB atoms, then B's kKB atom pairs
+          const uint32_t sfa_s = sa + C::kSfOff + h * 512;
+          const uint32_t sfb_s = sa + C::kSfOff + C::kKB * 512 + h * 1024;
           sfa = slot;
           sfb = slot + 4;
           if constexpr (kPair) {
-            tc_cp_32x128b_x4_pair(sfa, smem_desc_plain(sf, 0, 128));
-            tc_cp_32x128b_x4_pair(sfb, smem_desc_plain(sf + 512, 0, 128));
-            tc_cp_32x128b_x4_pair(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+            tc_cp_32x128b_x4_pair(sfa, smem_desc_plain(sfa_s, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb, smem_desc_plain(sfb_s, 0, 128));
+            tc_cp_32x128b_x4_pair(sfb + 4, smem_desc_plain(sfb_s + 512, 0, 128));
           } else {
-            tc_cp_32x128b_x4(sfa, smem_desc_plain(sf, 0, 128));
-            tc_cp_32x128b_x4(sfb, smem_desc_plain(sf + 512, 0, 128));
-            tc_cp_32x128b_x4(sfb + 4, smem_desc_plain(sf + 1024, 0, 128));
+            tc_cp_32x128b_x4(sfa, smem_desc_plain(sfa_s, 0, 128));
+            tc_cp_32x128b_x4(sfb, smem_desc_plain(sfb_s, 0, 128));
+            tc_cp_32x128b_x4(sfb + 4, smem_desc_plain(sfb_s + 512, 0, 128));
           }
         }
         ++kbc;

@@ -668,11 +668,13 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       }
       if (in.mx) {
         // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
-        // k-block), two atoms of B per (224 columns, k-block)
+        // k-block), two atoms of B per (224 columns, k-block); one copy takes a stage's kKB
+        // consecutive k-blocks
+        const int64_t kkb = is_pair(pl.variant) ? gb::Cfg<true, gb::kInMx>::kKB : gb::Cfg<false, gb::kInMx>::kKB;
         const int64_t a_rows = 2 * ((M + 127) / 128) * pl.k_blocks;
         const int64_t b_rows = 4 * pl.n_tiles * pl.k_blocks;
         const int64_t a_dim[2] = {256, a_rows}, b_dim[2] = {256, b_rows};
-        const int64_t a_box[2] = {256, 2}, b_box[2] = {256, 4};
+        const int64_t a_box[2] = {256, 2 * kkb}, b_box[2] = {256, 4 * kkb};
         if ((st = encode_map(&maps.sfa, sfa, a_dim, 256, a_box, dtype, true, false)) != GB_OK) return st;
         if ((st = encode_map(&maps.sfb, sfb, b_dim, 256, b_box, dtype, true, false)) != GB_OK) return st;
       }
