@@ -11,7 +11,10 @@
  * from shape:stride layouts divided into (tile, grid) modes ("Day 84: CUTLASS and CuTe
  * layouts" — "A layout is a shape and a stride").  The pair variant is used when
  * M > 128, the single-CTA variant otherwise, and narrow single-CTA tiles when N <= 64
- * (gb_set_kernel_variant overrides this).
+ * (gb_set_kernel_variant overrides this).  With K-major B (16-bit or FP8 inputs), a pair
+ * uses 256 x 224 tiles instead of 256 x 256 when that needs fewer tile-columns in all of its
+ * persistent waves ("CUTLASS, in depth" — "Worked example: tile choice and wave
+ * quantisation"): ceil(tiles / pairs) x width, pairs = half the device's SMs.
  *
  * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
  * "One notation, and no more transposes"):
@@ -250,16 +253,17 @@ gb_status gb_set_wait_timeout_ns(uint64_t ns);
 gb_status gb_debug_skip_k_block(int64_t k_block);
 
 /* Kernel variant for later calls (process-wide): 0 chooses by shape (the default: 4 when N
-   <= 64, else 2 when M > 128, else 1), 1 the single-CTA 128 x 256 kernel, 2 the CTA-pair
-   256 x 256 kernel, 3 the CTA-pair kernel in clusters of two pairs that share each B tile
-   through multicast copies (whole tiles only: the *_ws calls do not use stream-K with it),
-   4 the single-CTA kernel with narrow 128 x 64 tiles and eight 24 KiB stages (for outputs
-   with few columns; with a workspace, stream-K spreads K over the SMs).  Block-scaled FP8
-   has no form 3 or 4 and runs as 2 (M > 128) or 1.  GB_ERR_INVALID_ARG for other values. */
+   <= 64, else 1 when M <= 128, else 5 or 2 by the wave count above), 1 the single-CTA
+   128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 3 the CTA-pair kernel in clusters of
+   two pairs that share each B tile through multicast copies (whole tiles only: the *_ws
+   calls do not use stream-K with it), 4 the single-CTA kernel with narrow 128 x 64 tiles and
+   eight 24 KiB stages (for outputs with few columns; with a workspace, stream-K spreads K
+   over the SMs), 5 the CTA-pair kernel with 256 x 224 tiles (K-major B; with MN-major B it
+   runs as 2).  Block-scaled FP8 has no form 3, 4 or 5 and runs as 2 (M > 128) or 1.
+   GB_ERR_INVALID_ARG for other values. */
 gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2 or
-   3) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1 to 5) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
    in-tile element (r, c) (r < tile_m, c < tile_n, both from gb_gemm_make_plan), or -1
    when the element lies outside M x N.  out is a device buffer of tile_m * tile_n int64.
    Asynchronous on stream. */

@@ -5,33 +5,33 @@
 #include "gemm_launch.cuh"
 
 #ifndef GB_INST_GROUP
-#error "GB_INST_GROUP must be defined (0..9)"
+#error "GB_INST_GROUP must be defined (0..11)"
 #endif
 
 namespace gb {
 
-#define GB_PAIR(BF, IN, MC)                                                                  \
-  template gb_status prepare_pair<BF, IN, MC>(DeviceState*);                                 \
-  template gb_status launch_pair<BF, IN, MC>(const Maps&, const Params&, int, cudaStream_t);
+#define GB_PAIR(BF, IN, SHAPE)                                                               \
+  template gb_status prepare_pair<BF, IN, SHAPE>(DeviceState*);                              \
+  template gb_status launch_pair<BF, IN, SHAPE>(const Maps&, const Params&, int, cudaStream_t);
 #define GB_SINGLE(BF, IN, SHAPE) \
   template gb_status launch_single<BF, IN, SHAPE>(DeviceState*, const Maps&, const Params&, int, cudaStream_t);
 
 #if GB_INST_GROUP == 0      // the 16-bit CTA-pair kernels (the large-problem path)
-GB_PAIR(true, kIn16, false)
+GB_PAIR(true, kIn16, kShapeStd)
 #elif GB_INST_GROUP == 1
-GB_PAIR(false, kIn16, false)
+GB_PAIR(false, kIn16, kShapeStd)
 #elif GB_INST_GROUP == 2    // CTA pairs sharing B by multicast
-GB_PAIR(true, kIn16, true)
-GB_PAIR(false, kIn16, true)
+GB_PAIR(true, kIn16, kShapeMc)
+GB_PAIR(false, kIn16, kShapeMc)
 #elif GB_INST_GROUP == 3    // FP8 inputs, CTA pairs
-GB_PAIR(true, kIn8, false)
-GB_PAIR(false, kIn8, false)
+GB_PAIR(true, kIn8, kShapeStd)
+GB_PAIR(false, kIn8, kShapeStd)
 #elif GB_INST_GROUP == 4
-GB_PAIR(true, kIn8, true)
-GB_PAIR(false, kIn8, true)
+GB_PAIR(true, kIn8, kShapeMc)
+GB_PAIR(false, kIn8, kShapeMc)
 #elif GB_INST_GROUP == 5    // block-scaled FP8
-GB_PAIR(true, kInMx, false)
-GB_PAIR(false, kInMx, false)
+GB_PAIR(true, kInMx, kShapeStd)
+GB_PAIR(false, kInMx, kShapeStd)
 #elif GB_INST_GROUP == 6
 GB_SINGLE(true, kInMx, kShapeStd)
 GB_SINGLE(false, kInMx, kShapeStd)
@@ -41,6 +41,12 @@ GB_SINGLE(false, kIn16, kShapeStd)
 #elif GB_INST_GROUP == 8
 GB_SINGLE(true, kIn8, kShapeStd)
 GB_SINGLE(false, kIn8, kShapeStd)
+#elif GB_INST_GROUP == 10   // CTA pairs with 256 x 224 tiles
+GB_PAIR(true, kIn16, kShapeN224)
+GB_PAIR(false, kIn16, kShapeN224)
+#elif GB_INST_GROUP == 11
+GB_PAIR(true, kIn8, kShapeN224)
+GB_PAIR(false, kIn8, kShapeN224)
 #elif GB_INST_GROUP == 9    // single-CTA kernels, 128 x 64 tiles (few output columns)
 GB_SINGLE(true, kIn16, kShapeNarrow)
 GB_SINGLE(false, kIn16, kShapeNarrow)

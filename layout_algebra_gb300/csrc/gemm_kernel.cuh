@@ -58,22 +58,25 @@ constexpr int kMxTileN = 224;
 constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
 
 // Kernel shapes: the standard tiles, the CTA pair in clusters of two pairs sharing B by
-// multicast, and narrow single-CTA tiles (128 x 64) for problems with few output columns.
-enum : int { kShapeStd = 0, kShapeMc = 1, kShapeNarrow = 2 };
+// multicast, narrow single-CTA tiles (128 x 64) for problems with few output columns, and
+// CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a ragged last wave).
+enum : int { kShapeStd = 0, kShapeMc = 1, kShapeNarrow = 2, kShapeN224 = 3 };
 constexpr int kNarrowTileN = 64;
 
 template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
 struct Cfg {
   static constexpr bool kMx = kIn == kInMx;
   static constexpr bool kNarrow = kShape == kShapeNarrow;
+  static constexpr bool kN224 = kShape == kShapeN224;
   static constexpr int kTileM = kPair ? 256 : 128;
-  static constexpr int kTileN = kNarrow ? kNarrowTileN : (kMx ? kMxTileN : (kPair ? kPairTileN : kBN));
+  static constexpr int kTileN =
+      kNarrow ? kNarrowTileN : ((kMx || kN224) ? kMxTileN : (kPair ? kPairTileN : kBN));
   static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
   static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
   static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
   static constexpr int kRowsB = kRowsBSub * kNSub;                // B rows a CTA stages per k-block
   static constexpr int kAccBufs = (kMx || kTmemCols / kTileN >= 2) ? 2 : 1;   // accumulators in TMEM
-  static constexpr int kAccStride = kMx ? 256 : kTileN;           // TMEM columns between them
+  static constexpr int kAccStride = (kMx || kN224) ? 256 : kTileN;   // TMEM columns between them
   static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1;       // k-blocks per stage
   // narrow tiles: 24 KiB k-blocks, eight in flight
   static constexpr int kStages = kNarrow ? 8 : ((kPair && kNSub == 1) ? 3 : 4);
@@ -103,6 +106,7 @@ struct Cfg {
   static_assert(kAccBufs >= 1 && kAccBufs <= 2 && kTileN % kNSub == 0, "TMEM accumulators");
   static_assert(!kMx || (kTileN <= 224 && kTileN % 32 == 0 && kBSub % 1024 == 0), "MX tile");
   static_assert(!kNarrow || (!kPair && !kMx), "narrow tiles: single CTA, 16-bit or FP8 inputs");
+  static_assert(!kN224 || (kPair && !kMx), "224-column tiles: CTA pair, 16-bit or FP8 inputs");
 };
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -1160,15 +1164,16 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host launch side
+// Index of a pair shape in DeviceState's per-shape arrays.
+constexpr int pair_shape_index(int shape) { return shape == kShapeMc ? 1 : (shape == kShapeN224 ? 2 : 0); }
+
 // Per-device state the launchers keep (function attributes set, co-resident clusters).
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
   bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
-  bool attr_pair[2][3] = {};
-  bool attr_mc[2][3] = {};
-  int pair_clusters = 0;   // co-resident clusters of the pair kernel (0: not queried yet)
-  int mc_clusters = 0;     // co-resident 4-CTA clusters of the multicast kernel
+  bool attr_pair[2][3][3] = {};   // [bf16 out][input kind][pair shape: standard, multicast, 224 wide]
+  int pair_clusters[3] = {};      // co-resident clusters per pair shape (0: not queried yet)
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
   uint32_t* status = nullptr;   // device address of the status word
@@ -1185,9 +1190,9 @@ struct Maps {
 // Defined in gemm_launch.cuh; instances come from gemm_inst.cu.
 template <bool kBF16, int kIn, int kShape>
 gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s);
-template <bool kBF16, int kIn, bool kMc>
+template <bool kBF16, int kIn, int kShape>
 gb_status prepare_pair(DeviceState* dev);
-template <bool kBF16, int kIn, bool kMc>
+template <bool kBF16, int kIn, int kShape>
 gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s);
 
 }  // namespace gb

@@ -19,18 +19,19 @@ gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int gr
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
-template <bool kBF16, int kIn, bool kMc>
+template <bool kBF16, int kIn, int kShape>
 gb_status prepare_pair(DeviceState* dev) {
-  using C = gb::Cfg<true, kIn>;
+  using C = gb::Cfg<true, kIn, kShape>;
+  constexpr bool kMc = kShape == kShapeMc;
   constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
-  bool& attr = kMc ? dev->attr_mc[kBF16][kIn] : dev->attr_pair[kBF16][kIn];
+  bool& attr = dev->attr_pair[kBF16][kIn][pair_shape_index(kShape)];
   if (!attr) {
-    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kShape>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
     attr = true;
   }
-  int& clusters = kMc ? dev->mc_clusters : dev->pair_clusters;
+  int& clusters = dev->pair_clusters[pair_shape_index(kShape)];
   if (clusters == 0) {
     // a persistent grid must fit at once: ask how many clusters can be resident together
     cudaLaunchAttribute at[1];
@@ -45,7 +46,7 @@ gb_status prepare_pair(DeviceState* dev) {
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(kCl * (dev->sms / kCl), 1, 1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&n, gb::gemm_kernel<kBF16, true, kIn, kShape>, &cfg) != cudaSuccess ||
         n <= 0)
       n = dev->sms / kCl;
     clusters = std::min(n, dev->sms / kCl);
@@ -53,10 +54,10 @@ gb_status prepare_pair(DeviceState* dev) {
   return GB_OK;
 }
 
-template <bool kBF16, int kIn, bool kMc>
+template <bool kBF16, int kIn, int kShape>
 gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s) {
-  using C = gb::Cfg<true, kIn>;
-  constexpr int kCl = kMc ? 4 : 2;
+  using C = gb::Cfg<true, kIn, kShape>;
+  constexpr int kCl = kShape == kShapeMc ? 4 : 2;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCl;
@@ -69,7 +70,7 @@ gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(kCl * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kMc ? gb::kShapeMc : gb::kShapeStd>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kShape>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, p) != cudaSuccess)
     return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }

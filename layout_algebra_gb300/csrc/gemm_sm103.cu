@@ -133,6 +133,7 @@ std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
 int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast;
+                           // 5: CTA pair with 224-column tiles;
                            // 4: single CTA with narrow tiles
 int g_force_schedule = 0;  // 0: stream-K when a workspace is given and tiles leave a ragged
                            // last wave; 1: data-parallel only; 2: stream-K whenever possible
@@ -141,8 +142,11 @@ constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
 constexpr int kVariantPairMc = 3;   // clusters of two pairs sharing B tiles by multicast
 constexpr int kVariantNarrow = 4;   // single CTA, 128 x 64 tiles (few output columns)
+constexpr int kVariantPair224 = 5;  // CTA pair, 256 x 224 tiles (K-major B, 16-bit or FP8 inputs)
 
-bool is_pair(int variant) { return variant == kVariantPair || variant == kVariantPairMc; }
+bool is_pair(int variant) {
+  return variant == kVariantPair || variant == kVariantPairMc || variant == kVariantPair224;
+}
 
 using gb::DeviceState;
 using gb::Maps;
@@ -190,12 +194,12 @@ InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false
 // Tile width and the B rows one copy stages per CTA, per variant and input kind.
 int64_t tile_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
-  if (in.mx) return gb::kMxTileN;
+  if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
   return is_pair(variant) ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
 }
 int64_t mma_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
-  if (in.mx) return gb::kMxTileN;
+  if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
   return is_pair(variant) ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
 }
 
@@ -263,7 +267,18 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
 // Kernel for a problem: a forced variant, else narrow tiles when the output has at most 64
 // columns, the CTA pair when it has more than 128 rows, the single CTA otherwise.  Block-
 // scaled inputs have no multicast or narrow form and take the pair or the single CTA.
-int choose_variant(int64_t M, int64_t N, const InType& in) {
+// Tile width of a CTA pair ("CUTLASS, in depth", "Worked example: tile choice and wave
+// quantisation"): a persistent grid of G pairs runs ceil(tiles / G) waves of tiles whose time
+// is proportional to the tile width, so the 224-column tile is taken when its waves cost
+// less than the 256-column tile's (for 4096^3 on 76 pairs: 4 waves of 224 against 4 of 256).
+bool prefer_pair224(int64_t M, int64_t N, int pairs) {
+  if (pairs <= 0) return false;
+  const int64_t m_tiles = (M + 255) / 256;
+  auto cost = [&](int64_t w) { return (m_tiles * ((N + w - 1) / w) + pairs - 1) / pairs * w; };
+  return cost(gb::kMxTileN) < cost(256);
+}
+
+int choose_variant(int64_t M, int64_t N, const InType& in, int majorB, int sms) {
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -274,10 +289,14 @@ int choose_variant(int64_t M, int64_t N, const InType& in) {
     v = forced;
   else if (N <= gb::kNarrowTileN)
     v = kVariantNarrow;
+  else if (M <= gb::Cfg<false>::kTileM)
+    v = kVariantSingle;
   else
-    v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+    v = (!in.mx && majorB == GB_K_MAJOR && prefer_pair224(M, N, sms / 2)) ? kVariantPair224 : kVariantPair;
   if (in.mx && v == kVariantPairMc) v = kVariantPair;
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+  // 224-column tiles stage 112 B rows per CTA: K-major B only (an MN-major box is 64 wide)
+  if (v == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) v = kVariantPair;
   return v;
 }
 
@@ -291,6 +310,7 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   const bool pair = is_pair(variant);
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
   if (in.mx && (variant == kVariantPairMc || variant == kVariantNarrow)) return GB_ERR_INVALID_ARG;
+  if (variant == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) return GB_ERR_INVALID_ARG;
   const int64_t tile_n = tile_n_of(variant, in);
   // B rows one copy stages: one CTA's share of one MMA's columns; with multicast each CTA
   // copies a quarter of the pair's 256
@@ -440,6 +460,8 @@ bool epi_tma_fits(int variant, int kind) {
     return kind == kIn8 ? Cfg<false, kIn8, kShapeNarrow>::kEpiTma : Cfg<false, kIn16, kShapeNarrow>::kEpiTma;
   if (variant == kVariantPairMc)
     return kind == kIn8 ? Cfg<true, kIn8, kShapeMc>::kEpiTma : Cfg<true, kIn16, kShapeMc>::kEpiTma;
+  if (variant == kVariantPair224)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kEpiTma : Cfg<true, kIn16, kShapeN224>::kEpiTma;
   if (is_pair(variant))
     return kind == kInMx ? Cfg<true, kInMx>::kEpiTma
                          : (kind == kIn8 ? Cfg<true, kIn8>::kEpiTma : Cfg<true, kIn16>::kEpiTma);
@@ -504,17 +526,21 @@ void fill_params(const DeviceState* dev, const gb_gemm_plan& pl, int64_t M, int6
 }
 
 
-// Dispatch on the output type, the input kind and the two pair kernels (the multicast
-// pair takes 16-bit and FP8 inputs).
+// Dispatch on the output type, the input kind and the pair kernels (the multicast pair and the
+// 224-column pair take 16-bit and FP8 inputs).
 template <bool kBF16>
-gb_status prepare_pair_any(int kin, bool mc, DeviceState* dev) {
-  if (mc) return kin == gb::kIn8 ? prepare_pair<kBF16, gb::kIn8, true>(dev) : prepare_pair<kBF16, gb::kIn16, true>(dev);
-  if (kin == gb::kInMx) return prepare_pair<kBF16, gb::kInMx, false>(dev);
-  return kin == gb::kIn8 ? prepare_pair<kBF16, gb::kIn8, false>(dev) : prepare_pair<kBF16, gb::kIn16, false>(dev);
+gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
+  using namespace gb;
+  if (shape == kShapeMc)
+    return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeMc>(dev) : prepare_pair<kBF16, kIn16, kShapeMc>(dev);
+  if (shape == kShapeN224)
+    return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeN224>(dev) : prepare_pair<kBF16, kIn16, kShapeN224>(dev);
+  if (kin == kInMx) return prepare_pair<kBF16, kInMx, kShapeStd>(dev);
+  return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeStd>(dev) : prepare_pair<kBF16, kIn16, kShapeStd>(dev);
 }
 
 template <bool kBF16>
-gb_status launch_any(bool pair, int kin, bool mc, bool narrow, DeviceState* dev, const Maps& m, const Params& p,
+gb_status launch_any(bool pair, int kin, int shape, bool narrow, DeviceState* dev, const Maps& m, const Params& p,
                      int G, cudaStream_t s) {
   if (!pair) {
     if (narrow)
@@ -524,11 +550,15 @@ gb_status launch_any(bool pair, int kin, bool mc, bool narrow, DeviceState* dev,
     return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeStd>(dev, m, p, G, s)
                            : launch_single<kBF16, gb::kIn16, gb::kShapeStd>(dev, m, p, G, s);
   }
-  if (mc) return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, true>(m, p, G, s)
-                                 : launch_pair<kBF16, gb::kIn16, true>(m, p, G, s);
-  if (kin == gb::kInMx) return launch_pair<kBF16, gb::kInMx, false>(m, p, G, s);
-  return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, false>(m, p, G, s)
-                         : launch_pair<kBF16, gb::kIn16, false>(m, p, G, s);
+  if (shape == gb::kShapeMc)
+    return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeMc>(m, p, G, s)
+                           : launch_pair<kBF16, gb::kIn16, gb::kShapeMc>(m, p, G, s);
+  if (shape == gb::kShapeN224)
+    return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeN224>(m, p, G, s)
+                           : launch_pair<kBF16, gb::kIn16, gb::kShapeN224>(m, p, G, s);
+  if (kin == gb::kInMx) return launch_pair<kBF16, gb::kInMx, gb::kShapeStd>(m, p, G, s);
+  return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeStd>(m, p, G, s)
+                         : launch_pair<kBF16, gb::kIn16, gb::kShapeStd>(m, p, G, s);
 }
 
 // Workspace layout: one 32-bit flag per CTA (padded to 256 B), then one 128 x 256 fp32
@@ -591,7 +621,6 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   // dtype names the 16-bit type of C, D and the bias; the inputs share it unless in_f8 names
   // 8-bit input formats (with packed scale factors sfa / sfb when block-scaled)
   const InType in = in_f8 ? *in_f8 : in16(dtype);
-  const int variant = choose_variant(M, N, in);
   gb_status st = validate_sizes(M, N, K, lda, majorA, ldb, majorB, in.bytes);
   if (st != GB_OK) return st;
   if (dtype != GB_F16 && dtype != GB_BF16) return GB_ERR_INVALID_ARG;
@@ -618,6 +647,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
+  const int variant = choose_variant(M, N, in, majorB, dev->sms);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
@@ -640,7 +670,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       // of 64): fewer, larger copies keep the per-SM copy rate up (each copy costs a fixed
       // overhead).  Other operands use two-dimensional copies per k-block.
       const int64_t depth = gb::Cfg<true>::kKB;
-      const bool stage_boxes = pl.variant == kVariantPair && gb::Cfg<true>::kNSub == 1 && depth > 1 &&
+      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224) &&
+                               gb::Cfg<true>::kNSub == 1 && gb::Cfg<true, gb::kIn16, gb::kShapeN224>::kKB == depth && depth > 1 &&
                                K % in.bk() == 0;
       if (stage_boxes && majorA == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, depth, dtype, in.f8)) != GB_OK)
@@ -702,13 +733,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   const bool pair = is_pair(pl.variant);
   const bool mc = pl.variant == kVariantPairMc;
+  const int shape = mc ? gb::kShapeMc : (pl.variant == kVariantPair224 ? gb::kShapeN224 : gb::kShapeStd);
   const bool bf = dtype == GB_BF16;
   if (pair) {
-    st = bf ? prepare_pair_any<true>(in.kind(), mc, dev) : prepare_pair_any<false>(in.kind(), mc, dev);
+    st = bf ? prepare_pair_any<true>(in.kind(), shape, dev) : prepare_pair_any<false>(in.kind(), shape, dev);
     if (st != GB_OK) return st;
   }
   // CTAs (clusters) that can run at once
-  const int slots = mc ? dev->mc_clusters : pair ? dev->pair_clusters : dev->sms;
+  const int slots = pair ? dev->pair_clusters[gb::pair_shape_index(shape)] : dev->sms;
 
   // schedule: stream-K needs a workspace and some K; by default it is used when the tiles
   // leave a ragged last wave (or fewer tiles than CTAs)
@@ -737,8 +769,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool narrow = pl.variant == kVariantNarrow;
-  return bf ? launch_any<true>(pair, in.kind(), mc, narrow, dev, maps, p, G, s)
-            : launch_any<false>(pair, in.kind(), mc, narrow, dev, maps, p, G, s);
+  return bf ? launch_any<true>(pair, in.kind(), shape, narrow, dev, maps, p, G, s)
+            : launch_any<false>(pair, in.kind(), shape, narrow, dev, maps, p, G, s);
 }
 
 }  // namespace
@@ -873,7 +905,15 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
                             int majorB, gb_gemm_plan* plan) {
   if (!plan) return GB_ERR_INVALID_ARG;
   if (M < 0) return GB_ERR_INVALID_ARG;
-  return make_plan(dtype, choose_variant(M, N, in16(dtype)), M, N, K, lda, majorA, ldb, majorB, plan);
+  // the variant is chosen for this device's SM count; without a device (a plan made on a host
+  // with no GPU), for 152 SMs
+  int sms = 152, device = 0;
+  if (cudaGetDevice(&device) == cudaSuccess) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && n > 0) sms = n;
+  }
+  cudaGetLastError();
+  return make_plan(dtype, choose_variant(M, N, in16(dtype), majorB, sms), M, N, K, lda, majorA, ldb, majorB, plan);
 }
 
 gb_status gb_set_wait_timeout_ns(uint64_t ns) {

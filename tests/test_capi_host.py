@@ -37,7 +37,7 @@ def test_status_strings():
     assert "10.3" in G.status_string(3)
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["single", "pair", "pair_mc"])
+@pytest.fixture(params=[1, 2, 3, 5], ids=["single", "pair", "pair_mc", "pair224"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param
@@ -55,11 +55,15 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     lda = K if majors[0] == "K" else M
     ldb = K if majors[1] == "K" else N
     p = G.plan("f16", M, N, K, lda, majors[0], ldb, majors[1])
-    grid = grid1 if variant == 1 else grid2
-    tile_m = 128 if variant == 1 else 256
-    tile_n = 256                                 # every variant: 256-column tiles
-    rows_b = {1: 256, 2: 128, 3: 64}[variant]    # B rows one copy box stages per CTA
-    assert p["variant"] == variant and p["tile_m"] == tile_m and p["tile_n"] == tile_n
+    # 224-column tiles need K-major B: a forced 224 variant with MN-major B runs as the pair
+    want = 2 if (variant == 5 and majors[1] == "MN") else variant
+    grid = grid1 if want == 1 else grid2
+    tile_m = 128 if want == 1 else 256
+    tile_n = 224 if want == 5 else 256
+    if want == 5:
+        grid = (grid[0], -(-N // 224), grid[2])
+    rows_b = {1: 256, 2: 128, 3: 64, 5: 112}[want]    # B rows one copy box stages per CTA
+    assert p["variant"] == want and p["tile_m"] == tile_m and p["tile_n"] == tile_n
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
     # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
     for i, (ext, want) in enumerate(zip(grid[:2], [tile_m * N, tile_n])):
@@ -79,21 +83,30 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     d = p["instr_desc"]
     assert (d >> 4) & 3 == 1 and (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0
     assert (d >> 15) & 1 == (majors[0] == "MN") and (d >> 16) & 1 == (majors[1] == "MN")
-    assert (d >> 17) & 63 == 256 >> 3 and (d >> 24) & 31 == tile_m >> 4
+    assert (d >> 17) & 63 == tile_n >> 3 and (d >> 24) & 31 == tile_m >> 4
     assert p["vector_epilogue"] == 1
 
 
 def test_variant_choice_by_shape():
+    """Default choice (a plan made without a GPU assumes 152 SMs, 76 CTA pairs)."""
     G.set_kernel_variant(0)
     assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 1
-    assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 2
+    # CTA pairs: 224 columns when ceil(tiles / 76) x width is smaller than with 256
+    assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 5      # 3 x 224 vs 2 x 256 tiles, 1 wave
+    assert G.plan("f16", 19456, 256, 64, 64, "K", 64, "K")["variant"] == 2    # 2 waves of 224 vs 1 of 256
+    p = G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "K")                 # 4 waves of 224 vs 4 of 256
+    assert p["variant"] == 5 and (p["m_tiles"], p["n_tiles"], p["tile_n"]) == (16, 19, 224)
+    assert p["b_box"] == [64, 112] and (p["instr_desc"] >> 17) & 63 == 224 >> 3
+    assert G.plan("bf16", 8192, 8192, 8192, 8192, "K", 8192, "K")["variant"] == 2   # 16 x 224 = 14 x 256
+    assert G.plan("f16", 5000, 3000, 4104, 4104, "K", 4104, "K")["variant"] == 5
+    assert G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "MN")["variant"] == 2   # MN-major B
     # at most 64 output columns: narrow 128 x 64 tiles
     p = G.plan("f16", 4096, 16, 4096, 4096, "K", 4096, "K")
     assert p["variant"] == 4 and (p["tile_m"], p["tile_n"]) == (128, 64)
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 1, 64)
     assert p["b_box"] == [64, 64] and (p["instr_desc"] >> 17) & 63 == 64 >> 3
     with pytest.raises(G.GemmError):
-        G.set_kernel_variant(5)
+        G.set_kernel_variant(6)
 
 
 def test_plan_bf16_descriptor_and_scalar_epilogue(variant):

@@ -21,9 +21,9 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
-@pytest.fixture
-def pair():
-    G.set_kernel_variant(2)
+@pytest.fixture(params=[2, 5], ids=["pair", "pair224"])
+def pair(request):
+    G.set_kernel_variant(request.param)
     yield
     G.set_kernel_variant(0)
 
