@@ -142,7 +142,8 @@ struct Params {
   int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
   uint32_t* status;           // device status word: first failing wait, 0 if none
   // bit 0 (A), bit 1 (B): one copy moves all kKB k-blocks of the operand's stage (CTA pair,
-  // K a multiple of the k-block).  K-major: a three-dimensional map (k-block elements, rows,
+  // K a multiple of the k-block); bit 2 (B, multicast pairs): pair p copies k-block p of each
+  // stage into both pairs.  K-major: a three-dimensional map (k-block elements, rows,
   // k-blocks); MN-major (rows a multiple of 64): four-dimensional (64 MN elements, K rows of
   // a k-block, 64-wide MN chunks, k-blocks).  Otherwise one two-dimensional copy per k-block.
   int32_t kb_boxes;
@@ -402,8 +403,11 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
   // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
   const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
-  // stage-deep copies: CTA pairs without multicast, one 256-column MMA per k-block
-  constexpr bool kStageBoxes = kPair && !kMc && C::kNSub == 1 && C::kKB > 1;
+  // stage-deep copies: CTA pairs, one MMA per k-block along N.  With B multicast (two pairs
+  // of a cluster on the same B columns) the stage's two k-blocks of B are split between the
+  // pairs instead: pair pidx copies k-block pidx (this CTA's 128 rows) into both pairs.
+  constexpr bool kStageBoxes = kPair && C::kNSub == 1 && C::kKB > 1;
+  static_assert(!kMc || C::kKB == 2, "multicast: one k-block of B per pair");
   int stage = 0;
   uint32_t phase = 0;
   int64_t gkb = 0;
@@ -430,14 +434,15 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         // the last stage of a tile may hold fewer k-blocks: copy and count only those (a
         // stage-deep copy always lands whole, its k-blocks past K zero-filled)
         const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
-        bool a3 = false, b3 = false;
+        bool a3 = false, b3 = false, bsplit = false;
         if constexpr (kStageBoxes) {
           a3 = (p.kb_boxes & 1) != 0;
-          b3 = (p.kb_boxes & 2) != 0;
+          b3 = !kMc && (p.kb_boxes & 2) != 0;
+          bsplit = kMc && (p.kb_boxes & 4) != 0;
         }
         if (!kPair || prank == 0) {
           // scale factors always arrive for the whole stage (one copy per operand)
-          const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * (b3 ? C::kKB : nkb) +
+          const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * ((b3 || bsplit) ? C::kKB : nkb) +
                                C::kSfBytes * C::kKB) * (kPair ? 2u : 1u);
           mbar_arrive_expect_tx(full, tx);
         }
@@ -454,6 +459,14 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
             else
               tma_load_4d_pair(sa + C::kAStage, tmB, full_tgt, 0, 0, b_row0 / kSwz, sb * C::kKB);
           }
+          if constexpr (kMc) {
+            if (bsplit) {
+              // past K (a last stage of one k-block) the copy zero-fills; both halves always land
+              const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
+              tma_load_2d_pair_mc(sa + C::kAStage + pidx * C::kBHalf, tmB, full_tgt,
+                                  (sb * C::kKB + static_cast<int32_t>(pidx)) * p.bk_elems, b_row0, mask);
+            }
+          }
         }
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
@@ -463,6 +476,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
           if constexpr (kMc) {
             // both pairs need the same B rows: this CTA copies its pair's quarter of them
             // (64 rows) into itself and the same-rank CTA of the other pair
+            if (bsplit) continue;
             const uint32_t dst = sa + C::kAStage + h * C::kBHalf + pidx * kChunkBytes;
             const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
             if (p.majorB == 0)

@@ -670,7 +670,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       // of 64): fewer, larger copies keep the per-SM copy rate up (each copy costs a fixed
       // overhead).  Other operands use two-dimensional copies per k-block.
       const int64_t depth = gb::Cfg<true>::kKB;
-      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224) &&
+      const bool mc_b = pl.variant == kVariantPairMc;
+      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224 || mc_b) &&
                                gb::Cfg<true>::kNSub == 1 && gb::Cfg<true, gb::kIn16, gb::kShapeN224>::kKB == depth && depth > 1 &&
                                K % in.bk() == 0;
       if (stage_boxes && majorA == GB_K_MAJOR) {
@@ -685,7 +686,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       } else if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) {
         return st;
       }
-      if (stage_boxes && majorB == GB_K_MAJOR) {
+      if (mc_b && stage_boxes && majorB == GB_K_MAJOR) {
+        // multicast pairs split a stage's two k-blocks of B: one 2-D copy of a CTA's 128 rows
+        const int64_t box[2] = {pl.b_box[0], gb::Cfg<true>::kRowsBSub};
+        if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, box, dtype, in.f8)) != GB_OK) return st;
+        maps.kb_boxes |= 4;
+      } else if (mc_b) {
+        if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
+      } else if (stage_boxes && majorB == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, depth, dtype, in.f8)) != GB_OK)
           return st;
         maps.kb_boxes |= 2;
