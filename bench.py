@@ -490,7 +490,7 @@ def run_gb300(args):
                     "algorithmic_flops_per_launch": p.flops,
                     "algorithmic_bytes_per_launch": p.algorithmic_bytes}
     else:
-        # a run that reached the power cap is a long-step measurement: judge it against the
+        # a run that reached the power cap is a long-step measurement: compare it with the
         # sustained peak; otherwise against the burst peak of a kernel timed alone
         capped = "sw_power_cap" in (clocks.get("reasons") or [])
         peak, which = (sustained, "sustained") if capped else (burst, "burst")
