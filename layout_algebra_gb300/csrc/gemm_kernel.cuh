@@ -147,6 +147,10 @@ struct Params {
   // k-blocks); MN-major (rows a multiple of 64): four-dimensional (64 MN elements, K rows of
   // a k-block, 64-wide MN chunks, k-blocks).  Otherwise one two-dimensional copy per k-block.
   int32_t kb_boxes;
+  // k-blocks the stage-deep maps cover (K / bk rounded down): a stage reaching past them
+  // (the tail of a K that is not a multiple of the k-block) is copied per k-block through
+  // the two-dimensional tail maps instead; == k_blocks when K is a multiple
+  int32_t kb_full;
   // 1: the epilogue stages each 32 x 32 run of D in shared memory and writes it with a
   // tensor copy (tmD), and reads C the same way (tmC); 16-bit D, row-major, N % 8 == 0
   int32_t epi_tma;
@@ -396,8 +400,8 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int major, int k
 
 template <bool kPair, int kIn, int kShape>
 __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, const void* tmSFA,
-                             const void* tmSFB, uint8_t* smem, Ctl* ctl, uint32_t rank, uint32_t cluster,
-                             uint32_t nclusters) {
+                             const void* tmSFB, const void* tmAt, const void* tmBt, uint8_t* smem, Ctl* ctl,
+                             uint32_t rank, uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair, kIn, kShape>;
   constexpr bool kMc = kShape == kShapeMc;
   static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
@@ -435,10 +439,17 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         // stage-deep copy always lands whole, its k-blocks past K zero-filled)
         const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
         bool a3 = false, b3 = false, bsplit = false;
+        // operands with stage-deep maps copy a stage reaching past the maps' k-blocks (a K
+        // tail) per k-block through their two-dimensional tail maps
+        const void* tmA1 = tmA;
+        const void* tmB1 = tmB;
         if constexpr (kStageBoxes) {
-          a3 = (p.kb_boxes & 1) != 0;
-          b3 = !kMc && (p.kb_boxes & 2) != 0;
+          const bool whole = sb * C::kKB + C::kKB <= p.kb_full || p.kb_full == p.k_blocks;
+          a3 = whole && (p.kb_boxes & 1) != 0;
+          b3 = whole && !kMc && (p.kb_boxes & 2) != 0;
           bsplit = kMc && (p.kb_boxes & 4) != 0;
+          if (p.kb_boxes & 1) tmA1 = tmAt;
+          if (!kMc && (p.kb_boxes & 2)) tmB1 = tmBt;
         }
         if (!kPair || prank == 0) {
           // scale factors always arrive for the whole stage (one copy per operand)
@@ -471,7 +482,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
           if (!a3)
-            issue_operand<kPair>(p.majorA, tmA, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
+            issue_operand<kPair>(p.majorA, tmA1, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
                                  p.bk_elems);
           if constexpr (kMc) {
             // both pairs need the same B rows: this CTA copies its pair's quarter of them
@@ -487,7 +498,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
             // per MMA along N: this CTA's rows of that MMA's 256 tile columns
 #pragma unroll
             for (int j = 0; j < C::kNSub; ++j)
-              issue_operand<kPair>(p.majorB, tmB, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
+              issue_operand<kPair>(p.majorB, tmB1, sa + C::kAStage + h * C::kBHalf + j * C::kBSub,
                                    full_tgt, b_row0 + j * C::kMmaN, C::kRowsBSub, kb, p.bk_elems);
           }
         }
@@ -1092,6 +1103,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt,
                 const Params p) {
   using C = Cfg<kPair, kIn, kShape>;
   constexpr bool kMc = kShape == kShapeMc;
@@ -1155,7 +1167,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0)
-      run_producer<kPair, kIn, kShape>(p, &tmA, &tmB, &tmSFA, &tmSFB, smem, ctl, rank, cluster, nclusters);
+      run_producer<kPair, kIn, kShape>(p, &tmA, &tmB, &tmSFA, &tmSFB, &tmAt, &tmBt, smem, ctl, rank, cluster,
+                                       nclusters);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) run_mma<kPair, kIn, kShape>(p, smem, ctl, tmem_base, rank, cluster, nclusters);
@@ -1197,6 +1210,8 @@ struct DeviceState {
 struct Maps {
   CUtensorMap a, b, sfa, sfb;
   CUtensorMap c, d;   // tile-store epilogue: C and D as (N, M) tensors, 32 x 32 boxes
+  CUtensorMap at, bt; // two-dimensional maps of A, B for the K tail when a, b are stage-deep
+  int32_t kb_full;    // Params::kb_full
   int32_t epi_tma;    // Params::epi_tma: c (when C is read) and d are encoded
   int32_t kb_boxes;   // Params::kb_boxes: which of a, b are stage-deep (three-dimensional) maps
 };

@@ -15,7 +15,7 @@ gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int gr
       return GB_ERR_LAUNCH;
     attr = true;
   }
-  gb::gemm_kernel<kBF16, false, kIn, kShape><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, m.c, m.d, p);
+  gb::gemm_kernel<kBF16, false, kIn, kShape><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, m.c, m.d, m.at, m.bt, p);
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
@@ -70,7 +70,7 @@ gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(kCl * clusters, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kShape>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kShape>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, m.at, m.bt, p) != cudaSuccess)
     return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }

@@ -388,14 +388,15 @@ gb_status encode_map(CUtensorMap* map, const void* base, const int64_t dim[2], i
 // Stage-deep map of a K-major operand described by the two-dimensional (K, rows) geometry of
 // plan_operand: the K mode divided by the k-block, (K):(1) -> (bk, K/bk):(1, bk), as in the
 // zipped_divide of the operand by (rows, bk), gives copy dimensions (bk, rows, k-blocks) with
-// byte strides (row_bytes, bk * bytes); the box takes `depth` k-blocks at once.  Used only
-// when K is a multiple of bk, so no row reads past its own K elements.
+// byte strides (row_bytes, bk * bytes); the box takes `depth` k-blocks at once.  The map
+// covers the K / bk whole k-blocks only (rounded down), so no row reads past its own K
+// elements; a tail k-block goes through the two-dimensional map.
 gb_status encode_map_kblocks(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
                              const int64_t box[2], int64_t depth, int dtype, bool f8) {
   auto fn = encode_fn();
   if (!fn) return GB_ERR_LAUNCH;
   const int64_t bk = box[0], bytes = f8 ? 1 : 2;
-  if (dim[0] % bk != 0) return GB_ERR_INVALID_ARG;
+  if (dim[0] < bk) return GB_ERR_INVALID_ARG;
   cuuint64_t gdim[3] = {static_cast<cuuint64_t>(bk), static_cast<cuuint64_t>(dim[1]),
                         static_cast<cuuint64_t>(dim[0] / bk)};
   cuuint64_t gstride[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(bk * bytes)};
@@ -415,14 +416,15 @@ gb_status encode_map_kblocks(CUtensorMap* map, const void* base, const int64_t d
 // span) and the K mode by the k-block gives (64, chunks):(1, 64) and (bk, K/bk):(ld, bk ld);
 // ordered as the stage holds them, the copy dimensions are (64 MN elements, bk K rows,
 // MN chunks, k-blocks) with byte strides (row_bytes, 128, bk row_bytes).  The box takes
-// box_rows / 64 chunks and `depth` k-blocks.  Used only when rows and K are multiples of 64
-// and bk, so no copy reads an element outside the operand.
+// box_rows / 64 chunks and `depth` k-blocks.  Used only when rows are a multiple of 64; the
+// map covers the K / bk whole k-blocks (rounded down), so no copy reads an element outside the
+// operand, and a tail k-block goes through the two-dimensional map.
 gb_status encode_map_mn_kblocks(CUtensorMap* map, const void* base, const int64_t dim[2], int64_t row_bytes,
                                 int64_t box_rows, int64_t bk, int64_t depth, int dtype) {
   auto fn = encode_fn();
   if (!fn) return GB_ERR_LAUNCH;
   const int64_t span = gb::kSwz;
-  if (dim[0] % span != 0 || dim[1] % bk != 0 || box_rows % span != 0) return GB_ERR_INVALID_ARG;
+  if (dim[0] % span != 0 || dim[1] < bk || box_rows % span != 0) return GB_ERR_INVALID_ARG;
   cuuint64_t gdim[4] = {static_cast<cuuint64_t>(span), static_cast<cuuint64_t>(bk),
                         static_cast<cuuint64_t>(dim[0] / span), static_cast<cuuint64_t>(dim[1] / bk)};
   cuuint64_t gstride[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(span * 2),
@@ -671,9 +673,12 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       // overhead).  Other operands use two-dimensional copies per k-block.
       const int64_t depth = gb::Cfg<true>::kKB;
       const bool mc_b = pl.variant == kVariantPairMc;
+      // whole k-blocks the stage-deep maps cover; a K tail is copied per k-block (tail maps)
+      const int64_t kb_full = K / in.bk();
       const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224 || mc_b) &&
                                gb::Cfg<true>::kNSub == 1 && gb::Cfg<true, gb::kIn16, gb::kShapeN224>::kKB == depth && depth > 1 &&
-                               K % in.bk() == 0;
+                               kb_full >= 1;
+      maps.kb_full = static_cast<int32_t>(stage_boxes ? kb_full : pl.k_blocks);
       if (stage_boxes && majorA == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, depth, dtype, in.f8)) != GB_OK)
           return st;
@@ -705,6 +710,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       } else if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) {
         return st;
       }
+      if (maps.kb_full < pl.k_blocks) {
+        if ((maps.kb_boxes & 1) &&
+            (st = encode_map(&maps.at, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK)
+          return st;
+        if ((maps.kb_boxes & 2) &&
+            (st = encode_map(&maps.bt, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK)
+          return st;
+      }
       if (in.mx) {
         // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
         // k-block), two atoms of B per (224 columns, k-block); one copy takes a stage's kKB
@@ -729,6 +742,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   fill_params(dev, pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
   p.bk_elems = in.bk();
   p.kb_boxes = maps.kb_boxes;
+  p.kb_full = K > 0 ? maps.kb_full : 0;
   p.epi_tma = maps.epi_tma;
   if (epi) {
     p.fused = 1;

@@ -44,7 +44,9 @@ def ref16(p, data):
                   0 if p.majorB == "K" else 1, p.beta, C, p.N, O.dtype_code(p.dtype))
 
 
-@pytest.mark.parametrize("K", [64, 192, 320, 1024])
+# K multiples of the k-block (64) with even and odd k-block counts, and K tails (100, 200,
+# 1000: the stage reaching past K / 64 whole k-blocks goes through the two-dimensional maps)
+@pytest.mark.parametrize("K", [64, 100, 192, 200, 320, 1000, 1024])
 @pytest.mark.parametrize("majors", [("K", "K"), ("K", "MN"), ("MN", "K"), ("MN", "MN")])
 @pytest.mark.parametrize("MN", [(300, 520), (320, 576)], ids=["rows_ragged", "rows_x64"])
 def test_integer_exact_k_blocks(pair, K, majors, MN):
@@ -52,8 +54,9 @@ def test_integer_exact_k_blocks(pair, K, majors, MN):
     # 64); (320, 576): they take the four-dimensional stage copies, with whole 64-row chunks
     # past M and N zero-filled in the last tiles
     M, N = MN
-    lda = K + 16 if majors[0] == "K" else -(-M // 8) * 8 + 8   # multiples of 8 elements
-    ldb = K + 8 if majors[1] == "K" else N
+    # leading dimensions: multiples of 8 elements, padded past K / M
+    lda = -(-K // 8) * 8 + 16 if majors[0] == "K" else -(-M // 8) * 8 + 8
+    ldb = -(-K // 8) * 8 + 8 if majors[1] == "K" else N
     p = W.Problem("sd", M, N, K, "f16", majorA=majors[0], majorB=majors[1], has_c=True,
                   alpha=1.0, beta=1.0, dist="int2", c_dist="int2", seed=K + 7, lda=lda, ldb=ldb)
     data = W.make(p)
@@ -76,9 +79,10 @@ def test_random_odd_k_blocks_default_variant(dtype):
     assert np.all(np.abs(d - ref) <= bound)
 
 
-@pytest.mark.parametrize("K", [128, 384, 640])
+@pytest.mark.parametrize("K", [128, 200, 384, 640, 1000])
 def test_fp8_integer_exact_k_blocks(pair, K):
-    p = W.Problem("sd8", 320, 272, K, "f16", dist="int2", seed=K, a_fmt="e4m3", b_fmt="e5m2")
+    ld = -(-K // 16) * 16   # FP8 rows: multiples of 16 bytes
+    p = W.Problem("sd8", 320, 272, K, "f16", dist="int2", seed=K, a_fmt="e4m3", b_fmt="e5m2", lda=ld, ldb=ld)
     data = W.make(p)
     D = G.gemm_fp8(data["A"].to(DEV), data["B"].to(DEV), p.M, p.N, p.K, lda=data["lda"],
                    ldb=data["ldb"], a_format=p.a_fmt, b_format=p.b_fmt, out_dtype=torch.float16)
