@@ -34,19 +34,20 @@ constexpr int kCtlBytes = 512;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
-// Two variants share all code:
-//  single (kPair = false): one CTA per tile, 128 x 256 tile, 4 stages of A 128x64 + B 256x64,
-//         two 256-column accumulators in TMEM (the epilogue of one tile overlaps the main
-//         loop of the next);
-//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x kPairTileN tile; the
-//         even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256) reading both CTAs'
-//         shared memory, and each CTA's TMEM holds its own 128 rows of the accumulator.
-//         Each CTA stages its 128 A rows and, per 256-column MMA, its 128 of the 256 B rows.
+// The kernel variants share all code:
+//  single (kPair = false): one CTA per 128 x 256 tile, 4 stages of A 128x64 + B 256x64, two
+//         256-column accumulators in TMEM (the epilogue of one tile overlaps the main loop of
+//         the next); narrow single-CTA tiles of 128 x 64 for outputs with few columns;
+//  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x 256 (or 256 x 224) tile;
+//         the even CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared
+//         memory, and each CTA's TMEM holds its own 128 rows of the accumulator.  Each CTA
+//         stages its 128 A rows and its half of the tile's B rows, two k-blocks per stage;
+//         in clusters of two pairs (multicast) the pairs share B.
 //         A 512-column tile (kPairTileN = 512) feeds two MMAs from one k-block of A; the
 //         accumulator then fills TMEM, the epilogue no longer overlaps the next tile, and
 //         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
-//         the copy side's time did not drop with the 25 % fewer bytes (it follows the count
-//         of pipeline stages), so 256-column tiles with the overlapped epilogue stay.
+//         the gain was eaten by the exposed epilogue, so 256-column tiles with the
+//         overlapped epilogue stay (kPairTileN is kept at 256).
 // Input kinds: 16-bit (fp16/bf16, kind::f16), FP8 (kind::f8f6f4) and block-scaled FP8
 // (kind::mxf8f6f4 with one E8M0 scale per 32 K elements of each row of A and column of B).
 enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };

@@ -1,4 +1,4 @@
-// Persistent tiled GEMM for sm_103a:  D = alpha * A * B + beta * C.
+// Persistent tiled GEMM for sm_103a:  D = alpha * A * B + beta * C — host side and C ABI.
 //
 // What the pages define ("CUTLASS, in depth" — "The problem CUTLASS solves", "Kernel
 // schedules", "Epilogue fusion"; "Layouts as Algebra" — "The kernel, in three lines"):
@@ -7,26 +7,27 @@
 // multiplies and releases them; after the last K step the epilogue applies alpha and
 // beta and stores D.  Persistent CTAs loop over tiles in a grouped raster order.
 //
-// How it maps onto sm_103a:
-//   warp 0, one lane   tensor copies (TMA) of A/B k-blocks into a 4-stage ring of
-//                      128-byte-swizzled shared memory, counted on mbarriers;
-//   warp 1, one lane   tcgen05.mma (128 x 256 x 16, fp32 accumulate) into one of two
-//                      Tensor Memory accumulators (2 x 256 columns); tcgen05.commit
-//                      frees a stage when its MMAs retire and hands a finished
-//                      accumulator to the epilogue;  warp 1 also owns the TMEM allocation;
-//   warps 2-5          epilogue: tcgen05.ld of their 32-lane quarter, alpha*acc + beta*C
-//                      in fp32, round to fp16/bf16, 16-byte stores, rows/columns past
-//                      M/N predicated off.  The second accumulator lets the epilogue of
-//                      tile i overlap the main loop of tile i+1.
-// Tile origins and in-tile offsets of C/D are the evaluation of
-// zipped_divide((M,N):(N,1), (128,256)); the copy geometry of A and B comes from the
-// same divide of their layouts (host side, layout.cpp).
+// How it maps onto sm_103a (device code in gemm_kernel.cuh):
+//   warp 0, one lane   tensor copies (TMA) of A/B into a ring of 128-byte-swizzled shared
+//                      memory stages (a CTA pair: 3 stages of two k-blocks, one copy per
+//                      operand per stage), counted on mbarriers;
+//   warp 1, one lane   tcgen05.mma (fp32 accumulate) into one of two Tensor Memory
+//                      accumulators; tcgen05.commit frees a stage when its MMAs retire and
+//                      hands a finished accumulator to the epilogue; warp 1 also owns TMEM;
+//   warps 2-5          epilogue: tcgen05.ld of their 32-lane quarter, alpha*acc + beta*C in
+//                      fp32 (and the fused nodes), rounded to fp16/bf16 and written through
+//                      shared-memory staging tiles by tensor copies clipped at M and N (C read
+//                      the same way), or with per-thread 16-byte stores (FP8 outputs, N % 8
+//                      != 0).  The second accumulator lets the epilogue of tile i overlap the
+//                      main loop of tile i+1.
+// This file: the layout-algebra planning of a call (tile grids, copy geometry, the C/D offset
+// map: zipped_divide((M,N):(N,1), (BM,BN)) and the divides of A and B, see layout.cpp), tensor
+// map encoding, the variant and schedule choice, the plan cache, and the C ABI.
 //
-// Every wait is bounded: past the limit the waiting thread records a code in the device status word,
-// raises an abort flag in shared memory, and all roles leave their loops; the copy
-// stage waits for its own copies in flight, the MMA stage for its own MMAs, and TMEM is
+// Every wait is bounded: past the limit the waiting thread records a code in the device
+// status word, raises an abort flag in shared memory, and all roles leave their loops; the
+// copy stage waits for its own copies in flight, the MMA stage for its own MMAs, and TMEM is
 // always released before the CTA exits.
-
 
 #include <cuda.h>
 #include <cuda_bf16.h>
