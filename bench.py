@@ -412,9 +412,12 @@ def run_gb300(args):
     total_ms = starts[0].elapsed_time(ends[-1])
     if graph is not None:
         kernel_ms = total_ms / args.steps
+        per_launch_ms = [kernel_ms]
     else:
         per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         kernel_ms = sum(per_launch_ms) / len(per_launch_ms)
+    launch_stats = {"kernel_ms_best": min(per_launch_ms),
+                    "kernel_ms_median": statistics.median(per_launch_ms)}
     elapsed_s, total_flops = aggregate(total_ms / 1e3, float(p.flops) * args.steps, world, dev)
     value = total_flops / elapsed_s / 1e12
     clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.05)
@@ -487,6 +490,7 @@ def run_gb300(args):
                     "traffic": traffic,
                     "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
                     "tflops": achieved, "kernel": "gb::gemm_kernel", "kernel_ms": kernel_ms,
+                    **launch_stats,
                     "algorithmic_flops_per_launch": p.flops,
                     "algorithmic_bytes_per_launch": p.algorithmic_bytes}
     else:
@@ -505,6 +509,7 @@ def run_gb300(args):
                     "frac_of_nominal": achieved / (2250.0 * ratio),
                     "frac_of_clock_peak": achieved / clock_peak, "clock_peak": clock_peak,
                     "kernel": "gb::gemm_kernel", "kernel_ms": kernel_ms,
+                    **launch_stats,
                     "algorithmic_flops_per_launch": p.flops,
                     "algorithmic_bytes_per_launch": p.algorithmic_bytes}
 

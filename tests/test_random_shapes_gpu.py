@@ -1,0 +1,63 @@
+"""GPU parity on seeded random problems through the default variant choice.
+
+Each case draws M, N, K (with tails against every tile size: 128/256 rows, 64/224/256
+columns, 64-element k-blocks), the majors, the 16-bit type, alpha and beta, then compares
+every output with the fp64 oracle under the acceptance bound.  Integer-valued cases (every
+fourth) must match bit for bit.  The default choice picks the single, narrow, pair or
+224-column pair kernel from the shape, so the cases also exercise that choice.
+"""
+import numpy as np
+import pytest
+import torch
+
+from layout_algebra_gb300 import binding as G
+from layout_algebra_gb300 import workloads as W
+from oracle import gemm_ref as O
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def draw(i):
+    rng = np.random.default_rng(1000 + i)
+    M = int(rng.choice([1, 7, 64, 127, 129, 200, 255, 257, 300, 513, 640, 1000]))
+    N = int(rng.choice([8, 13, 16, 40, 64, 72, 100, 200, 224, 256, 264, 448, 520, 696]))
+    K = int(rng.choice([8, 40, 64, 100, 128, 192, 200, 320, 1000]))
+    majors = (str(rng.choice(["K", "MN"])), str(rng.choice(["K", "MN"])))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    integer = i % 4 == 0
+    alpha = 1.0 if integer else float(rng.choice([1.0, 0.75, -1.25]))
+    beta = float(rng.choice([0.0, 1.0])) if integer else float(rng.choice([0.0, 0.5, -1.0]))
+    return M, N, K, majors, dtype, integer, alpha, beta
+
+
+@pytest.mark.parametrize("i", range(96))
+def test_random_problem(i):
+    M, N, K, majors, dtype, integer, alpha, beta = draw(i)
+    pad = lambda n: -(-n // 8) * 8
+    lda = pad(K) + (8 if i % 3 == 0 else 0) if majors[0] == "K" else pad(M)
+    ldb = pad(K) if majors[1] == "K" else pad(N) + (8 if i % 5 == 0 else 0)
+    dist = "int2" if integer else "normal"
+    p = W.Problem("rnd%d" % i, M, N, K, dtype, majorA=majors[0], majorB=majors[1], has_c=beta != 0.0,
+                  alpha=alpha, beta=beta, dist=dist, c_dist=dist, seed=77 + i, lda=lda, ldb=ldb)
+    data = W.make(p)
+    C = data["C"].to(DEV) if data["C"] is not None else None
+    D = G.gemm(data["A"].to(DEV), data["B"].to(DEV), M, N, K, lda=lda, ldb=ldb, majorA=majors[0],
+               majorB=majors[1], alpha=alpha, beta=beta, C=C)
+    st, detail = G.last_device_status()
+    assert st == 0, "device status %d detail %#x" % (st, detail)
+    code = O.dtype_code(dtype)
+    ref, sab = O.gemm(M, N, K, alpha, W.bits(data["A"]), lda, 0 if majors[0] == "K" else 1,
+                      W.bits(data["B"]), ldb, 0 if majors[1] == "K" else 1, beta,
+                      W.bits(data["C"]) if data["C"] is not None else None, N, code)
+    d = O.decode(code, W.bits(D.cpu()))[: M * N].reshape(M, N)
+    if integer:
+        want = O.decode(code, O.round_to(code, ref)).reshape(M, N)
+        assert np.array_equal(d, want)
+        return
+    c = O.decode(code, W.bits(data["C"])).reshape(M, N) if data["C"] is not None else None
+    bound = O.bound(code, alpha, beta, ref.reshape(M, N), sab.reshape(M, N), c)
+    assert np.all(np.isfinite(d))
+    assert np.all(np.abs(d - ref.reshape(M, N)) <= bound), "worst %.3g of the bound" % float(
+        np.max(np.abs(d - ref.reshape(M, N)) / bound))
