@@ -61,3 +61,39 @@ def test_random_problem(i):
     assert np.all(np.isfinite(d))
     assert np.all(np.abs(d - ref.reshape(M, N)) <= bound), "worst %.3g of the bound" % float(
         np.max(np.abs(d - ref.reshape(M, N)) / bound))
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_random_fp8_problem(i):
+    """FP8 inputs (K-major, rows of a multiple of 16 bytes) with 16-bit C and D."""
+    rng = np.random.default_rng(5000 + i)
+    M = int(rng.choice([1, 100, 128, 129, 256, 300, 513, 700]))
+    N = int(rng.choice([16, 24, 64, 72, 200, 224, 256, 264, 520]))
+    K = int(rng.choice([16, 32, 100, 128, 200, 256, 384, 1000]))
+    fa, fb = str(rng.choice(["e4m3", "e5m2"])), str(rng.choice(["e4m3", "e5m2"]))
+    dtype = str(rng.choice(["f16", "bf16"]))
+    integer = i % 4 == 0
+    alpha = 1.0 if integer else float(rng.choice([1.0, 0.5]))
+    beta = float(rng.choice([0.0, 1.0])) if integer else float(rng.choice([0.0, 0.25]))
+    ld = -(-K // 16) * 16
+    p = W.Problem("rnd8_%d" % i, M, N, K, dtype, has_c=beta != 0.0, alpha=alpha, beta=beta,
+                  dist="int2" if integer else "uniform", c_dist="int2" if integer else "normal",
+                  seed=91 + i, a_fmt=fa, b_fmt=fb, lda=ld, ldb=ld)
+    data = W.make(p)
+    C = data["C"].to(DEV) if data["C"] is not None else None
+    D = G.gemm_fp8(data["A"].to(DEV), data["B"].to(DEV), M, N, K, lda=ld, ldb=ld, a_format=fa,
+                   b_format=fb, out_dtype=W.torch_dtype(dtype), alpha=alpha, beta=beta, C=C)
+    st, detail = G.last_device_status()
+    assert st == 0, "device status %d detail %#x" % (st, detail)
+    code = O.dtype_code(dtype)
+    ref, sab = O.gemm(M, N, K, alpha, W.bits(data["A"]), ld, O.K_MAJOR, W.bits(data["B"]), ld, O.K_MAJOR,
+                      beta, W.bits(data["C"]) if data["C"] is not None else None, N, code,
+                      a_dtype=O.dtype_code(fa), b_dtype=O.dtype_code(fb))
+    d = O.decode(code, W.bits(D.cpu())).reshape(M, N)
+    ref = ref.reshape(M, N)
+    if integer:
+        assert np.array_equal(d, O.decode(code, O.round_to(code, ref)).reshape(M, N))
+        return
+    c = O.decode(code, W.bits(data["C"])).reshape(M, N) if data["C"] is not None else None
+    bound = O.bound(code, alpha, beta, ref, sab.reshape(M, N), c)
+    assert np.all(np.isfinite(d)) and np.all(np.abs(d - ref) <= bound)
