@@ -104,9 +104,10 @@ gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha,
    one flag per SM).  GB_ERR_UNSUPPORTED_ARCH without a compute capability 10.3 device. */
 gb_status gb_gemm_workspace_bytes(size_t* bytes);
 
-/* Schedule for later *_ws calls (process-wide): 0 stream-K when the output tiles leave a
-   ragged last wave or are fewer than the CTAs (the default), 1 whole tiles only, 2 stream-K
-   whenever K > 0.  GB_ERR_INVALID_ARG for other values. */
+/* Schedule for later *_ws calls (process-wide): 0 (the default) stream-K when the output
+   tiles are fewer than the CTAs and the (tile, stage) units give every CTA at least two,
+   else whole tiles; 1 whole tiles only; 2 stream-K whenever K > 0.  GB_ERR_INVALID_ARG for
+   other values. */
 gb_status gb_set_schedule(int schedule);
 
 /* Fused epilogue ("CUTLASS, in depth" — "Epilogue fusion": load C, load a bias vector,

@@ -1165,6 +1165,10 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
   if constexpr (kPair) cluster_sync();   // peer barriers initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  // launched with programmatic stream serialisation: the set-up above may overlap the end of
+  // the previous kernel in the stream; nothing below touches global memory before it is done
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0)

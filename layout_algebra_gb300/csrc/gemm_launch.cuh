@@ -8,14 +8,28 @@ namespace gb {
 template <bool kBF16, int kIn, int kShape>
 gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s) {
   using C = gb::Cfg<false, kIn, kShape>;
-  bool& attr = dev->attr_single[kBF16][kIn][kShape == gb::kShapeNarrow];
-  if (!attr) {
+  bool& smem_set = dev->attr_single[kBF16][kIn][kShape == gb::kShapeNarrow];
+  if (!smem_set) {
     if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, false, kIn, kShape>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes) != cudaSuccess)
       return GB_ERR_LAUNCH;
-    attr = true;
+    smem_set = true;
   }
-  gb::gemm_kernel<kBF16, false, kIn, kShape><<<grid, C::kThreads, C::kSmemBytes, s>>>(m.a, m.b, m.sfa, m.sfb, m.c, m.d, m.at, m.bt, p);
+  // programmatic stream serialisation: the kernel's set-up may overlap the end of the previous
+  // kernel in the stream (it waits for that kernel before touching global memory)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, false, kIn, kShape>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, m.at,
+                         m.bt, p) != cudaSuccess)
+    return GB_ERR_LAUNCH;
   return cudaGetLastError() == cudaSuccess ? GB_OK : GB_ERR_LAUNCH;
 }
 
@@ -58,17 +72,20 @@ template <bool kBF16, int kIn, int kShape>
 gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s) {
   using C = gb::Cfg<true, kIn, kShape>;
   constexpr int kCl = kShape == kShapeMc ? 4 : 2;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic stream serialisation (see launch_single)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cfg.gridDim = dim3(kCl * clusters, 1, 1);
   if (cudaLaunchKernelEx(&cfg, gb::gemm_kernel<kBF16, true, kIn, kShape>, m.a, m.b, m.sfa, m.sfb, m.c, m.d, m.at, m.bt, p) != cudaSuccess)
     return GB_ERR_LAUNCH;

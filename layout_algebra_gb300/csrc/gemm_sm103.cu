@@ -134,10 +134,10 @@ std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
 int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast;
-                           // 5: CTA pair with 224-column tiles;
-                           // 4: single CTA with narrow tiles
-int g_force_schedule = 0;  // 0: stream-K when a workspace is given and tiles leave a ragged
-                           // last wave; 1: data-parallel only; 2: stream-K whenever possible
+                           // 4: single CTA with narrow tiles; 5: CTA pair with 224-column tiles
+int g_force_schedule = 0;  // 0: stream-K when a workspace is given, the tiles are fewer than the
+                           // CTAs and every CTA gets two stage-blocks; 1: data-parallel only;
+                           // 2: stream-K whenever possible
 
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
@@ -775,7 +775,12 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;   // the same for every input kind
   p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   bool sk = !mc && workspace != nullptr && p.nsb > 0 && sched != 1;   // multicast: whole tiles
-  if (sk && sched == 0) sk = p.num_tiles % slots != 0;
+  // default: only an under-filled GPU gains (fewer tiles than CTAs, the decode-like shapes);
+  // a ragged last wave of a larger problem is cheaper than the partial-tile hand-offs (the
+  // 224-column pair tiles absorb most of it), and a K too short to give every CTA two
+  // stage-blocks costs more in hand-offs than it spreads
+  if (sk && sched == 0)
+    sk = p.num_tiles < slots && static_cast<int64_t>(p.num_tiles) * p.nsb >= 2 * static_cast<int64_t>(slots);
   int G;
   if (sk) {
     G = slots;

@@ -278,6 +278,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have completed and
+// their memory operations are visible, and let the grid that depends on this one be scheduled
+// (it runs its own set-up, then waits in griddep_wait for this grid to complete).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 16-byte shared-memory load / store at a shared-window address.
 __device__ __forceinline__ uint4 ld_shared_u4(uint32_t addr) {
   uint4 v;
