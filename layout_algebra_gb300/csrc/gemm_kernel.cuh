@@ -278,7 +278,8 @@ __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl* ctl, 
 
 // Grouped raster order: runs of group_m M-tiles, walked down M first, then across N,
 // so that CTAs working at the same time share A rows and B columns in L2 ("CUTLASS, in
-// depth" — "Kernel schedules", rasterisation).
+// depth" — "Kernel schedules", rasterisation).  Odd groups walk N backwards, so a group
+// starts on the B columns the previous one ended on (still in L2).
 __device__ __forceinline__ void raster(int32_t t, int32_t m_tiles, int32_t n_tiles, int32_t group_m,
                                        int32_t& mt, int32_t& nt) {
   const int32_t per_group = group_m * n_tiles;
@@ -288,6 +289,7 @@ __device__ __forceinline__ void raster(int32_t t, int32_t m_tiles, int32_t n_til
   const int32_t local = t - g * per_group;
   mt = first_m + local % gm;
   nt = local / gm;
+  if (g & 1) nt = n_tiles - 1 - nt;
 }
 
 __device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t& mt, int32_t& nt) {
