@@ -26,7 +26,10 @@
  *
  * Ownership and execution: every buffer is caller-owned device memory; the call
  * allocates nothing, is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
- * default stream) and returns once the kernel is queued.  The call reads no C when
+ * default stream) and returns once the kernel is queued.  The kernel is launched with
+ * programmatic stream serialisation: its set-up may overlap the end of the previous kernel
+ * in the stream, and it touches global memory only after that kernel has completed (stream
+ * order is kept for every buffer).  The call reads no C when
  * beta == 0, and then C may be NULL.  M == 0 or N == 0 is a no-op; K == 0 gives
  * D = beta*C.
  *
