@@ -53,7 +53,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
 
 // Block-scaled FP8 uses 224-column tiles: two accumulators (at TMEM columns 0 and 256) and,
-// in the 32 columns behind each, one slot of scale factors (4 columns for A's 128 rows, 8
+// in the 32 columns behind each, two slots of scale factors (4 columns for A's 128 rows, 8
 // for B's columns), so the epilogue still overlaps the next tile.
 constexpr int kMxTileN = 224;
 constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
@@ -599,9 +599,10 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       for (int h = 0; h < nkb; ++h) {
         uint32_t sfa = 0, sfb = 0;
         if constexpr (C::kMx) {
-          // this k-block's scale factors into a TMEM slot behind an accumulator (two slots
-          // alternate; copies and MMAs of one thread execute in issue order)
-          const uint32_t slot = tmem_base + C::kTileN + (kbc & 1u) * C::kAccStride;
+          // this k-block's scale factors into a TMEM slot behind an accumulator (four slots of
+          // 12 columns, two in the 32 columns behind each accumulator, rotate; copies and MMAs
+          // of one thread execute in issue order)
+          const uint32_t slot = tmem_base + C::kTileN + (kbc & 1u) * C::kAccStride + ((kbc >> 1) & 1u) * 16u;
           // the stage holds A's kKB atoms, then B's kKB atom pairs
           const uint32_t sfa_s = sa + C::kSfOff + h * 512;
           const uint32_t sfb_s = sa + C::kSfOff + C::kKB * 512 + h * 1024;
