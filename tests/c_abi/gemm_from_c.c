@@ -1,0 +1,79 @@
+/*
+ * A plain C caller of the GEMM C ABI (include/gb300_gemm.h): no Python, no torch.  It owns
+ * its device buffers (CUDA runtime), calls gb_gemm_f16 on a stream with a K-major A and an
+ * MN-major B, reads the device status word, and checks D exactly: the operands are small
+ * integers, so every sum is an integer far below 2^11 and exact in fp16 and fp32.
+ * Exit status 0 on success.
+ */
+#include <cuda_runtime_api.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include "gb300_gemm.h"
+
+static uint16_t f16_of_int(int v) {
+  /* exact binary16 encoding of a small integer (|v| < 2048) */
+  if (v == 0) return 0;
+  uint16_t sign = v < 0 ? 0x8000u : 0u;
+  unsigned a = (unsigned)(v < 0 ? -v : v);
+  int e = 0;
+  while ((a >> e) > 1) ++e;
+  unsigned frac = (a << (10 - e)) & 0x3FFu;
+  return (uint16_t)(sign | ((unsigned)(e + 15) << 10) | frac);
+}
+
+static int int_of_f16(uint16_t h) {
+  int e = (h >> 10) & 0x1F, f = h & 0x3FF;
+  if (e == 0) return 0; /* only exact small integers are expected */
+  int mag = (1 << 10 | f);
+  mag = e - 25 >= 0 ? mag << (e - 25) : mag >> (25 - e);
+  return (h & 0x8000u) ? -mag : mag;
+}
+
+int main(void) {
+  const int64_t M = 300, N = 200, K = 136, lda = 136, ldb = 200; /* A K-major, B N-major */
+  uint16_t *A = malloc(M * lda * 2), *B = malloc(K * ldb * 2), *C = malloc(M * N * 2), *D = malloc(M * N * 2);
+  int *a = malloc(M * K * sizeof(int)), *b = malloc(K * N * sizeof(int)), *c = malloc(M * N * sizeof(int));
+  if (!A || !B || !C || !D || !a || !b || !c) return 2;
+  unsigned s = 12345u;
+  for (int64_t i = 0; i < M * K; ++i) { s = s * 1103515245u + 12345u; a[i] = (int)((s >> 16) % 5) - 2; }
+  for (int64_t i = 0; i < K * N; ++i) { s = s * 1103515245u + 12345u; b[i] = (int)((s >> 16) % 5) - 2; }
+  for (int64_t i = 0; i < M * N; ++i) { s = s * 1103515245u + 12345u; c[i] = (int)((s >> 16) % 5) - 2; }
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t k = 0; k < K; ++k) A[m * lda + k] = f16_of_int(a[m * K + k]);
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t n = 0; n < N; ++n) B[k * ldb + n] = f16_of_int(b[k * N + n]);
+  for (int64_t i = 0; i < M * N; ++i) C[i] = f16_of_int(c[i]);
+
+  void *dA, *dB, *dC, *dD;
+  cudaStream_t st;
+  if (cudaMalloc(&dA, M * lda * 2) || cudaMalloc(&dB, K * ldb * 2) || cudaMalloc(&dC, M * N * 2) ||
+      cudaMalloc(&dD, M * N * 2) || cudaStreamCreate(&st))
+    return 3;
+  cudaMemcpy(dA, A, M * lda * 2, cudaMemcpyHostToDevice);
+  cudaMemcpy(dB, B, K * ldb * 2, cudaMemcpyHostToDevice);
+  cudaMemcpy(dC, C, M * N * 2, cudaMemcpyHostToDevice);
+  gb_status r = gb_gemm_f16(M, N, K, 1.0f, dA, lda, GB_K_MAJOR, dB, ldb, GB_MN_MAJOR, 1.0f, dC, dD, st);
+  if (r != GB_OK) { fprintf(stderr, "gb_gemm_f16: %s\n", gb_status_string(r)); return 4; }
+  uint32_t detail = 0;
+  r = gb_last_device_status(st, &detail);
+  if (r != GB_OK) { fprintf(stderr, "device status: %s (%#x)\n", gb_status_string(r), detail); return 5; }
+  cudaMemcpy(D, dD, M * N * 2, cudaMemcpyDeviceToHost);
+  long bad = 0;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      int want = c[m * N + n];
+      for (int64_t k = 0; k < K; ++k) want += a[m * K + k] * b[k * N + n];
+      if (int_of_f16(D[m * N + n]) != want) ++bad;
+    }
+  /* argument errors come back before any launch */
+  if (gb_gemm_f16(M, N, K, 1.0f, (char*)dA + 2, lda, GB_K_MAJOR, dB, ldb, GB_MN_MAJOR, 0.0f, NULL, dD, st) !=
+      GB_ERR_MISALIGNED)
+    return 6;
+  if (gb_gemm_f16(M, N, K, 1.0f, dA, lda, GB_K_MAJOR, dB, ldb, GB_MN_MAJOR, 1.0f, NULL, dD, st) != GB_ERR_INVALID_ARG)
+    return 7;
+  printf("C ABI: %ld of %ld outputs wrong\n", bad, (long)(M * N));
+  cudaFree(dA); cudaFree(dB); cudaFree(dC); cudaFree(dD); cudaStreamDestroy(st);
+  return bad == 0 ? 0 : 1;
+}
