@@ -159,6 +159,30 @@ def test_long_k():
     check(p, data, run(p, data))
 
 
+def test_output_past_2_31_elements():
+    """D of 2^31 elements (4 GiB): element offsets past the int32 range in the epilogue and a
+    tile grid of 8192 x 4 tiles; sampled outputs (first, middle and last rows, random
+    entries) against the oracle."""
+    M, N, K = 1 << 21, 1024, 64
+    p = W.Problem("big", M, N, K, "f16", dist="uniform", seed=61)
+    data = W.make(p)
+    D = torch.empty(M * N, dtype=torch.float16, device=DEV)
+    G.gemm(data["A"].to(DEV), data["B"].to(DEV), M, N, K, lda=K, ldb=K, D=D)
+    st, detail = G.last_device_status()
+    assert st == 0, "device status %d detail %#x" % (st, detail)
+    rng = np.random.default_rng(7)
+    rows = np.concatenate([np.repeat([0, M // 2, M - 256, M - 1], N), rng.integers(0, M, 20000)])
+    cols = np.concatenate([np.tile(np.arange(N), 4), rng.integers(0, N, 20000)])
+    idx = torch.from_numpy(rows * N + cols).to(DEV)
+    d = O.decode(O.F16, W.bits(D[idx].cpu()))
+    ref, sab = O.gemm(M, N, K, 1.0, W.bits(data["A"]), K, 0, W.bits(data["B"]), K, 0, 0.0, None, N, O.F16,
+                      rows, cols)
+    bound = O.bound(O.F16, 1.0, 0.0, ref, sab, None)
+    assert np.all(np.abs(d - ref) <= bound)
+    del D
+    torch.cuda.empty_cache()
+
+
 def test_k_zero_gives_beta_c(variant):
     p = W.Problem("k0", 200, 264, 0, "f16", has_c=True, alpha=2.0, beta=0.5,
                   c_dist="uniform", seed=61)
