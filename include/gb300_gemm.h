@@ -29,8 +29,9 @@
  * default stream) and returns once the kernel is queued.  The kernel is launched with
  * programmatic stream serialisation: its set-up may overlap the end of the previous kernel
  * in the stream, and it touches global memory only after that kernel has completed (stream
- * order is kept for every buffer).  The call reads no C when
- * beta == 0, and then C may be NULL.  M == 0 or N == 0 is a no-op; K == 0 gives
+ * order is kept for every buffer).  Calls may come from several host threads at once: the
+ * library's host state (per-device set-up, cached plans) is kept under a lock.  The call
+ * reads no C when beta == 0, and then C may be NULL.  M == 0 or N == 0 is a no-op; K == 0 gives
  * D = beta*C.
  *
  * Errors are reported before any launch (validation "can_implement", "CUTLASS, in
@@ -248,7 +249,8 @@ typedef struct {
 gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
                             int64_t ldb, int majorB, gb_gemm_plan* plan);
 
-/* Robustness knobs (process-wide, read at launch; not thread-safe with concurrent calls):
+/* Robustness knobs (process-wide, read when a call launches, so a change made while other
+   threads launch reaches some of their calls and not others):
    the limit on every in-kernel wait, in nanoseconds (0 restores the 2 s default), and a
    test hook that makes the copy stage skip the k-block with the given running index
    (-1 disables), so that the consumer's bounded wait runs out and the timeout path is

@@ -364,7 +364,8 @@ def make_workspace(device=None):
 
 
 def set_schedule(schedule):
-    """0: stream-K for ragged last waves (default); 1: whole tiles only; 2: stream-K always."""
+    """0 (default): stream-K, given a workspace, when the tiles are fewer than the CTAs and each
+    CTA gets two stage-blocks; 1: whole tiles only; 2: stream-K whenever a workspace is given."""
     st = lib().gb_set_schedule(int(schedule))
     if st != 0:
         raise GemmError(st, "set_schedule")

@@ -13,8 +13,9 @@ namespace gb {
 #define GB_PAIR(BF, IN, SHAPE)                                                               \
   template gb_status prepare_pair<BF, IN, SHAPE>(DeviceState*);                              \
   template gb_status launch_pair<BF, IN, SHAPE>(const Maps&, const Params&, int, cudaStream_t);
-#define GB_SINGLE(BF, IN, SHAPE) \
-  template gb_status launch_single<BF, IN, SHAPE>(DeviceState*, const Maps&, const Params&, int, cudaStream_t);
+#define GB_SINGLE(BF, IN, SHAPE)                                                             \
+  template gb_status prepare_single<BF, IN, SHAPE>(DeviceState*);                            \
+  template gb_status launch_single<BF, IN, SHAPE>(const Maps&, const Params&, int, cudaStream_t);
 
 #if GB_INST_GROUP == 0      // the 16-bit CTA-pair kernels (the large-problem path)
 GB_PAIR(true, kIn16, kShapeStd)

@@ -1203,6 +1203,9 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 constexpr int pair_shape_index(int shape) { return shape == kShapeMc ? 1 : (shape == kShapeN224 ? 2 : 0); }
 
 // Per-device state the launchers keep (function attributes set, co-resident clusters).
+// The host writes it only while holding its device-state lock (calls may come from several
+// host threads); each field goes from its initial value to its final one once, except the
+// stream-K launch counter.
 struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
@@ -1225,8 +1228,12 @@ struct Maps {
 };
 
 // Defined in gemm_launch.cuh; instances come from gemm_inst.cu.
+// prepare_* set the function attributes (and, for pairs, count the co-resident clusters)
+// once per device: call them with the device-state lock held.  launch_* touch no shared state.
 template <bool kBF16, int kIn, int kShape>
-gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s);
+gb_status prepare_single(DeviceState* dev);
+template <bool kBF16, int kIn, int kShape>
+gb_status launch_single(const Maps& m, const Params& p, int grid, cudaStream_t s);
 template <bool kBF16, int kIn, int kShape>
 gb_status prepare_pair(DeviceState* dev);
 template <bool kBF16, int kIn, int kShape>

@@ -6,7 +6,7 @@
 namespace gb {
 
 template <bool kBF16, int kIn, int kShape>
-gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int grid, cudaStream_t s) {
+gb_status prepare_single(DeviceState* dev) {
   using C = gb::Cfg<false, kIn, kShape>;
   bool& smem_set = dev->attr_single[kBF16][kIn][kShape == gb::kShapeNarrow];
   if (!smem_set) {
@@ -15,6 +15,12 @@ gb_status launch_single(DeviceState* dev, const Maps& m, const Params& p, int gr
       return GB_ERR_LAUNCH;
     smem_set = true;
   }
+  return GB_OK;
+}
+
+template <bool kBF16, int kIn, int kShape>
+gb_status launch_single(const Maps& m, const Params& p, int grid, cudaStream_t s) {
+  using C = gb::Cfg<false, kIn, kShape>;
   // programmatic stream serialisation: the kernel's set-up may overlap the end of the previous
   // kernel in the stream (it waits for that kernel before touching global memory)
   cudaLaunchAttribute attr[1];

@@ -151,10 +151,14 @@ bool is_pair(int variant) {
 
 using gb::DeviceState;
 using gb::Maps;
+using gb::prepare_single;
 using gb::launch_single;
 using gb::prepare_pair;
 using gb::launch_pair;
 
+// Per-device launcher state; every write to it (probing, function attributes, cluster
+// counts, the stream-K launch counter) happens with g_dev_mu held.
+std::mutex g_dev_mu;
 DeviceState g_dev[128];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -476,6 +480,7 @@ gb_status device_state(DeviceState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
   if (dev < 0 || dev >= 128) return GB_ERR_UNSUPPORTED_ARCH;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceState& d = g_dev[dev];
   if (!d.probed) {
     if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -530,7 +535,16 @@ void fill_params(const DeviceState* dev, const gb_gemm_plan& pl, int64_t M, int6
 
 
 // Dispatch on the output type, the input kind and the pair kernels (the multicast pair and the
-// 224-column pair take 16-bit and FP8 inputs).
+// 224-column pair take 16-bit and FP8 inputs).  prepare_*_any run with g_dev_mu held.
+template <bool kBF16>
+gb_status prepare_single_any(int kin, bool narrow, DeviceState* dev) {
+  using namespace gb;
+  if (narrow)
+    return kin == kIn8 ? prepare_single<kBF16, kIn8, kShapeNarrow>(dev) : prepare_single<kBF16, kIn16, kShapeNarrow>(dev);
+  if (kin == kInMx) return prepare_single<kBF16, kInMx, kShapeStd>(dev);
+  return kin == kIn8 ? prepare_single<kBF16, kIn8, kShapeStd>(dev) : prepare_single<kBF16, kIn16, kShapeStd>(dev);
+}
+
 template <bool kBF16>
 gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
   using namespace gb;
@@ -543,15 +557,15 @@ gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
 }
 
 template <bool kBF16>
-gb_status launch_any(bool pair, int kin, int shape, bool narrow, DeviceState* dev, const Maps& m, const Params& p,
-                     int G, cudaStream_t s) {
+gb_status launch_any(bool pair, int kin, int shape, bool narrow, const Maps& m, const Params& p, int G,
+                     cudaStream_t s) {
   if (!pair) {
     if (narrow)
-      return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeNarrow>(dev, m, p, G, s)
-                             : launch_single<kBF16, gb::kIn16, gb::kShapeNarrow>(dev, m, p, G, s);
-    if (kin == gb::kInMx) return launch_single<kBF16, gb::kInMx, gb::kShapeStd>(dev, m, p, G, s);
-    return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeStd>(dev, m, p, G, s)
-                           : launch_single<kBF16, gb::kIn16, gb::kShapeStd>(dev, m, p, G, s);
+      return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeNarrow>(m, p, G, s)
+                             : launch_single<kBF16, gb::kIn16, gb::kShapeNarrow>(m, p, G, s);
+    if (kin == gb::kInMx) return launch_single<kBF16, gb::kInMx, gb::kShapeStd>(m, p, G, s);
+    return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeStd>(m, p, G, s)
+                           : launch_single<kBF16, gb::kIn16, gb::kShapeStd>(m, p, G, s);
   }
   if (shape == gb::kShapeMc)
     return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeMc>(m, p, G, s)
@@ -758,12 +772,17 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   const bool mc = pl.variant == kVariantPairMc;
   const int shape = mc ? gb::kShapeMc : (pl.variant == kVariantPair224 ? gb::kShapeN224 : gb::kShapeStd);
   const bool bf = dtype == GB_BF16;
-  if (pair) {
-    st = bf ? prepare_pair_any<true>(in.kind(), shape, dev) : prepare_pair_any<false>(in.kind(), shape, dev);
+  const bool narrow = pl.variant == kVariantNarrow;
+  int slots;   // CTAs (clusters) that can run at once
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (pair)
+      st = bf ? prepare_pair_any<true>(in.kind(), shape, dev) : prepare_pair_any<false>(in.kind(), shape, dev);
+    else
+      st = bf ? prepare_single_any<true>(in.kind(), narrow, dev) : prepare_single_any<false>(in.kind(), narrow, dev);
     if (st != GB_OK) return st;
+    slots = pair ? dev->pair_clusters[gb::pair_shape_index(shape)] : dev->sms;
   }
-  // CTAs (clusters) that can run at once
-  const int slots = pair ? dev->pair_clusters[gb::pair_shape_index(shape)] : dev->sms;
 
   // schedule: stream-K needs a workspace and some K; by default it is used when the tiles
   // leave a ragged last wave (or fewer tiles than CTAs)
@@ -786,8 +805,11 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     G = slots;
     const int full = p.num_tiles / G;
     p.dp_tiles = full >= 2 ? (full - 1) * G : 0;
-    if (++dev->epoch == 0) dev->epoch = 1;
-    p.epoch = dev->epoch;
+    {
+      std::lock_guard<std::mutex> lk(g_dev_mu);
+      if (++dev->epoch == 0) dev->epoch = 1;
+      p.epoch = dev->epoch;
+    }
     p.ws_flags = static_cast<uint32_t*>(workspace);
     p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                          ((static_cast<int64_t>(dev->sms) * 4 + 255) / 256) * 256);
@@ -796,9 +818,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.dp_tiles = p.num_tiles;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool narrow = pl.variant == kVariantNarrow;
-  return bf ? launch_any<true>(pair, in.kind(), shape, narrow, dev, maps, p, G, s)
-            : launch_any<false>(pair, in.kind(), shape, narrow, dev, maps, p, G, s);
+  return bf ? launch_any<true>(pair, in.kind(), shape, narrow, maps, p, G, s)
+            : launch_any<false>(pair, in.kind(), shape, narrow, maps, p, G, s);
 }
 
 }  // namespace
@@ -1002,11 +1023,14 @@ gb_status gb_debug_stage_bytes(int dtype, int which, int64_t M, int64_t N, int64
   Params p;
   fill_params(dev, pl, M, N, K, 1.0f, majorA, majorB, 0.0f, nullptr, nullptr, &p);
   const int smem = 1024 + gb::Cfg<false>::kStageBytes + gb::kCtlBytes;
-  if (!dev->dbg_attr) {
-    if (cudaFuncSetAttribute(gb::stage_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return GB_ERR_LAUNCH;
-    dev->dbg_attr = true;
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!dev->dbg_attr) {
+      if (cudaFuncSetAttribute(gb::stage_bytes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+        return GB_ERR_LAUNCH;
+      dev->dbg_attr = true;
+    }
   }
   gb::stage_bytes_kernel<<<1, 32, smem, static_cast<cudaStream_t>(stream)>>>(
       tm, p, which, static_cast<int32_t>(tile), static_cast<int32_t>(k_block), static_cast<uint4*>(out));
