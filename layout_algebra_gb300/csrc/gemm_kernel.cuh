@@ -830,32 +830,50 @@ __device__ __forceinline__ uint32_t* part_flag(const Params& p, uint32_t c, uint
   return p.ws_flags + static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank;
 }
 
-// Warp-collective bounded wait until a partial-ready flag carries this launch's epoch.
+// Warp-collective bounded wait until the partial-ready flags of the CTAs (pairs) c_lo..c_hi
+// that hold stream-K units carry this launch's epoch.  The flags are spread over the lanes
+// (lane l watches c_lo + l, c_lo + l + 32, ...), so one poll has all of them in flight
+// instead of one round trip per flag; each lane's acquire load orders, and the warp barrier
+// then passes on to every lane, the contributors' partials before the reads that follow.
 template <bool kPair>
-__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, Ctl* ctl, uint64_t limit) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) {
-    uint64_t t0 = 0;
-    for (uint32_t n = 0;; ++n) {
-      if (ld_acquire_gpu(flag) == epoch) {
-        ok = 1;
-        break;
-      }
-      if ((n & 63) == 63) {
-        if (aborted(ctl)) break;
-        const uint64_t now = global_timer_ns();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > limit) {
-          raise_status<kPair>(ctl, kSiteFixup);
-          break;
+__device__ __noinline__ bool wait_flags(const Params& p, uint32_t G, uint32_t c_lo, uint32_t c_hi, uint32_t rank,
+                                        Ctl* ctl) {
+  const uint32_t lane = threadIdx.x & 31;
+  uint32_t c = c_lo + lane;   // this lane's next flag still to be seen set
+  uint64_t t0 = 0;
+  for (uint32_t n = 0;; ++n) {
+    // a flag seen set stays set for this launch (only this owner clears it, afterwards)
+    while (c <= c_hi &&
+           (!sk_has_units(p, G, c) || ld_acquire_gpu(part_flag<kPair>(p, c, rank)) == p.epoch))
+      c += 32;
+    if (__all_sync(0xffffffffu, c > c_hi)) break;
+    if ((n & 63) == 63) {
+      int stop = 0;
+      if (lane == 0) {
+        if (aborted(ctl)) {
+          stop = 1;
+        } else {
+          const uint64_t now = global_timer_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > p.timeout_ns) {
+            raise_status<kPair>(ctl, kSiteFixup);
+            stop = 1;
+          }
         }
       }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) (void)ld_acquire_gpu(flag);   // every lane acquires before reading the partial
-  return ok != 0;
+  __syncwarp();
+  return true;
+}
+
+// The next CTA (pair) at or after c, up to c_hi, whose stream-K range holds units (c_hi + 1
+// if none).
+__device__ __forceinline__ uint32_t next_contributor(const Params& p, uint32_t G, uint32_t c, uint32_t c_hi) {
+  while (c <= c_hi && !sk_has_units(p, G, c)) ++c;
+  return c;
 }
 
 // One 32-column run of the tile-store epilogue for this warp's 32 rows: C from its staging
@@ -933,6 +951,13 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   // (two runs earlier) has finished reading.
   const bool tma = C::kEpiTma && p.epi_tma != 0;
   const uint32_t stg = smem_addr(epi_smem) + static_cast<uint32_t>(ew) * 4u * C::kEpiBufBytes;
+  // stream-K owner: this lane's column of this warp's share of the stage ring, where the
+  // other CTAs' partials of a run are gathered (kPartBatch CTAs x 32 columns x 32 rows fp32)
+  constexpr int kRingBytes = C::kStages * C::kStageBytes;
+  constexpr int kPartBatch = kRingBytes / (C::kEpiWarps * 4096) < 8 ? kRingBytes / (C::kEpiWarps * 4096) : 8;
+  static_assert(kPartBatch >= 1, "the stage ring holds one run of partials per epilogue warp");
+  const uint32_t part_buf = smem_addr(epi_smem) - static_cast<uint32_t>(kRingBytes) +
+                            static_cast<uint32_t>(ew) * kPartBatch * 4096u + static_cast<uint32_t>(lane) * 4u;
   uint32_t gr = 0, c_phase = 0;
   uint32_t c_pending = 0;            // staging buffers with a C copy issued, not yet waited for
   int32_t it = 0;
@@ -992,11 +1017,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     if (owner_with_parts) {
       c_lo = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile) * p.nsb + item.sb1);
       c_hi = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile + 1) * p.nsb - 1);
-      bool ok = true;
-      for (uint32_t c = c_lo; ok && c <= c_hi; ++c)
-        if (sk_has_units(p, nclusters, c))
-          ok = wait_flag<kPair>(part_flag<kPair>(p, c, rank), p.epoch, ctl, p.timeout_ns);
-      if (!ok) break;
+      if (!wait_flags<kPair>(p, nclusters, c_lo, c_hi, rank, ctl)) break;
     }
     float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
     bool ok = true;
@@ -1016,12 +1037,25 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
           for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
         } else {
-          for (uint32_t c = c_lo; c <= c_hi; ++c) {
-            if (!sk_has_units(p, nclusters, c)) continue;
-            const float* part = part_slot<kPair>(p, c, rank);
+          // the other CTAs' partials of this run, added in CTA order: up to kPartBatch
+          // CTAs' values are gathered at once (asynchronous copies, one round trip) into
+          // this warp's part of the stage ring, which is idle here — a split tile is its
+          // owner's last item, so every copy into the ring has landed and every MMA
+          // reading it has completed
+          uint32_t c = next_contributor(p, nclusters, c_lo, c_hi);
+          while (c <= c_hi) {
+            int n = 0;
+            for (; n < kPartBatch && c <= c_hi; ++n) {
+              const float* part = part_slot<kPair>(p, c, rank) + c0 * 128 + lrow;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (c0 + i) * 128 + lrow));
+              for (int i = 0; i < 32; ++i) cp_async_4(part_buf + (n * 32 + i) * 128, part + i * 128);
+              c = next_contributor(p, nclusters, c + 1, c_hi);
+            }
+            cp_async_wait_all();   // this lane reads back only what it copied
+            for (int k = 0; k < n; ++k)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                acc[i] = __float_as_uint(__uint_as_float(acc[i]) + ld_shared_f32(part_buf + (k * 32 + i) * 128));
           }
           if (C::kEpiTma && tstore)
             ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
@@ -1063,9 +1097,11 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
       // with the same launch number (a replayed CUDA graph) waits for fresh ones.  A CTA
       // owns at most one split tile per launch, so fix_done completes phase 0 once.
       if (!wait_warp<kPair>(smem_addr(&ctl->fix_done), 0u, ctl, p.timeout_ns, kSiteFixup)) break;
+      // (relaxed stores: nothing reads these flags again in this launch, and the next launch
+      // starts after this one has completed)
       if (lane == 0)
         for (uint32_t c = c_lo; c <= c_hi; ++c)
-          if (sk_has_units(p, nclusters, c)) st_release_gpu(part_flag<kPair>(p, c, rank), 0u);
+          if (sk_has_units(p, nclusters, c)) st_relaxed_gpu(part_flag<kPair>(p, c, rank), 0u);
       __syncwarp();
     }
     if (contributor && warp == 2) {
