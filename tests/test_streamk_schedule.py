@@ -6,8 +6,9 @@ remaining (tile, stage-block) units, cut at tile boundaries.  dp_tiles = (tiles/
 when tiles >= 2G, else 0.  The owner of a split tile holds its first unit; the other
 holders are found from the range bounds.  These checks mirror that arithmetic and verify:
 every unit is covered once, the owner's contributor set is exactly the other holders,
-and a split tile is each contributor's first stream-K item (so partials are written
-before any owner can wait for them).
+a split tile is each contributor's first stream-K item (so partials are written
+before any owner can wait for them), and a split tile is its owner's last item, at most one
+per CTA (so the owner's stage ring is idle while it gathers the partials there).
 """
 import random
 
@@ -54,6 +55,7 @@ def test_stream_k_split_invariants(seed):
             for t, s0, s1 in schedule(c, G, tiles, nsb, dp):
                 cover.setdefault(t, []).append((s0, s1, c))
         assert sorted(cover) == list(range(tiles))
+        owned_split = {}
         for t, parts in cover.items():
             parts.sort()
             assert parts[0][0] == 0 and parts[-1][1] == nsb
@@ -62,6 +64,8 @@ def test_stream_k_split_invariants(seed):
             if len(parts) == 1:
                 continue
             owner = parts[0]
+            assert schedule(owner[2], G, tiles, nsb, dp)[-1] == (t, owner[0], owner[1])
+            owned_split[owner[2]] = owned_split.get(owner[2], 0) + 1
             lo = owner_of(t * nsb + owner[1], G, U, dp, nsb)
             hi = owner_of((t + 1) * nsb - 1, G, U, dp, nsb)
             got = [c for c in range(lo, hi + 1) if has_units(c, G, U)]
@@ -69,6 +73,7 @@ def test_stream_k_split_invariants(seed):
             for _, _, c in parts[1:]:
                 sk_items = schedule(c, G, tiles, nsb, dp)[len(range(c, dp, G)):]
                 assert sk_items[0][0] == t
+        assert all(n == 1 for n in owned_split.values())
 
 
 def test_balance():
