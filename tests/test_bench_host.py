@@ -84,6 +84,15 @@ def test_traffic_record_requires_matching_kernel(tmp_path, monkeypatch):
     rec["kernel_sha"] = "stale"
     (prof / "traffic.json").write_text(json.dumps(rec))
     assert bench.load_traffic("w") is None
+    # a workload re-captured later carries its own hash, which wins over the file's
+    rec["workloads"]["w"]["kernel_sha"] = bench.kernel_source_hash()
+    rec["workloads"]["v"] = {"dram_bytes_per_launch": 7}
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.load_traffic("w") == 123 and bench.load_traffic("v") is None
+    rec["workloads"]["w"]["kernel_sha"] = "stale"
+    rec["kernel_sha"] = bench.kernel_source_hash()
+    (prof / "traffic.json").write_text(json.dumps(rec))
+    assert bench.load_traffic("w") is None and bench.load_traffic("v") == 7
 
 
 def test_peaks_fallback(tmp_path, monkeypatch):
