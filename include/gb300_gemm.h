@@ -87,8 +87,10 @@ gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
    K loop of some tiles across CTAs ("stream-K", after "CUTLASS, in depth" — "Kernel
    schedules": split-K and stream-K divide K across CTAs when output tiles are too few to
    fill the GPU, at the cost of a reduction and a workspace).  Each CTA first runs whole
-   tiles, then an even contiguous share of the remaining (tile, k-block) units; the CTA that
-   holds a tile's first k-units adds the other CTAs' fp32 partials before the epilogue.
+   tiles, then an even contiguous share of the remaining (tile, stage-block) units (a
+   stage-block is the k-blocks one pipeline stage holds: two for CTA pairs, one for single
+   CTAs); the CTA that holds a tile's first unit adds the other CTAs' fp32 partials, in CTA
+   order, before the epilogue.
    workspace: device memory of at least gb_gemm_workspace_bytes() bytes, 256-byte aligned,
    zero-filled before its first use and not shared by calls that may run at the same time
    (it is reused as is by later calls; each launch tags its hand-offs with a new number).
@@ -109,7 +111,7 @@ gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha,
 gb_status gb_gemm_workspace_bytes(size_t* bytes);
 
 /* Schedule for later *_ws calls (process-wide): 0 (the default) stream-K when the output
-   tiles are fewer than the CTAs and the (tile, stage) units give every CTA at least two,
+   tiles are fewer than the CTAs and the (tile, stage-block) units give every CTA at least two,
    else whole tiles; 1 whole tiles only; 2 stream-K whenever K > 0.  GB_ERR_INVALID_ARG for
    other values. */
 gb_status gb_set_schedule(int schedule);
