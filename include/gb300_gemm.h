@@ -177,7 +177,7 @@ gb_status gb_gemm_fp8(int a_format, int b_format, int out_dtype, int64_t M, int6
    operand 1 for B with N rows), 16-byte aligned device buffers.  C, D, epi, workspace and
    stream as for gb_gemm_fp8.  Errors as for gb_gemm_fp8, plus GB_ERR_INVALID_ARG for a
    missing scale buffer when K > 0.  Uses the single-CTA kernel for M <= 128 and the
-   CTA-pair kernel otherwise (variant 3 runs as variant 2). */
+   CTA-pair kernel otherwise. */
 gb_status gb_gemm_mxfp8(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K,
                         float alpha, const void* A, int64_t lda, const void* sfa,
                         const void* B, int64_t ldb, const void* sfb,
@@ -262,16 +262,16 @@ gb_status gb_debug_skip_k_block(int64_t k_block);
 
 /* Kernel variant for later calls (process-wide): 0 chooses by shape (the default: 4 when N
    <= 64, else 1 when M <= 128, else 5 or 2 by the wave count above), 1 the single-CTA
-   128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 3 the CTA-pair kernel in clusters of
-   two pairs that share each B tile through multicast copies (whole tiles only: the *_ws
-   calls do not use stream-K with it), 4 the single-CTA kernel with narrow 128 x 64 tiles and
-   eight 24 KiB stages (for outputs with few columns; with a workspace, stream-K spreads K
-   over the SMs), 5 the CTA-pair kernel with 256 x 224 tiles (K-major B; with MN-major B it
-   runs as 2).  Block-scaled FP8 has no form 3, 4 or 5 and runs as 2 (M > 128) or 1.
-   GB_ERR_INVALID_ARG for other values. */
+   128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 4 the single-CTA kernel with narrow
+   128 x 64 tiles and eight 24 KiB stages (for outputs with few columns; with a workspace,
+   stream-K spreads K over the SMs), 5 the CTA-pair kernel with 256 x 224 tiles (K-major B;
+   with MN-major B it runs as 2).  Block-scaled FP8 has no form 4 or 5 and runs as 2
+   (M > 128) or 1.  Every variant copies each tile into one CTA only (no copy multicast).
+   GB_ERR_INVALID_ARG for other values (3 included). */
 gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1 to 5) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2, 4 or
+   5) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
    in-tile element (r, c) (r < tile_m, c < tile_n, both from gb_gemm_make_plan), or -1
    when the element lies outside M x N.  out is a device buffer of tile_m * tile_n int64.
    Asynchronous on stream. */

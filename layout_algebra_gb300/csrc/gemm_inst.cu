@@ -5,7 +5,7 @@
 #include "gemm_launch.cuh"
 
 #ifndef GB_INST_GROUP
-#error "GB_INST_GROUP must be defined (0..11)"
+#error "GB_INST_GROUP must be defined (0..9)"
 #endif
 
 namespace gb {
@@ -21,31 +21,25 @@ namespace gb {
 GB_PAIR(true, kIn16, kShapeStd)
 #elif GB_INST_GROUP == 1
 GB_PAIR(false, kIn16, kShapeStd)
-#elif GB_INST_GROUP == 2    // CTA pairs sharing B by multicast
-GB_PAIR(true, kIn16, kShapeMc)
-GB_PAIR(false, kIn16, kShapeMc)
-#elif GB_INST_GROUP == 3    // FP8 inputs, CTA pairs
+#elif GB_INST_GROUP == 2    // FP8 inputs, CTA pairs
 GB_PAIR(true, kIn8, kShapeStd)
 GB_PAIR(false, kIn8, kShapeStd)
-#elif GB_INST_GROUP == 4
-GB_PAIR(true, kIn8, kShapeMc)
-GB_PAIR(false, kIn8, kShapeMc)
-#elif GB_INST_GROUP == 5    // block-scaled FP8
+#elif GB_INST_GROUP == 3    // block-scaled FP8
 GB_PAIR(true, kInMx, kShapeStd)
 GB_PAIR(false, kInMx, kShapeStd)
-#elif GB_INST_GROUP == 6
+#elif GB_INST_GROUP == 4
 GB_SINGLE(true, kInMx, kShapeStd)
 GB_SINGLE(false, kInMx, kShapeStd)
-#elif GB_INST_GROUP == 7    // single-CTA kernels, 128 x 256 tiles
+#elif GB_INST_GROUP == 5    // single-CTA kernels, 128 x 256 tiles
 GB_SINGLE(true, kIn16, kShapeStd)
 GB_SINGLE(false, kIn16, kShapeStd)
-#elif GB_INST_GROUP == 8
+#elif GB_INST_GROUP == 6
 GB_SINGLE(true, kIn8, kShapeStd)
 GB_SINGLE(false, kIn8, kShapeStd)
-#elif GB_INST_GROUP == 10   // CTA pairs with 256 x 224 tiles
+#elif GB_INST_GROUP == 7    // CTA pairs with 256 x 224 tiles
 GB_PAIR(true, kIn16, kShapeN224)
 GB_PAIR(false, kIn16, kShapeN224)
-#elif GB_INST_GROUP == 11
+#elif GB_INST_GROUP == 8
 GB_PAIR(true, kIn8, kShapeN224)
 GB_PAIR(false, kIn8, kShapeN224)
 #elif GB_INST_GROUP == 9    // single-CTA kernels, 128 x 64 tiles (few output columns)

@@ -41,8 +41,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 //  pair   (kPair = true):  a cluster of two CTAs on two SMs per 256 x 256 (or 256 x 224) tile;
 //         the even CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared
 //         memory, and each CTA's TMEM holds its own 128 rows of the accumulator.  Each CTA
-//         stages its 128 A rows and its half of the tile's B rows, two k-blocks per stage;
-//         in clusters of two pairs (multicast) the pairs share B.
+//         stages its 128 A rows and its half of the tile's B rows, two k-blocks per stage.
 //         A 512-column tile (kPairTileN = 512) feeds two MMAs from one k-block of A; the
 //         accumulator then fills TMEM, the epilogue no longer overlaps the next tile, and
 //         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
@@ -58,10 +57,10 @@ enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
 constexpr int kMxTileN = 224;
 constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
 
-// Kernel shapes: the standard tiles, the CTA pair in clusters of two pairs sharing B by
-// multicast, narrow single-CTA tiles (128 x 64) for problems with few output columns, and
-// CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a ragged last wave).
-enum : int { kShapeStd = 0, kShapeMc = 1, kShapeNarrow = 2, kShapeN224 = 3 };
+// Kernel shapes: the standard tiles, narrow single-CTA tiles (128 x 64) for problems with few
+// output columns, and CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a
+// ragged last wave).  No shape loads a tile into several CTAs at once (no copy multicast).
+enum : int { kShapeStd = 0, kShapeNarrow = 1, kShapeN224 = 2 };
 constexpr int kNarrowTileN = 64;
 
 template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
@@ -143,8 +142,7 @@ struct Params {
   int32_t bk_elems;           // K elements of one k-block: 64 (16-bit inputs), 128 (8-bit)
   uint32_t* status;           // device status word: first failing wait, 0 if none
   // bit 0 (A), bit 1 (B): one copy moves all kKB k-blocks of the operand's stage (CTA pair,
-  // K a multiple of the k-block); bit 2 (B, multicast pairs): pair p copies k-block p of each
-  // stage into both pairs.  K-major: a three-dimensional map (k-block elements, rows,
+  // K a multiple of the k-block).  K-major: a three-dimensional map (k-block elements, rows,
   // k-blocks); MN-major (rows a multiple of 64): four-dimensional (64 MN elements, K rows of
   // a k-block, 64-wide MN chunks, k-blocks).  Otherwise one two-dimensional copy per k-block.
   int32_t kb_boxes;
@@ -296,22 +294,6 @@ __device__ __forceinline__ void tile_coords(const Params& p, int32_t t, int32_t&
   raster(t, p.m_tiles, p.n_tiles, p.group_m, mt, nt);
 }
 
-// Tile of work item t for pair `pidx` of its cluster.  With B multicast (kMc) a work item
-// is a super-tile of two M-tiles over one column of B tiles: pair 0 takes M-tile 2s,
-// pair 1 takes 2s + 1 (past the last M-tile when m_tiles is odd: its rows are all out of
-// range, and it still loads its share of B for pair 0).
-template <bool kMc>
-__device__ __forceinline__ void item_coords(const Params& p, int32_t t, uint32_t pidx, int32_t& mt,
-                                            int32_t& nt) {
-  if constexpr (kMc) {
-    int32_t sm;
-    raster(t, (p.m_tiles + 1) / 2, p.n_tiles, max(1, p.group_m / 2), sm, nt);
-    mt = 2 * sm + static_cast<int32_t>(pidx);
-  } else {
-    tile_coords(p, t, mt, nt);
-  }
-}
-
 // One unit of work: stage-blocks [sb0, sb1) of tile `tile`.
 struct Item {
   int32_t tile, sb0, sb1;
@@ -406,15 +388,9 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
                              const void* tmSFB, const void* tmAt, const void* tmBt, uint8_t* smem, Ctl* ctl,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair, kIn, kShape>;
-  constexpr bool kMc = kShape == kShapeMc;
-  static_assert(!(kMc && C::kMx), "block-scaled inputs use the pair without multicast");
-  // kMc: a cluster of two pairs on super-tiles; CTA rank = 2 * pair + (rank in pair)
-  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
-  // stage-deep copies: CTA pairs, one MMA per k-block along N.  With B multicast (two pairs
-  // of a cluster on the same B columns) the stage's two k-blocks of B are split between the
-  // pairs instead: pair pidx copies k-block pidx (this CTA's 128 rows) into both pairs.
+  const uint32_t prank = rank & 1u;   // rank in the pair; the even CTA leads
+  // stage-deep copies: CTA pairs, one MMA per k-block along N
   constexpr bool kStageBoxes = kPair && C::kNSub == 1 && C::kKB > 1;
-  static_assert(!kMc || C::kKB == 2, "multicast: one k-block of B per pair");
   int stage = 0;
   uint32_t phase = 0;
   int64_t gkb = 0;
@@ -425,7 +401,7 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   Item item;
   while (ok && sched.next(p, nclusters, item)) {
     int32_t mt, nt;
-    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    tile_coords(p, item.tile, mt, nt);
     const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA;
     const int32_t b_row0 = nt * C::kTileN + static_cast<int32_t>(prank) * C::kRowsBSub;
     for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
@@ -436,12 +412,12 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
       if (gkb != p.skip_kb) {
         const uint32_t full = smem_addr(&ctl->full[stage]);
         // in a pair both CTAs' copies are counted on the even CTA's barrier
-        const uint32_t full_tgt = kPair ? map_to_cta(full, leader) : full;
+        const uint32_t full_tgt = kPair ? map_to_cta(full, 0) : full;
         const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
         // the last stage of a tile may hold fewer k-blocks: copy and count only those (a
         // stage-deep copy always lands whole, its k-blocks past K zero-filled)
         const int nkb = min(C::kKB, p.k_blocks - sb * C::kKB);
-        bool a3 = false, b3 = false, bsplit = false;
+        bool a3 = false, b3 = false;
         // operands with stage-deep maps copy a stage reaching past the maps' k-blocks (a K
         // tail) per k-block through their two-dimensional tail maps
         const void* tmA1 = tmA;
@@ -449,14 +425,13 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
         if constexpr (kStageBoxes) {
           const bool whole = sb * C::kKB + C::kKB <= p.kb_full || p.kb_full == p.k_blocks;
           a3 = whole && (p.kb_boxes & 1) != 0;
-          b3 = whole && !kMc && (p.kb_boxes & 2) != 0;
-          bsplit = kMc && (p.kb_boxes & 4) != 0;
+          b3 = whole && (p.kb_boxes & 2) != 0;
           if (p.kb_boxes & 1) tmA1 = tmAt;
-          if (!kMc && (p.kb_boxes & 2)) tmB1 = tmBt;
+          if (p.kb_boxes & 2) tmB1 = tmBt;
         }
         if (!kPair || prank == 0) {
           // scale factors always arrive for the whole stage (one copy per operand)
-          const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * ((b3 || bsplit) ? C::kKB : nkb) +
+          const uint32_t tx = (C::kAHalf * (a3 ? C::kKB : nkb) + C::kBHalf * (b3 ? C::kKB : nkb) +
                                C::kSfBytes * C::kKB) * (kPair ? 2u : 1u);
           mbar_arrive_expect_tx(full, tx);
         }
@@ -473,31 +448,13 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
             else
               tma_load_4d_pair(sa + C::kAStage, tmB, full_tgt, 0, 0, b_row0 / kSwz, sb * C::kKB);
           }
-          if constexpr (kMc) {
-            if (bsplit) {
-              // past K (a last stage of one k-block) the copy zero-fills; both halves always land
-              const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
-              tma_load_2d_pair_mc(sa + C::kAStage + pidx * C::kBHalf, tmB, full_tgt,
-                                  (sb * C::kKB + static_cast<int32_t>(pidx)) * p.bk_elems, b_row0, mask);
-            }
-          }
         }
         for (int h = 0; h < nkb; ++h) {
           const int32_t kb = sb * C::kKB + h;
           if (!a3)
             issue_operand<kPair>(p.majorA, tmA1, sa + h * C::kAHalf, full_tgt, a_row0, kRowsA, kb,
                                  p.bk_elems);
-          if constexpr (kMc) {
-            // both pairs need the same B rows: this CTA copies its pair's quarter of them
-            // (64 rows) into itself and the same-rank CTA of the other pair
-            if (bsplit) continue;
-            const uint32_t dst = sa + C::kAStage + h * C::kBHalf + pidx * kChunkBytes;
-            const uint16_t mask = static_cast<uint16_t>((1u << prank) | (1u << (prank + 2)));
-            if (p.majorB == 0)
-              tma_load_2d_pair_mc(dst, tmB, full_tgt, kb * p.bk_elems, b_row0 + pidx * kSwz, mask);
-            else
-              tma_load_2d_pair_mc(dst, tmB, full_tgt, b_row0 + pidx * kSwz, kb * kBK, mask);
-          } else if (!b3) {
+          if (!b3) {
             // per MMA along N: this CTA's rows of that MMA's 256 tile columns
 #pragma unroll
             for (int j = 0; j < C::kNSub; ++j)
@@ -558,13 +515,10 @@ template <bool kPair, int kIn, int kShape>
 __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_base, uint32_t rank,
                         uint32_t cluster, uint32_t nclusters) {
   using C = Cfg<kPair, kIn, kShape>;
-  constexpr bool kMc = kShape == kShapeMc;
   uint32_t kbc = 0;                        // k-blocks issued: selects the scale-factor slot
   if (kPair && (rank & 1u) != 0) return;   // the even CTA issues for the pair
-  // a stage is free once every pair reading it has finished: with B multicast the other
-  // pair's copies land in this pair's stages too, so releases go to all four CTAs
-  const uint16_t release_mask = kMc ? 0xF : 0x3;
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (rank & ~1u));
+  // a stage is free, and an accumulator full, for both CTAs of the pair at once
+  constexpr uint16_t kPairMask = 0x3;
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true, issued_any = false;
@@ -650,7 +604,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       }
       issued_any = true;
       if constexpr (kPair)
-        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), release_mask);
+        tc_commit_pair_mc(smem_addr(&ctl->empty[stage]), kPairMask);
       else
         tc_commit(smem_addr(&ctl->empty[stage]));
       if (++stage == C::kStages) {
@@ -665,7 +619,7 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
       if constexpr (kPair) mbar_arrive_cluster(map_to_cta(af, rank + 1));
     } else {
       if constexpr (kPair)
-        tc_commit_pair_mc(af, pair_mask);
+        tc_commit_pair_mc(af, kPairMask);
       else
         tc_commit(af);
     }
@@ -935,8 +889,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
                              uint32_t rank, uint32_t cluster, uint32_t nclusters, uint8_t* epi_smem,
                              const void* tmC, const void* tmD) {
   using C = Cfg<kPair, kIn, kShape>;
-  constexpr bool kMc = kShape == kShapeMc;
-  const uint32_t prank = rank & 1u, pidx = rank >> 1, leader = rank & ~1u;
+  const uint32_t prank = rank & 1u;
   const int q = warp & 3;            // a warp may read TMEM lanes 32*(warp%4) .. +31
   const int lrow = q * 32 + lane;    // accumulator row in this CTA = TMEM lane
   // with eight epilogue warps two share a lane quarter and split the columns
@@ -967,7 +920,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   Item item;
   for (; sched.next(p, nclusters, item); ++it) {
     int32_t mt, nt;
-    item_coords<kMc>(p, item.tile, pidx, mt, nt);
+    tile_coords(p, item.tile, mt, nt);
     const bool row_ok = static_cast<int64_t>(mt) * C::kTileM + r < p.M;
     const int32_t cols_left = p.N - nt * C::kTileN;
     const int64_t base = d_offset(p, mt, nt, r, 0);
@@ -1086,7 +1039,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     if (lane == 0) {
       const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
       if constexpr (kPair)
-        mbar_arrive_cluster(map_to_cta(ae, leader));
+        mbar_arrive_cluster(map_to_cta(ae, 0));
       else
         mbar_arrive(ae);
       if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
@@ -1146,7 +1099,6 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
                 const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmBt,
                 const Params p) {
   using C = Cfg<kPair, kIn, kShape>;
-  constexpr bool kMc = kShape == kShapeMc;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* epi_smem = smem + C::kStages * C::kStageBytes;   // tile-store staging (1024-aligned)
@@ -1160,7 +1112,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_addr(&ctl->full[s]), 1);
-      mbar_init(smem_addr(&ctl->empty[s]), kMc ? 2 : 1);   // one release per pair reading it
+      mbar_init(smem_addr(&ctl->empty[s]), 1);   // one release (the pair's MMA commit)
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(smem_addr(&ctl->acc_full[b]), 1);
@@ -1236,7 +1188,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 
 // ------------------------------------------------------------------ host launch side
 // Index of a pair shape in DeviceState's per-shape arrays.
-constexpr int pair_shape_index(int shape) { return shape == kShapeMc ? 1 : (shape == kShapeN224 ? 2 : 0); }
+constexpr int pair_shape_index(int shape) { return shape == kShapeN224 ? 1 : 0; }
 
 // Per-device state the launchers keep (function attributes set, co-resident clusters).
 // The host writes it only while holding its device-state lock (calls may come from several
@@ -1246,8 +1198,8 @@ struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
   bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
-  bool attr_pair[2][3][3] = {};   // [bf16 out][input kind][pair shape: standard, multicast, 224 wide]
-  int pair_clusters[3] = {};      // co-resident clusters per pair shape (0: not queried yet)
+  bool attr_pair[2][3][2] = {};   // [bf16 out][input kind][pair shape: standard, 224 wide]
+  int pair_clusters[2] = {};      // co-resident clusters per pair shape (0: not queried yet)
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
   uint32_t* status = nullptr;   // device address of the status word

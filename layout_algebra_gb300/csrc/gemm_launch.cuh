@@ -42,8 +42,7 @@ gb_status launch_single(const Maps& m, const Params& p, int grid, cudaStream_t s
 template <bool kBF16, int kIn, int kShape>
 gb_status prepare_pair(DeviceState* dev) {
   using C = gb::Cfg<true, kIn, kShape>;
-  constexpr bool kMc = kShape == kShapeMc;
-  constexpr int kCl = kMc ? 4 : 2;   // CTAs per cluster
+  constexpr int kCl = 2;   // CTAs per cluster: one pair
   bool& attr = dev->attr_pair[kBF16][kIn][pair_shape_index(kShape)];
   if (!attr) {
     if (cudaFuncSetAttribute(gb::gemm_kernel<kBF16, true, kIn, kShape>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -77,7 +76,7 @@ gb_status prepare_pair(DeviceState* dev) {
 template <bool kBF16, int kIn, int kShape>
 gb_status launch_pair(const Maps& m, const Params& p, int clusters, cudaStream_t s) {
   using C = gb::Cfg<true, kIn, kShape>;
-  constexpr int kCl = kShape == kShapeMc ? 4 : 2;
+  constexpr int kCl = 2;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCl;

@@ -133,20 +133,19 @@ using gb::Params;
 std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
-int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 3: two pairs, B multicast;
-                           // 4: single CTA with narrow tiles; 5: CTA pair with 224-column tiles
+int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 4: single CTA with
+                           // narrow tiles; 5: CTA pair with 224-column tiles (3 is not a variant)
 int g_force_schedule = 0;  // 0: stream-K when a workspace is given, the tiles are fewer than the
                            // CTAs and every CTA gets two stage-blocks; 1: data-parallel only;
                            // 2: stream-K whenever possible
 
 constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
-constexpr int kVariantPairMc = 3;   // clusters of two pairs sharing B tiles by multicast
 constexpr int kVariantNarrow = 4;   // single CTA, 128 x 64 tiles (few output columns)
 constexpr int kVariantPair224 = 5;  // CTA pair, 256 x 224 tiles (K-major B, 16-bit or FP8 inputs)
 
 bool is_pair(int variant) {
-  return variant == kVariantPair || variant == kVariantPairMc || variant == kVariantPair224;
+  return variant == kVariantPair || variant == kVariantPair224;
 }
 
 using gb::DeviceState;
@@ -271,7 +270,7 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
 
 // Kernel for a problem: a forced variant, else narrow tiles when the output has at most 64
 // columns, the CTA pair when it has more than 128 rows, the single CTA otherwise.  Block-
-// scaled inputs have no multicast or narrow form and take the pair or the single CTA.
+// scaled inputs have no narrow form and take the pair or the single CTA.
 // Tile width of a CTA pair ("CUTLASS, in depth", "Worked example: tile choice and wave
 // quantisation"): a persistent grid of G pairs runs ceil(tiles / G) waves of tiles whose time
 // is proportional to the tile width, so the 224-column tile is taken when its waves cost
@@ -298,7 +297,6 @@ int choose_variant(int64_t M, int64_t N, const InType& in, int majorB, int sms) 
     v = kVariantSingle;
   else
     v = (!in.mx && majorB == GB_K_MAJOR && prefer_pair224(M, N, sms / 2)) ? kVariantPair224 : kVariantPair;
-  if (in.mx && v == kVariantPairMc) v = kVariantPair;
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
   // 224-column tiles stage 112 B rows per CTA: K-major B only (an MN-major box is 64 wide)
   if (v == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) v = kVariantPair;
@@ -314,13 +312,11 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   if (variant != kVariantSingle && variant != kVariantNarrow && !is_pair(variant)) return GB_ERR_INVALID_ARG;
   const bool pair = is_pair(variant);
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
-  if (in.mx && (variant == kVariantPairMc || variant == kVariantNarrow)) return GB_ERR_INVALID_ARG;
+  if (in.mx && variant == kVariantNarrow) return GB_ERR_INVALID_ARG;
   if (variant == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) return GB_ERR_INVALID_ARG;
   const int64_t tile_n = tile_n_of(variant, in);
-  // B rows one copy stages: one CTA's share of one MMA's columns; with multicast each CTA
-  // copies a quarter of the pair's 256
-  int64_t rows_b = pair ? mma_n_of(variant, in) / 2 : mma_n_of(variant, in);
-  if (variant == kVariantPairMc) rows_b = gb::kSwz;
+  // B rows one copy stages: one CTA's share of one MMA's columns
+  const int64_t rows_b = pair ? mma_n_of(variant, in) / 2 : mma_n_of(variant, in);
   std::memset(pl, 0, sizeof(*pl));
   pl->variant = variant;
   pl->tile_m = tile_m;
@@ -465,8 +461,6 @@ bool epi_tma_fits(int variant, int kind) {
   using namespace gb;
   if (variant == kVariantNarrow)
     return kind == kIn8 ? Cfg<false, kIn8, kShapeNarrow>::kEpiTma : Cfg<false, kIn16, kShapeNarrow>::kEpiTma;
-  if (variant == kVariantPairMc)
-    return kind == kIn8 ? Cfg<true, kIn8, kShapeMc>::kEpiTma : Cfg<true, kIn16, kShapeMc>::kEpiTma;
   if (variant == kVariantPair224)
     return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kEpiTma : Cfg<true, kIn16, kShapeN224>::kEpiTma;
   if (is_pair(variant))
@@ -506,9 +500,7 @@ void fill_params(const DeviceState* dev, const gb_gemm_plan& pl, int64_t M, int6
   p->m_tiles = static_cast<int32_t>(pl.m_tiles);
   p->n_tiles = static_cast<int32_t>(pl.n_tiles);
   p->k_blocks = static_cast<int32_t>(pl.k_blocks);
-  // work items: tiles, or with B multicast super-tiles of two M-tiles
-  p->num_tiles = static_cast<int32_t>(
-      (pl.variant == kVariantPairMc ? (pl.m_tiles + 1) / 2 : pl.m_tiles) * pl.n_tiles);
+  p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);   // work items: output tiles
   p->group_m = is_pair(pl.variant) ? 8 : 16;
   const int kkb = is_pair(pl.variant) ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
   p->nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
@@ -534,8 +526,8 @@ void fill_params(const DeviceState* dev, const gb_gemm_plan& pl, int64_t M, int6
 }
 
 
-// Dispatch on the output type, the input kind and the pair kernels (the multicast pair and the
-// 224-column pair take 16-bit and FP8 inputs).  prepare_*_any run with g_dev_mu held.
+// Dispatch on the output type, the input kind and the pair kernels (the 224-column pair takes
+// 16-bit and FP8 inputs).  prepare_*_any run with g_dev_mu held.
 template <bool kBF16>
 gb_status prepare_single_any(int kin, bool narrow, DeviceState* dev) {
   using namespace gb;
@@ -548,8 +540,6 @@ gb_status prepare_single_any(int kin, bool narrow, DeviceState* dev) {
 template <bool kBF16>
 gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
   using namespace gb;
-  if (shape == kShapeMc)
-    return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeMc>(dev) : prepare_pair<kBF16, kIn16, kShapeMc>(dev);
   if (shape == kShapeN224)
     return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeN224>(dev) : prepare_pair<kBF16, kIn16, kShapeN224>(dev);
   if (kin == kInMx) return prepare_pair<kBF16, kInMx, kShapeStd>(dev);
@@ -567,9 +557,6 @@ gb_status launch_any(bool pair, int kin, int shape, bool narrow, const Maps& m, 
     return kin == gb::kIn8 ? launch_single<kBF16, gb::kIn8, gb::kShapeStd>(m, p, G, s)
                            : launch_single<kBF16, gb::kIn16, gb::kShapeStd>(m, p, G, s);
   }
-  if (shape == gb::kShapeMc)
-    return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeMc>(m, p, G, s)
-                           : launch_pair<kBF16, gb::kIn16, gb::kShapeMc>(m, p, G, s);
   if (shape == gb::kShapeN224)
     return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeN224>(m, p, G, s)
                            : launch_pair<kBF16, gb::kIn16, gb::kShapeN224>(m, p, G, s);
@@ -682,15 +669,14 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     if ((st = make_plan(dtype, variant, M, N, K, lda, majorA, ldb, majorB, &pl, &in)) != GB_OK) return st;
     std::memset(&maps, 0, sizeof(maps));
     if (K > 0) {
-      // CTA pairs without multicast copy a whole stage (kKB k-blocks) of an operand with one
+      // CTA pairs copy a whole stage (kKB k-blocks) of an operand with one
       // copy when K is a multiple of the k-block (and, MN-major, the operand's rows a multiple
       // of 64): fewer, larger copies keep the per-SM copy rate up (each copy costs a fixed
       // overhead).  Other operands use two-dimensional copies per k-block.
       const int64_t depth = gb::Cfg<true>::kKB;
-      const bool mc_b = pl.variant == kVariantPairMc;
       // whole k-blocks the stage-deep maps cover; a K tail is copied per k-block (tail maps)
       const int64_t kb_full = K / in.bk();
-      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224 || mc_b) &&
+      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224) &&
                                gb::Cfg<true>::kNSub == 1 && gb::Cfg<true, gb::kIn16, gb::kShapeN224>::kKB == depth && depth > 1 &&
                                kb_full >= 1;
       maps.kb_full = static_cast<int32_t>(stage_boxes ? kb_full : pl.k_blocks);
@@ -706,14 +692,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       } else if ((st = encode_map(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, dtype, in.f8)) != GB_OK) {
         return st;
       }
-      if (mc_b && stage_boxes && majorB == GB_K_MAJOR) {
-        // multicast pairs split a stage's two k-blocks of B: one 2-D copy of a CTA's 128 rows
-        const int64_t box[2] = {pl.b_box[0], gb::Cfg<true>::kRowsBSub};
-        if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, box, dtype, in.f8)) != GB_OK) return st;
-        maps.kb_boxes |= 4;
-      } else if (mc_b) {
-        if ((st = encode_map(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, dtype, in.f8)) != GB_OK) return st;
-      } else if (stage_boxes && majorB == GB_K_MAJOR) {
+      if (stage_boxes && majorB == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.b, B, pl.b_dim, pl.b_row_bytes, pl.b_box, depth, dtype, in.f8)) != GB_OK)
           return st;
         maps.kb_boxes |= 2;
@@ -769,8 +748,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.vec8_ok = (pl.d_elem_stride[1] == 1 && N % 16 == 0) ? 1 : 0;
   }
   const bool pair = is_pair(pl.variant);
-  const bool mc = pl.variant == kVariantPairMc;
-  const int shape = mc ? gb::kShapeMc : (pl.variant == kVariantPair224 ? gb::kShapeN224 : gb::kShapeStd);
+  const int shape = pl.variant == kVariantPair224 ? gb::kShapeN224 : gb::kShapeStd;
   const bool bf = dtype == GB_BF16;
   const bool narrow = pl.variant == kVariantNarrow;
   int slots;   // CTAs (clusters) that can run at once
@@ -793,7 +771,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;   // the same for every input kind
   p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
-  bool sk = !mc && workspace != nullptr && p.nsb > 0 && sched != 1;   // multicast: whole tiles
+  bool sk = workspace != nullptr && p.nsb > 0 && sched != 1;
   // default: only an under-filled GPU gains (fewer tiles than CTAs, the decode-like shapes);
   // a ragged last wave of a larger problem is cheaper than the partial-tile hand-offs (the
   // 224-column pair tiles absorb most of it), and a K too short to give every CTA two

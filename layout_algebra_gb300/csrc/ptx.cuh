@@ -340,18 +340,6 @@ __device__ __forceinline__ void bulk_wait_group() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Pair copy multicast to the CTAs of `mask` (same shared-memory offset in each).  With
-// .cta_group::2 the bytes landing in a destination CTA are counted on the barrier at
-// `bar`'s offset in the even CTA of that destination's pair (`bar` names an even CTA).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, uint32_t bar,
-                                                    int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_nctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
