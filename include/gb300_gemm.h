@@ -215,8 +215,9 @@ gb_status gb_mx_pack_scales(int operand, int64_t rows, int64_t K, const void* sr
    device share the one array and it keeps the last call's contents, so calls that may run
    at the same time on the GPU (different streams, overlapping launches) race and must not
    be issued.  The first call on each device looks up the array's device address and
-   clears its flags (a synchronous memset); make that first call before any stream
-   capture.  Other arguments, errors and ownership as for gb_gemm_f16. */
+   clears its flags (an asynchronous memset on `stream`, ahead of the call's kernel); make
+   that first call before any stream capture.  Other arguments, errors and ownership as
+   for gb_gemm_f16. */
 gb_status gb_gemm_noalloc(int dtype, int64_t M, int64_t N, int64_t K, float alpha,
                           const void* A, int64_t lda, int majorA,
                           const void* B, int64_t ldb, int majorB,

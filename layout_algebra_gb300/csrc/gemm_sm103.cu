@@ -1050,10 +1050,11 @@ extern "C" gb_status gb_gemm_noalloc(int dtype, int64_t M, int64_t N, int64_t K,
     if (g_noalloc_ptr[device] == nullptr) {
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return GB_ERR_CUDA;
-      // the hand-off flags must not hold a launch number of this process
-      if (cudaMemset(ptr, 0, static_cast<size_t>(workspace_bytes_for(dev->sms) - dev->sms * int64_t(gb::kSlotFloats) * 4)) !=
-          cudaSuccess)
-        return GB_ERR_CUDA;
+      // the hand-off flags start at zero (no launch number): the array is zero when the module
+      // loads, and is cleared once more here, in stream order before this call's kernel
+      const size_t flag_bytes =
+          static_cast<size_t>(workspace_bytes_for(dev->sms) - dev->sms * int64_t(gb::kSlotFloats) * 4);
+      if (cudaMemsetAsync(ptr, 0, flag_bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) return GB_ERR_CUDA;
       g_noalloc_ptr[device] = ptr;
     }
     scratch = g_noalloc_ptr[device];

@@ -1,9 +1,10 @@
 """GPU parity: the sm_103a GEMM through its C ABI against the fp64 oracle.
 
 Acceptance: |D - ref| <= 2^-9 (|alpha| sum|ab| + |beta c|) + one output ulp, and bit
-equality on integer-valued problems.  Full-size workloads are compared on sampled
-outputs (tile-boundary rows and columns plus seeded random entries); smaller problems
-that still span several tiles with ragged tails are compared element by element.
+equality on integer-valued problems.  Every full-size workload is compared on every
+output (the 8192^3 one in a test marked slow), and also on sampled outputs
+(tile-boundary rows and columns plus seeded random entries); smaller problems that still
+span several tiles with ragged tails are compared element by element.
 """
 import numpy as np
 import pytest
@@ -114,6 +115,36 @@ def test_ragged_workload_full_compare():
     data = W.make(p)
     D = run(p, data)
     check(p, data, D)
+
+
+def full_compare(name):
+    """Every output of a named workload against the oracle.  The oracle gets the same
+    logical A and B stored K-major (the generator draws the logical matrices before it lays
+    them out, so only the storage differs): its k loop then reads both operands
+    contiguously, which keeps a full pass of these sizes to tens of seconds on the host."""
+    p = W.WORKLOADS[name]
+    data = W.make(p)
+    D = run(p, data)
+    pk = p.with_(majorA="K", majorB="K", lda=None, ldb=None)
+    data_k = data if pk == p else W.make(pk)
+    worst = check(pk, data_k, D)
+    print("%s: worst element at %.3f of budget over all %d outputs" % (name, worst, p.M * p.N))
+
+
+def test_full_compare_4096():
+    full_compare("gemm4096_f16")
+
+
+def test_full_compare_mnmajor():
+    """16384 x 1024 x 4096 with M-major A and N-major B: every output."""
+    full_compare("gemm16384x1024x4096_mnmajor_f16")
+
+
+@pytest.mark.slow
+def test_full_compare_8192_bf16_c():
+    """8192^3 bf16 with C, every one of its 67M outputs (about 1.1e12 fp64 multiply-adds on
+    the host: minutes)."""
+    full_compare("gemm8192_bf16_c")
 
 
 # --------------------------------------------------------------------------- shapes and majors

@@ -118,3 +118,32 @@ def test_typed_gemm_integer_exact():
     ref, _ = O.gemm(M, N, K, 1.0, A, K, O.K_MAJOR, B, K, O.K_MAJOR, 0.0, None, N, O.F16,
                     a_dtype=O.E4M3, b_dtype=O.E5M2)
     assert np.array_equal(ref, (ai @ bi).astype(np.float64))
+
+
+@pytest.mark.parametrize("code,tdt,maxcode", [(O.E4M3, torch.float8_e4m3fn, 0x7E),
+                                               (O.E5M2, torch.float8_e5m2, 0x7B)])
+def test_ulp_fp8_is_the_gap_to_the_next_code(code, tdt, maxcode):
+    """ulp_fp8 (part of the FP8-output acceptance bound) equals, at every finite non-negative
+    value of the format, the distance to the next larger finite value, read off torch's own
+    float8 decoding (independent of the oracle's decoder)."""
+    b = np.arange(maxcode + 1, dtype=np.uint8)     # 0 .. the largest finite code
+    vals = torch.from_numpy(b).view(tdt).double().numpy()
+    gaps = vals[1:] - vals[:-1]
+    assert np.array_equal(O.ulp_fp8(code, vals[:-1]), gaps)
+    # the sign does not matter
+    assert np.array_equal(O.ulp_fp8(code, -vals[:-1]), gaps)
+
+
+@pytest.mark.parametrize("code,points", [
+    # OCP E4M3: 3 fraction bits, smallest normal exponent -6, largest finite 448 = 1.75 * 2^8
+    (O.E4M3, [(0.0, 2.0 ** -9), (1.0, 2.0 ** -3), (448.0, 2.0 ** 5), (2.0 ** -6, 2.0 ** -9),
+              (2.0 ** -7, 2.0 ** -9), (3.0, 2.0 ** -2)]),
+    # OCP E5M2: 2 fraction bits, smallest normal exponent -14, largest finite 57344 = 1.75 * 2^15
+    (O.E5M2, [(0.0, 2.0 ** -16), (1.0, 2.0 ** -2), (57344.0, 2.0 ** 13), (2.0 ** -14, 2.0 ** -16),
+              (2.0 ** -15, 2.0 ** -16), (3.0, 2.0 ** -1)]),
+])
+def test_ulp_fp8_values_fixed_by_the_formats(code, points):
+    """Spacings the two OCP FP8 formats fix by their field widths."""
+    r = np.array([x for x, _ in points])
+    want = np.array([u for _, u in points])
+    assert np.array_equal(O.ulp_fp8(code, r), want)

@@ -3,7 +3,9 @@
 It serves callers that may not allocate device memory while they run a GEMM, for
 instance code inside a runtime that owns all device memory or code on a path where an
 allocation would synchronise the device: its stream-K scratch is an array built into the
-library.  This checks it against the existing entry points on two calls in a row, each
+library.  The schedule is forced to stream-K here, so every call splits tiles across CTAs
+and hands fp32 partials over through that array; two calls in a row (the second one
+reading flags the first one left) are checked against the existing entry points, each
 within the acceptance bound the other GEMM tests use.  The file is named to be collected
 last, so a run that stops at the first failure has run every other test before it.
 """
@@ -20,6 +22,16 @@ pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda", 0)
 
+PROBLEMS = [
+    # few tiles: stream-K splits every tile across many CTAs
+    W.Problem("na1", 1000, 1000, 777, "bf16", has_c=True, alpha=1.25, beta=0.5, dist="normal",
+              c_dist="normal", seed=301, lda=784, ldb=784),
+    # whole tiles first, then split tiles; other majors and dtype
+    W.Problem("na2", 4100, 2056, 1536, "f16", majorA="MN", majorB="MN", has_c=True,
+              alpha=0.75, beta=1.0, dist="uniform", c_dist="normal", c_sigma=0.5, seed=302,
+              lda=4104),
+]
+
 
 def _noalloc(p, A, B, C, D):
     st = _native.lib().gb_gemm_noalloc(
@@ -32,43 +44,53 @@ def _noalloc(p, A, B, C, D):
     assert st == 0, "device status %d detail %#x" % (st, detail)
 
 
-def _bound_and_values(p, data, D):
+def _reference(p, data):
     code = O.dtype_code(p.dtype)
     C = W.bits(data["C"]) if data["C"] is not None else None
     ref, sab = O.gemm(p.M, p.N, p.K, p.alpha, W.bits(data["A"]), data["lda"],
                       G.major_code(p.majorA), W.bits(data["B"]), data["ldb"],
                       G.major_code(p.majorB), p.beta, C, p.N, code)
     c = O.decode(code, C).reshape(p.M, p.N) if C is not None else None
-    bound = O.bound(code, p.alpha, p.beta, ref, sab, c)
-    return ref, bound
+    return ref, O.bound(code, p.alpha, p.beta, ref, sab, c)
 
 
-@pytest.mark.parametrize("problems", [[
-    # few tiles: stream-K splits every tile across many CTAs
-    W.Problem("na1", 1000, 1000, 777, "bf16", has_c=True, alpha=1.25, beta=0.5, dist="normal",
-              c_dist="normal", seed=301, lda=784, ldb=784),
-    # ragged last wave of whole tiles plus split tiles, other majors and dtype
-    W.Problem("na2", 4100, 2056, 1536, "f16", majorA="MN", majorB="MN", has_c=True,
-              alpha=0.75, beta=1.0, dist="uniform", c_dist="normal", c_sigma=0.5, seed=302,
-              lda=4104),
-]])
-def test_no_alloc_matches_existing_entry_points_on_two_calls(problems):
-    workspace = G.make_workspace(DEV)
-    for p in problems:                       # two calls in a row share the built-in array
+@pytest.fixture(scope="module")
+def cases():
+    """Operands on the device and the oracle's values, once per problem."""
+    out = []
+    for p in PROBLEMS:
         data = W.make(p)
-        A, B = data["A"].to(DEV), data["B"].to(DEV)
-        C = data["C"].to(DEV) if data["C"] is not None else None
-        kw = dict(lda=data["lda"], ldb=data["ldb"], majorA=p.majorA, majorB=p.majorB,
-                  alpha=p.alpha, beta=p.beta, C=C)
-        D_ws = G.gemm(A, B, p.M, p.N, p.K, workspace=workspace, **kw)     # existing, stream-K
-        D_plain = G.gemm(A, B, p.M, p.N, p.K, **kw)                      # existing, no scratch
-        D_na = torch.full((p.M * p.N,), float("nan"), dtype=A.dtype, device=DEV)
-        _noalloc(p, A, B, C, D_na)
-        torch.cuda.synchronize()
-        code = O.dtype_code(p.dtype)
-        ref, bound = _bound_and_values(p, data, D_na)
-        got = O.decode(code, W.bits(D_na.cpu())).reshape(p.M, p.N)
-        for other in (D_ws, D_plain):
-            want = O.decode(code, W.bits(other.cpu())).reshape(p.M, p.N)
-            assert np.all(np.abs(got - want) <= bound)
-        assert np.all(np.abs(got - ref) <= bound)
+        dev = {k: data[k].to(DEV) if data[k] is not None else None for k in ("A", "B", "C")}
+        out.append((p, data, dev, _reference(p, data)))
+    return out
+
+
+@pytest.fixture
+def forced_stream_k():
+    G.set_schedule(2)          # stream-K whenever K > 0: every call uses the scratch
+    yield
+    G.set_schedule(0)
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 4, 5], ids=["auto", "single", "pair", "narrow", "pair224"])
+def test_no_alloc_matches_existing_entry_points_on_two_calls(cases, forced_stream_k, variant):
+    workspace = G.make_workspace(DEV)
+    G.set_kernel_variant(variant)
+    try:
+        for p, data, dev, (ref, bound) in cases:   # two calls in a row share the built-in array
+            A, B, C = dev["A"], dev["B"], dev["C"]
+            kw = dict(lda=data["lda"], ldb=data["ldb"], majorA=p.majorA, majorB=p.majorB,
+                      alpha=p.alpha, beta=p.beta, C=C)
+            D_ws = G.gemm(A, B, p.M, p.N, p.K, workspace=workspace, **kw)   # existing, stream-K
+            D_plain = G.gemm(A, B, p.M, p.N, p.K, **kw)                    # existing, no scratch
+            D_na = torch.full((p.M * p.N,), float("nan"), dtype=A.dtype, device=DEV)
+            _noalloc(p, A, B, C, D_na)
+            torch.cuda.synchronize()
+            code = O.dtype_code(p.dtype)
+            got = O.decode(code, W.bits(D_na.cpu())).reshape(p.M, p.N)
+            for other in (D_ws, D_plain):
+                want = O.decode(code, W.bits(other.cpu())).reshape(p.M, p.N)
+                assert np.all(np.abs(got - want) <= bound)
+            assert np.all(np.abs(got - ref) <= bound)
+    finally:
+        G.set_kernel_variant(0)
