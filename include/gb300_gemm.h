@@ -24,9 +24,10 @@
  *              GB_MN_MAJOR B(k,n) = B[k*ldb + n]   (row-major, ldb >= N)
  *   C, D (M x N): row-major, leading dimension N.  C and D have the symbol's dtype.
  *
- * Ownership and execution: every buffer is caller-owned device memory; the call
- * allocates nothing, is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
- * default stream) and returns once the kernel is queued.  The kernel is launched with
+ * Ownership and execution: every buffer is caller-owned device memory (the *_host calls
+ * below take host memory instead); the call allocates nothing, is asynchronous on
+ * `stream` (a cudaStream_t; NULL is the legacy default stream) and returns once the
+ * kernel is queued.  The kernel is launched with
  * programmatic stream serialisation: its set-up may overlap the end of the previous kernel
  * in the stream, and it touches global memory only after that kernel has completed (stream
  * order is kept for every buffer).  Calls may come from several host threads at once: the
@@ -222,6 +223,50 @@ gb_status gb_gemm_noalloc(int dtype, int64_t M, int64_t N, int64_t K, float alph
                           const void* A, int64_t lda, int majorA,
                           const void* B, int64_t ldb, int majorB,
                           float beta, const void* C, void* D, void* stream);
+
+/* The same GEMMs with every operand in HOST memory (pinned, pageable or managed; device
+   pointers are rejected with GB_ERR_INVALID_ARG): for a caller that holds its matrices on
+   the host ("Day 84: CUTLASS and CuTe layouts" — "Two programs": the harness copies the
+   operands in, runs the kernel and reads D back).  Layouts, alpha/beta, validation and
+   results are those of gb_gemm_f16 / gb_gemm_bf16 / gb_gemm_fp8 (every output equal, bit
+   for bit, to the device call's); for gb_gemm_fp8_host, epi->bias is a host array of N
+   values and epi->amax a host float, both optional.
+   Execution: B goes to the device first; then A's and C's rows go up in row blocks
+   (gb_gemm_host_row_blocks) on a copy stream while earlier blocks are multiplied on
+   `stream` and their D rows come back on a second copy stream, so the copies in both
+   directions and the GEMM overlap.  The call is asynchronous on `stream`: it returns once
+   the work is queued (with pageable buffers some copies finish before it returns), and D
+   (and *amax) hold the result once `stream` has reached the end of the call (e.g. after
+   cudaStreamSynchronize(stream)).  Work queued on `stream` before the call (e.g. writes to
+   the host operands) comes first.
+   Memory: unlike the device entry points, these calls use device staging memory owned by
+   the library: one buffer per device for A, B, C and D, allocated on the first call and
+   grown when a call needs more (growing synchronises the device), kept for later calls
+   until gb_host_staging_free().  Host-operand calls on one device share it, so each call
+   waits on the GPU for the previous one (on any stream) to release it.  Errors: those of
+   the device entry points, checked before any copy; GB_ERR_CUDA if a copy, event or
+   allocation fails. */
+gb_status gb_gemm_f16_host(int64_t M, int64_t N, int64_t K, float alpha,
+                           const void* A, int64_t lda, int majorA,
+                           const void* B, int64_t ldb, int majorB,
+                           float beta, const void* C, void* D, void* stream);
+gb_status gb_gemm_bf16_host(int64_t M, int64_t N, int64_t K, float alpha,
+                            const void* A, int64_t lda, int majorA,
+                            const void* B, int64_t ldb, int majorB,
+                            float beta, const void* C, void* D, void* stream);
+gb_status gb_gemm_fp8_host(int a_format, int b_format, int out_dtype, int64_t M, int64_t N, int64_t K,
+                           float alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+                           float beta, const void* C, void* D, const gb_epilogue* epi, void* stream);
+
+/* Row blocks of a host-operand call with M rows: *count blocks, block i = rows
+   [bounds[i], bounds[i+1]); bounds must hold 9 values.  One block when M < 2048, else up to
+   8 blocks of at least 1024 rows, each but the last a multiple of 256 rows (so every block
+   starts 16-byte aligned in A, C and D).  Pure host computation. */
+gb_status gb_gemm_host_row_blocks(int64_t M, int64_t* bounds, int* count);
+
+/* Free the current device's staging buffer of the host-operand calls (synchronises the
+   device).  The next host-operand call allocates it again. */
+gb_status gb_host_staging_free(void);
 
 /* Synchronises `stream`, then returns GB_ERR_TIMEOUT if any kernel of this library on the
    current device recorded a wait that ran out since the last call (the raw code goes to

@@ -15,7 +15,8 @@ GEMM_SYMBOLS = [
     "gb_debug_epilogue_map", "gb_debug_stage_bytes", "gb_set_kernel_variant",
     "gb_gemm_f16_ws", "gb_gemm_bf16_ws", "gb_gemm_workspace_bytes", "gb_set_schedule",
     "gb_gemm_noalloc", "gb_gemm_ex", "gb_gemm_fp8", "gb_gemm_mxfp8", "gb_mx_scales_bytes",
-    "gb_mx_pack_scales",
+    "gb_mx_pack_scales", "gb_gemm_f16_host", "gb_gemm_bf16_host", "gb_gemm_fp8_host",
+    "gb_gemm_host_row_blocks", "gb_host_staging_free",
 ]
 LAYOUT_SYMBOLS = [
     "la_error_string", "la_size", "la_cosize", "la_eval", "la_eval_coord", "la_coalesce",
@@ -62,7 +63,7 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     i64, f32, vp, ci = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int
     cp, sz = ctypes.c_char_p, ctypes.c_size_t
-    for name in ("gb_gemm_f16", "gb_gemm_bf16"):
+    for name in ("gb_gemm_f16", "gb_gemm_bf16", "gb_gemm_f16_host", "gb_gemm_bf16_host"):
         fn = getattr(L, name)
         fn.restype = ci
         fn.argtypes = [i64, i64, i64, f32, vp, i64, ci, vp, i64, ci, f32, vp, vp, vp]
@@ -79,6 +80,13 @@ def lib():
     L.gb_gemm_mxfp8.restype = ci
     L.gb_gemm_mxfp8.argtypes = [ci, ci, ci, i64, i64, i64, f32, vp, i64, vp, vp, i64, vp, f32, vp, vp,
                                 ctypes.POINTER(Epilogue), vp, sz, vp]
+    L.gb_gemm_fp8_host.restype = ci
+    L.gb_gemm_fp8_host.argtypes = [ci, ci, ci, i64, i64, i64, f32, vp, i64, vp, i64, f32, vp, vp,
+                                   ctypes.POINTER(Epilogue), vp]
+    L.gb_gemm_host_row_blocks.restype = ci
+    L.gb_gemm_host_row_blocks.argtypes = [i64, ctypes.POINTER(i64), ctypes.POINTER(ci)]
+    L.gb_host_staging_free.restype = ci
+    L.gb_host_staging_free.argtypes = []
     L.gb_mx_scales_bytes.restype = ci
     L.gb_mx_scales_bytes.argtypes = [ci, i64, i64, ctypes.POINTER(sz)]
     L.gb_mx_pack_scales.restype = ci

@@ -2,8 +2,9 @@
 
 ``gemm`` takes torch tensors holding the STORED operands (see include/gb300_gemm.h for
 the K-major / MN-major conventions) and calls gb_gemm_f16 / gb_gemm_bf16 on the current
-CUDA stream.  When the operands are host tensors the call stages them to the device with
-torch copies, runs the same C-ABI call, and copies D back into a host tensor: that is the
+CUDA stream.  When the operands are host tensors it calls gb_gemm_f16_host /
+gb_gemm_bf16_host, which stage them to the device, run the GEMM and copy D back into a
+host tensor (the row blocks and the copy/compute overlap live in the library): that is the
 end-to-end path a caller holding host buffers uses.
 """
 import ctypes
@@ -53,84 +54,32 @@ def _stream_handle(stream):
 
 
 # ----------------------------------------------------------------------------- host operands
-#
-# A call with host (pinned) operands stages them to the device and reads D back.  With
-# K-major A and enough rows, the problem is cut into row blocks of A, C and D (multiples
-# of 256 rows, so every block starts 16-byte aligned): B goes up first, then block i's A
-# and C rows go up on one copy stream while block i-1 is multiplied on the caller's stream
-# and block i-2's D rows come down on another, so the two copy directions and the GEMM
-# overlap.  Each block is one C-ABI call on the sub-matrices (M' rows, pointers offset by
-# the block's first row); a block's outputs are the same as in one call over all rows.
-
-_copy_streams = {}
 
 
-def _copy_pair(dev):
-    s = _copy_streams.get(dev.index)
-    if s is None:
-        s = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
-        _copy_streams[dev.index] = s
-    return s
+def row_blocks(M):
+    """Row blocks [m0, m1) in which a host-operand call stages A, C and D (gb_gemm_host_row_blocks)."""
+    bounds = (ctypes.c_int64 * 9)()
+    n = ctypes.c_int()
+    st = lib().gb_gemm_host_row_blocks(M, bounds, ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "row_blocks")
+    return [(bounds[i], bounds[i + 1]) for i in range(n.value)]
 
 
-def row_blocks(M, chunkable):
-    """Row blocks [m0, m1) of a host-operand call: up to 8 blocks of >= 1024 rows, each a
-    multiple of 256 rows except the last."""
-    if not chunkable or M < 2048:
-        return [(0, M)]
-    n = min(8, M // 1024)
-    rows = -(-M // n)
-    rows = -(-rows // 256) * 256
-    return [(m0, min(M, m0 + rows)) for m0 in range(0, M, rows)]
+def host_staging_free():
+    """Free this device's staging buffer of the host-operand calls."""
+    st = lib().gb_host_staging_free()
+    if st != 0:
+        raise GemmError(st, "host_staging_free")
 
 
-def _staged(M, N, A, a_row_elems, B, C, extras, D_host, out_dtype, launch, stream):
-    """Run launch(A_d, B_d, C_d, D_d, extras_d, m0, m1, s) over row blocks with host operands
-    staged to the device.  a_row_elems: elements of A per row (lda) when A's rows are
-    contiguous (K-major), else None (A goes up whole before the first block)."""
-    dev = torch.device("cuda", torch.cuda.current_device())
-    main = stream if stream is not None else torch.cuda.current_stream(dev)
-    up, down = _copy_pair(dev)
-    with torch.cuda.stream(main):
-        A_d = torch.empty(A.numel(), dtype=A.dtype, device=dev)
-        B_d = torch.empty(B.numel(), dtype=B.dtype, device=dev)
-        C_d = torch.empty(C.numel(), dtype=C.dtype, device=dev) if C is not None else None
-        D_d = torch.empty(M * N, dtype=out_dtype, device=dev)
-        ex_d = [torch.empty(t.numel(), dtype=t.dtype, device=dev) if t is not None else None
-                for t in extras]
-    if D_host is None:
-        D_host = torch.empty(M * N, dtype=out_dtype, pin_memory=True)
-    up.wait_stream(main)
-    down.wait_stream(main)
-    blocks = row_blocks(M, a_row_elems is not None)
-    with torch.cuda.stream(up):
-        B_d.copy_(B, non_blocking=True)
-        for t, t_d in zip(extras, ex_d):
-            if t is not None:
-                t_d.copy_(t, non_blocking=True)
-        if a_row_elems is None:
-            A_d.copy_(A, non_blocking=True)
-    for m0, m1 in blocks:
-        with torch.cuda.stream(up):
-            if a_row_elems is not None:
-                a0, a1 = m0 * a_row_elems, min(m1 * a_row_elems, A.numel())
-                A_d[a0:a1].copy_(A[a0:a1], non_blocking=True)
-            if C is not None:
-                C_d[m0 * N:m1 * N].copy_(C[m0 * N:m1 * N], non_blocking=True)
-            ready = torch.cuda.Event()
-            ready.record(up)
-        main.wait_event(ready)
-        launch(A_d, B_d, C_d, D_d, ex_d, m0, m1, main)
-        done = torch.cuda.Event()
-        done.record(main)
-        down.wait_event(done)
-        with torch.cuda.stream(down):
-            D_host[m0 * N:m1 * N].copy_(D_d[m0 * N:m1 * N], non_blocking=True)
-    # the caller's stream sees D on the host; the staging buffers (allocated on it) are
-    # released only after every copy that touches them
-    main.wait_stream(down)
-    main.wait_stream(up)
-    return D_host
+def _host_out(D, numel, dtype):
+    """The host tensor that receives D: the caller's, or a new pinned one."""
+    if D is None:
+        return torch.empty(numel, dtype=dtype, pin_memory=True)
+    if D.is_cuda:
+        raise TypeError("with host operands, D must be a host tensor")
+    return D
 
 
 def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0, C=None,
@@ -138,14 +87,13 @@ def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0
     """D = alpha * A @ B + beta * C.  Returns D (M*N elements, row-major).
 
     A, B, C are flat (or any contiguous) tensors of one dtype.  Device tensors: D is
-    written in place (allocated if None).  Host tensors: operands are staged to the device
-    in row blocks overlapped with the GEMM, and D (a host tensor, pinned if given so)
-    receives the result.
+    written in place (allocated if None).  Host tensors: gb_gemm_*_host stages them to the
+    device in row blocks overlapped with the GEMM, and D (a host tensor, pinned if
+    allocated here) receives the result once the stream reaches the end of the call.
     """
     dt = dtype_code(A.dtype)
     if B.dtype != A.dtype or (C is not None and C.dtype != A.dtype):
         raise TypeError("A, B and C must share one dtype")
-    esz = A.element_size()
 
     def call(A_ptr, B_ptr, C_ptr, D_ptr, rows, s):
         if workspace is None:
@@ -161,15 +109,15 @@ def gemm(A, B, M, N, K, *, lda, ldb, majorA="K", majorB="K", alpha=1.0, beta=0.0
             raise GemmError(st)
 
     if not A.is_cuda:
-        k_major_a = major_code(majorA) == K_MAJOR
-
-        def launch(A_s, B_s, C_s, D_s, _ex, m0, m1, s):
-            # block rows m0..m1: A K-major starts m0 rows of lda in (M-major A is never cut)
-            call(A_s.data_ptr() + m0 * lda * esz, B_s.data_ptr(),
-                 None if C_s is None else C_s.data_ptr() + m0 * N * esz,
-                 D_s.data_ptr() + m0 * N * esz, m1 - m0, s)
-
-        return _staged(M, N, A, lda if k_major_a else None, B, C, [], D, A.dtype, launch, stream)
+        if workspace is not None:
+            raise ValueError("host operands take no workspace")
+        D_h = _host_out(D, M * N, A.dtype)
+        fn = lib().gb_gemm_bf16_host if dt == BF16 else lib().gb_gemm_f16_host
+        st = fn(M, N, K, float(alpha), _ptr(A), lda, major_code(majorA), _ptr(B), ldb,
+                major_code(majorB), float(beta), _ptr(C), _ptr(D_h), _stream_handle(stream))
+        if st != 0:
+            raise GemmError(st, "gemm (host operands)")
+        return D_h
     D_d = D if D is not None else torch.empty(M * N, dtype=A.dtype, device=A.device)
     call(_ptr(A), _ptr(B), _ptr(C), _ptr(D_d), M, stream)
     return D_d
@@ -224,8 +172,8 @@ def gemm_fp8(A, B, M, N, K, *, lda, ldb, a_format=None, b_format=None, out_dtype
     A (M x K, leading dimension lda) and B (stored as N rows of K, leading dimension ldb) are
     K-major byte tensors: float8_e4m3fn / float8_e5m2, or uint8 codes with a_format /
     b_format naming the format.  C, D and bias are of out_dtype; per-tensor scales belong in
-    alpha.  out_format "e4m3"/"e5m2" gives a float8 D.  Host operands are staged to the
-    device and D (a host tensor, pinned if given so) receives the result, as for ``gemm``.
+    alpha.  out_format "e4m3"/"e5m2" gives a float8 D.  Host operands (with a host bias and
+    a host amax) go through gb_gemm_fp8_host, as for ``gemm``.
     """
     fa = fp8_format(a_format if a_format is not None else A.dtype)
     fb = fp8_format(b_format if b_format is not None else B.dtype)
@@ -243,16 +191,16 @@ def gemm_fp8(A, B, M, N, K, *, lda, ldb, a_format=None, b_format=None, out_dtype
             raise GemmError(st, "gemm_fp8")
 
     if not A.is_cuda:
-        csz = torch.empty(0, dtype=out_dtype).element_size()
-        dsz = torch.empty(0, dtype=dd).element_size()
-
-        def launch(A_s, B_s, C_s, D_s, ex, m0, m1, s):
-            call(A_s.data_ptr() + m0 * lda, B_s.data_ptr(),
-                 None if C_s is None else C_s.data_ptr() + m0 * N * csz,
-                 None if ex[0] is None else ex[0].data_ptr(),
-                 D_s.data_ptr() + m0 * N * dsz, m1 - m0, s)
-
-        return _staged(M, N, A, lda, B, C, [bias], D, dd, launch, stream)
+        if workspace is not None:
+            raise ValueError("host operands take no workspace")
+        D_h = _host_out(D, M * N, dd)
+        epi = Epilogue(_ptr(bias), ACTIVATIONS[activation], _ptr(amax), fmt, float(out_scale))
+        st = lib().gb_gemm_fp8_host(fa, fb, od, M, N, K, float(alpha), _ptr(A), lda, _ptr(B), ldb,
+                                    float(beta), _ptr(C), _ptr(D_h), ctypes.byref(epi),
+                                    _stream_handle(stream))
+        if st != 0:
+            raise GemmError(st, "gemm_fp8 (host operands)")
+        return D_h
     if D is None:
         D = torch.empty(M * N, dtype=dd, device=A.device)
     call(_ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(D), M, stream)

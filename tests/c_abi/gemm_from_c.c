@@ -2,7 +2,10 @@
  * A plain C caller of the GEMM C ABI (include/gb300_gemm.h): no Python, no torch.  It owns
  * its device buffers (CUDA runtime), calls gb_gemm_f16 on a stream with a K-major A and an
  * MN-major B, reads the device status word, and checks D exactly: the operands are small
- * integers, so every sum is an integer far below 2^11 and exact in fp16 and fp32.
+ * integers, so every sum is an integer far below 2^11 and exact in fp16 and fp32.  Then it
+ * calls gb_gemm_f16_host with plain malloc'd (pageable) host buffers: the same problem
+ * (D must equal the device call's bit for bit), and a taller one with an M-major A that the
+ * library stages in four row blocks, checked exactly against integer sums.
  * Exit status 0 on success.
  */
 #include <cuda_runtime_api.h>
@@ -74,6 +77,46 @@ int main(void) {
   if (gb_gemm_f16(M, N, K, 1.0f, dA, lda, GB_K_MAJOR, dB, ldb, GB_MN_MAJOR, 1.0f, NULL, dD, st) != GB_ERR_INVALID_ARG)
     return 7;
   printf("C ABI: %ld of %ld outputs wrong\n", bad, (long)(M * N));
+
+  /* host buffers: the same problem through gb_gemm_f16_host */
+  uint16_t* D2 = malloc(M * N * 2);
+  if (!D2) return 2;
+  r = gb_gemm_f16_host(M, N, K, 1.0f, A, lda, GB_K_MAJOR, B, ldb, GB_MN_MAJOR, 1.0f, C, D2, st);
+  if (r != GB_OK) { fprintf(stderr, "gb_gemm_f16_host: %s\n", gb_status_string(r)); return 8; }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return 9;
+  long diff = 0;
+  for (int64_t i = 0; i < M * N; ++i) diff += D2[i] != D[i];
+  printf("host call: %ld of %ld outputs differ from the device call\n", diff, (long)(M * N));
+  /* device pointers are refused by the host entry point */
+  if (gb_gemm_f16_host(M, N, K, 1.0f, dA, lda, GB_K_MAJOR, dB, ldb, GB_MN_MAJOR, 0.0f, NULL, D2, st) !=
+      GB_ERR_INVALID_ARG)
+    return 10;
+
+  /* a taller problem, M-major A (column-major, lda >= M2), staged in row blocks */
+  const int64_t M2 = 4352, lda2 = 4360;
+  int64_t bounds[9];
+  int nblocks = 0;
+  if (gb_gemm_host_row_blocks(M2, bounds, &nblocks) != GB_OK || nblocks != 4) return 11;
+  uint16_t *A2 = malloc(K * lda2 * 2), *C2 = malloc(M2 * N * 2), *D3 = malloc(M2 * N * 2);
+  int *a2 = malloc(M2 * K * sizeof(int)), *c2 = malloc(M2 * N * sizeof(int));
+  if (!A2 || !C2 || !D3 || !a2 || !c2) return 2;
+  for (int64_t i = 0; i < M2 * K; ++i) { s = s * 1103515245u + 12345u; a2[i] = (int)((s >> 16) % 5) - 2; }
+  for (int64_t i = 0; i < M2 * N; ++i) { s = s * 1103515245u + 12345u; c2[i] = (int)((s >> 16) % 5) - 2; }
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t m = 0; m < M2; ++m) A2[m + k * lda2] = f16_of_int(a2[m * K + k]);
+  for (int64_t i = 0; i < M2 * N; ++i) C2[i] = f16_of_int(c2[i]);
+  r = gb_gemm_f16_host(M2, N, K, 1.0f, A2, lda2, GB_MN_MAJOR, B, ldb, GB_MN_MAJOR, -1.0f, C2, D3, st);
+  if (r != GB_OK) { fprintf(stderr, "gb_gemm_f16_host (M-major): %s\n", gb_status_string(r)); return 12; }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return 13;
+  long bad2 = 0;
+  for (int64_t m = 0; m < M2; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      int want = -c2[m * N + n];
+      for (int64_t k = 0; k < K; ++k) want += a2[m * K + k] * b[k * N + n];
+      if (int_of_f16(D3[m * N + n]) != want) ++bad2;
+    }
+  printf("host call, M-major A in %d row blocks: %ld of %ld outputs wrong\n", nblocks, bad2, (long)(M2 * N));
+  if (gb_host_staging_free() != GB_OK) return 14;
   cudaFree(dA); cudaFree(dB); cudaFree(dC); cudaFree(dD); cudaStreamDestroy(st);
-  return bad == 0 ? 0 : 1;
+  return (bad == 0 && diff == 0 && bad2 == 0) ? 0 : 1;
 }

@@ -161,15 +161,16 @@ def test_gemm_call_validation_without_gpu():
 
 
 def test_host_row_blocks():
-    """Row blocks of a host-operand call: up to 8 blocks of >= 1024 rows, multiples of 256
-    rows (every block's first row keeps 16-byte alignment), covering [0, M) exactly."""
+    """Row blocks of a host-operand call (gb_gemm_host_row_blocks): up to 8 blocks of >= 1024
+    rows, multiples of 256 rows (every block's first row keeps 16-byte alignment), covering
+    [0, M) exactly."""
     from layout_algebra_gb300 import binding as G
-    assert G.row_blocks(1000, True) == [(0, 1000)]
-    assert G.row_blocks(8192, False) == [(0, 8192)]
-    assert G.row_blocks(8192, True) == [(i * 1024, (i + 1) * 1024) for i in range(8)]
-    assert G.row_blocks(5000, True) == [(0, 1280), (1280, 2560), (2560, 3840), (3840, 5000)]
+    assert G.row_blocks(1000) == [(0, 1000)]
+    assert G.row_blocks(2047) == [(0, 2047)]
+    assert G.row_blocks(8192) == [(i * 1024, (i + 1) * 1024) for i in range(8)]
+    assert G.row_blocks(5000) == [(0, 1280), (1280, 2560), (2560, 3840), (3840, 5000)]
     for M in (2048, 2049, 3000, 4097, 16384, 100000):
-        b = G.row_blocks(M, True)
+        b = G.row_blocks(M)
         assert b[0][0] == 0 and b[-1][1] == M and len(b) <= 8
         assert all(m1 == n0 for (_, m1), (n0, _) in zip(b, b[1:]))
         assert all(m0 % 256 == 0 and m1 - m0 >= 1 for m0, m1 in b)

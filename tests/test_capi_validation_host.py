@@ -116,3 +116,38 @@ def test_schedule_and_dtype_arguments():
     assert lib.gb_gemm_ex(5, 64, 64, 64, 1.0, P, 64, 0, P, 64, 0, 0.0, None, P, None, None, 0,
                           None) == INVALID
     assert lib.gb_gemm_noalloc(5, 64, 64, 64, 1.0, P, 64, 0, P, 64, 0, 0.0, None, P, None) == INVALID
+
+
+@pytest.mark.parametrize("fn", ["gb_gemm_f16_host", "gb_gemm_bf16_host"])
+@pytest.mark.parametrize("args,status", [
+    ((-1, 64, 64, 1.0, P, 64, 0, P, 64, 0, 0.0, None, P), INVALID),     # negative M
+    ((64, 64, 64, 1.0, P, 32, 0, P, 64, 0, 0.0, None, P), INVALID),     # lda < K
+    ((64, 64, 64, 1.0, P, 68, 0, P, 64, 0, 0.0, None, P), MISALIGNED),  # lda*2 not a multiple of 16
+    ((64, 64, 64, 1.0, P, 64, 0, P, 64, 2, 0.0, None, P), INVALID),     # bad major
+    ((64, 64, 64, 1.0, P, 64, 0, P, 64, 0, 1.0, None, P), INVALID),     # beta != 0 without C
+    ((64, 64, 64, 1.0, P, 64, 0, P, 64, 0, 0.0, None, None), INVALID),  # no D
+    ((64, 64, 64, 1.0, None, 64, 0, P, 64, 0, 0.0, None, P), INVALID),  # no A with K > 0
+    ((0, 64, 64, 1.0, None, 0, 0, None, 0, 0, 0.0, None, None), OK),    # empty: nothing to do
+])
+def test_host_entry_arguments(fn, args, status):
+    """The host-operand entry points check their arguments before any copy."""
+    assert getattr(_native.lib(), fn)(*args, None) == status
+
+
+def test_fp8_host_entry_arguments():
+    lib = _native.lib()
+    f = lib.gb_gemm_fp8_host
+    assert f(E4M3, 7, BF16, 64, 64, 64, 1.0, P, 64, P, 64, 0.0, None, P, None, None) == INVALID
+    assert f(E4M3, E4M3, 9, 64, 64, 64, 1.0, P, 64, P, 64, 0.0, None, P, None, None) == INVALID
+    assert f(E4M3, E4M3, BF16, 64, 64, 64, 1.0, P, 72, P, 64, 0.0, None, P, None, None) == MISALIGNED
+    assert f(E4M3, E5M2, F16, 64, 64, 64, 1.0, P, 64, P, 64, 0.0, None, P,
+             ctypes.byref(epi(out=5)), None) == INVALID
+
+
+def test_host_row_block_arguments():
+    lib = _native.lib()
+    bounds = (ctypes.c_int64 * 9)()
+    n = ctypes.c_int()
+    assert lib.gb_gemm_host_row_blocks(-1, bounds, ctypes.byref(n)) == INVALID
+    assert lib.gb_gemm_host_row_blocks(10, None, ctypes.byref(n)) == INVALID
+    assert lib.gb_gemm_host_row_blocks(10, bounds, ctypes.byref(n)) == OK and n.value == 1

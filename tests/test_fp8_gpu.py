@@ -180,3 +180,27 @@ def test_host_operands_row_blocks():
     Dd = run(p, data)
     assert not Dh.is_cuda
     assert torch.equal(Dh.view(torch.int16), Dd.cpu().view(torch.int16))
+
+
+def test_host_operands_fused_bias_amax_fp8_out():
+    """gb_gemm_fp8_host with a host bias, a host amax and an E4M3 output, in two row blocks:
+    the same bytes and amax as the device call."""
+    p = W.Problem("h8f", 2304, 272, 256, "bf16", has_c=True, alpha=0.5, beta=0.25, dist="normal",
+                  c_dist="normal", seed=212, a_fmt="e4m3", b_fmt="e4m3")
+    data = W.make(p)
+    g = torch.Generator().manual_seed(9)
+    bias = torch.randn(p.N, generator=g).to(torch.bfloat16)
+    kw = dict(lda=data["lda"], ldb=data["ldb"], a_format=p.a_fmt, b_format=p.b_fmt,
+              out_dtype=torch.bfloat16, alpha=p.alpha, beta=p.beta, activation="gelu",
+              out_format="e4m3", out_scale=4.0)
+    amax_h = torch.full((1,), 0.5, dtype=torch.float32).pin_memory()
+    Dh = G.gemm_fp8(data["A"].pin_memory(), data["B"].pin_memory(), p.M, p.N, p.K,
+                    C=data["C"].pin_memory(), bias=bias.pin_memory(), amax=amax_h, **kw)
+    torch.cuda.synchronize()
+    amax_d = torch.full((1,), 0.5, dtype=torch.float32, device=DEV)
+    Dd = G.gemm_fp8(data["A"].to(DEV), data["B"].to(DEV), p.M, p.N, p.K, C=data["C"].to(DEV),
+                    bias=bias.to(DEV), amax=amax_d, **kw)
+    torch.cuda.synchronize()
+    assert not Dh.is_cuda and Dh.dtype == torch.float8_e4m3fn
+    assert torch.equal(Dh.view(torch.uint8), Dd.cpu().view(torch.uint8))
+    assert float(amax_h.item()) == float(amax_d.item()) and float(amax_h.item()) > 0.5

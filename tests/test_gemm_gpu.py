@@ -282,24 +282,57 @@ def test_host_buffers_end_to_end():
     check(p, data, D)
 
 
-@pytest.mark.parametrize("dtype,M,majorA", [("bf16", 4096, "K"), ("f16", 5000, "K"), ("f16", 2304, "MN")])
-def test_host_buffers_row_blocks_match_device_call(dtype, M, majorA):
-    """Host operands go through the row-block staging path (A, C up and D down in blocks
-    overlapped with the GEMM); its result equals one device call over all rows."""
+@pytest.mark.parametrize("dtype,M,majorA,pinned", [("bf16", 4096, "K", True), ("f16", 5000, "K", True),
+                                                  ("f16", 2304, "MN", True), ("bf16", 4352, "MN", False),
+                                                  ("f16", 3000, "K", False)])
+def test_host_buffers_row_blocks_match_device_call(dtype, M, majorA, pinned):
+    """Host operands through gb_gemm_*_host (A, C up and D down in row blocks overlapped with
+    the GEMM, inside the library); pinned and pageable buffers, both majors of A.  The result
+    equals one device call over all rows, bit for bit."""
     N, K = 520, 200
-    lda = K if majorA == "K" else M
+    lda = K if majorA == "K" else M + 8
     p = W.Problem("e2eb", M, N, K, dtype, majorA=majorA, has_c=True, alpha=1.25, beta=0.5,
                   dist="normal", c_dist="normal", seed=M + 3, lda=lda)
     data = W.make(p)
-    assert len(G.row_blocks(M, majorA == "K")) == (1 if majorA == "MN" else min(8, M // 1024))
-    Dh = G.gemm(data["A"].pin_memory(), data["B"].pin_memory(), M, N, K, lda=lda,
-                ldb=data["ldb"], majorA=majorA, alpha=p.alpha, beta=p.beta,
-                C=data["C"].pin_memory())
+    assert len(G.row_blocks(M)) == min(8, M // 1024)
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    D_h = torch.full((M * N,), float("nan"), dtype=W.torch_dtype(dtype))
+    if pinned:
+        D_h = D_h.pin_memory()
+    Dh = G.gemm(host(data["A"]), host(data["B"]), M, N, K, lda=lda, ldb=data["ldb"], majorA=majorA,
+                alpha=p.alpha, beta=p.beta, C=host(data["C"]), D=D_h)
     torch.cuda.synchronize()
     Dd = run(p, data)
-    assert not Dh.is_cuda
+    assert Dh is D_h and not Dh.is_cuda
     assert torch.equal(Dh.view(torch.int16), Dd.cpu().view(torch.int16))
     check(p, data, Dh, *sample_entries(M, N, seed=5, n_random=4000))
+
+
+def test_host_call_ordering_on_two_streams():
+    """Host-operand calls share the library's staging buffer: calls issued back to back on
+    two streams, each with its own operands, still each get their own result."""
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    probs = [W.Problem("hs%d" % i, 2048 + 256 * i, 264, 136, "f16", has_c=True, alpha=1.0, beta=1.0,
+                       dist="int2", c_dist="int2", seed=90 + i) for i in range(4)]
+    datas = [W.make(p) for p in probs]
+    for i, (p, d) in enumerate(zip(probs, datas)):
+        outs.append(G.gemm(d["A"].pin_memory(), d["B"].pin_memory(), p.M, p.N, p.K, lda=d["lda"],
+                           ldb=d["ldb"], alpha=p.alpha, beta=p.beta, C=d["C"].pin_memory(),
+                           stream=streams[i % 2]))
+    torch.cuda.synchronize()
+    for p, d, D in zip(probs, datas, outs):
+        check(p, d, D, exact=True)
+
+
+def test_host_entry_rejects_device_pointers():
+    p = W.Problem("hd", 64, 64, 64, "f16", dist="int2", seed=3)
+    data = W.make(p)
+    A, B = data["A"].to(DEV), data["B"].to(DEV)
+    D = torch.empty(64 * 64, dtype=torch.float16)
+    st = G.lib().gb_gemm_f16_host(64, 64, 64, 1.0, A.data_ptr(), 64, 0, B.data_ptr(), 64, 0, 0.0,
+                                  None, D.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 1
 
 
 def test_device_misalignment_rejected():
