@@ -35,6 +35,12 @@ DEFAULT_WORKLOAD = "gemm8192_bf16_c"
 METRIC_MX = "GEMM TFLOP/s (2MNK/s) at 8192^3 block-scaled (MX) e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 METRIC_FP8 = "GEMM TFLOP/s (2MNK/s) at 8192^3 e4m3 inputs->fp32 acc; % of GB300 dense FP8 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published dense FP16/BF16 tensor rate of one GB300 (Blackwell Ultra) GPU: the HGX
+# B300 specification lists 36 PFLOPS FP16/BF16 for 8 GPUs, quoted with 2:4 structured
+# sparsity, i.e. 2.25 PFLOP/s dense per GPU
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_SOURCE = ("NVIDIA HGX B300 specification: FP16/BF16 tensor 36 PFLOPS per 8 GPUs with 2:4 "
+                  "sparsity = 2.25 PFLOP/s dense per GPU")
 KERNEL_SOURCES = ["layout_algebra_gb300/csrc/gemm_sm103.cu", "layout_algebra_gb300/csrc/gemm_kernel.cuh",
                   "layout_algebra_gb300/csrc/gemm_launch.cuh", "layout_algebra_gb300/csrc/gemm_inst.cu",
                   "layout_algebra_gb300/csrc/ptx.cuh"]
@@ -130,16 +136,66 @@ def barrier(world, local):
             dist.barrier()
 
 
+class NvmlReader:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes): SM clock, its
+    maximum, power draw and the clock event reasons of one GPU.  Nothing is set."""
+
+    SM = 1                          # NVML_CLOCK_SM
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, nvml_index):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(nvml_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for GPU %d" % nvml_index)
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.index = nvml_index
+        u = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, ctypes.byref(u))
+        self.max_mhz = u.value
+
+    def row(self):
+        """One sample in nvidia-smi's field order (see ClockSampler.FIELDS)."""
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, ct.byref(mhz))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        act = lambda bit: "Active" if rs.value & bit else "Not Active"   # noqa: E731
+        return [str(self.index), str(mhz.value), str(self.max_mhz), "%.2f" % (mw.value / 1000.0),
+                hex(rs.value), act(0x8), act(0x40), act(0x20), act(0x4)]
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples, each stamped with its arrival time."""
+    """Clock/throttle samples, each stamped with its arrival time: NVML queried in-process
+    every 5 ms when the driver's library loads, else nvidia-smi every 100 ms."""
 
     FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    NVML_PERIOD_S = 0.005
 
     def __init__(self, gpu_index):
         self.samples = []
         self.proc = None
+        self.source = None
+        self._stop = False
+        try:
+            self.nvml = NvmlReader(int(gpu_index))
+            self.nvml.row()
+        except (OSError, ValueError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.source = "NVML in-process, every %d ms" % round(self.NVML_PERIOD_S * 1e3)
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
@@ -147,8 +203,14 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except OSError:
             return
+        self.source = "nvidia-smi, every 100 ms"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+
+    def _poll(self):
+        while not self._stop:
+            self.samples.append((time.time(), self.nvml.row()))
+            time.sleep(self.NVML_PERIOD_S)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -157,6 +219,9 @@ class ClockSampler:
                 self.samples.append((time.time(), parts))
 
     def stop(self):
+        self._stop = True
+        if self.nvml is not None:
+            self.thread.join(timeout=1)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -185,7 +250,9 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(inside), "window": window,
-                "power_w_max": max(power) if power else None}
+                "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": max(power) if power else None,
+                "source": getattr(self, "source", None)}
 
 
 def oracle_sample(problem, data, seconds, max_rows=None):
@@ -375,7 +442,10 @@ def run_gb300(args):
     if st != 0:
         raise RuntimeError("device status %d (%#x) during warm-up" % (st, detail))
 
-    phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
+    try:   # NVML's index of this device (CUDA_VISIBLE_DEVICES taken into account)
+        phys = torch.cuda._get_nvml_device_index(dev)
+    except Exception:   # noqa: BLE001 - any failure: fall back to the variable itself
+        phys = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local if world > 1 else 0]
     sampler = ClockSampler(phys)
     time.sleep(0.3)
 
@@ -445,12 +515,14 @@ def run_gb300(args):
                               workspace=ws)
             D_h.copy_(Dd, non_blocking=True)
         elif f8:
+            # gb_gemm_fp8_host: host buffers in, D out (staging and overlap in the library)
             G.gemm_fp8(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, a_format=p.a_fmt,
                        b_format=p.b_fmt, out_dtype=out_dt, alpha=p.alpha, beta=p.beta, C=C_h,
-                       D=D_h, workspace=ws)
+                       D=D_h)
         else:
+            # gb_gemm_f16_host / gb_gemm_bf16_host
             G.gemm(A_h, B_h, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
-                   alpha=p.alpha, beta=p.beta, C=C_h, D=D_h, workspace=ws)
+                   alpha=p.alpha, beta=p.beta, C=C_h, D=D_h)
 
     for _ in range(2):
         public_call()
@@ -509,12 +581,19 @@ def run_gb300(args):
                                    % (peak_src, which, "_sustained" if capped else ""),
                     "frac_of_burst": achieved / burst,
                     "frac_of_sustained": achieved / sustained,
-                    "frac_of_nominal": achieved / (2250.0 * ratio),
+                    "frac_of_nominal": achieved / (NOMINAL_BF16_TFLOPS * ratio),
+                    "nominal_source": NOMINAL_SOURCE,
                     "frac_of_clock_peak": achieved / clock_peak, "clock_peak": clock_peak,
                     "kernel": "gb::gemm_kernel", "kernel_ms": kernel_ms,
                     **launch_stats,
                     "algorithmic_flops_per_launch": p.flops,
                     "algorithmic_bytes_per_launch": p.algorithmic_bytes}
+    if clocks.get("sm_mhz"):
+        # the kernel time in SM clock cycles at the median clock of the timed region: compares
+        # runs at different clocks (a short burst at the maximum, a long power-capped run)
+        roofline["sm_cycles_per_launch"] = kernel_ms * 1e-3 * clocks["sm_mhz"] * 1e6
+        roofline["kernel_ms_at_max_clock"] = roofline["sm_cycles_per_launch"] / (
+            (clocks.get("sm_max_mhz") or clocks["sm_mhz"]) * 1e3)
 
     line = {
         "metric": METRIC_FP8 if f8 else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -522,22 +601,27 @@ def run_gb300(args):
         "scaling": "weak", "vs_baseline": None, "dtype": p.a_fmt if f8 else p.dtype, "data": "synthetic",
         "config": workload_config(p),
         "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "entry_point": ("host copies + gb_gemm_mxfp8 (no host form)" if mx else
+                                "gb_gemm_fp8_host" if f8 else "gb_gemm_%s_host" % p.dtype)},
         "roofline": roofline, "clocks": clocks, "gpu_launches": args.steps,
     }
-    line["config"]["entry_point"] = ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
-                                     if ws is not None else "gb_gemm_%s" % p.dtype)
+    # how the timed launches were made (kept out of "config", which names the workload only
+    # and is the same in both arms)
+    path = {"entry_point": ("gb_gemm_%s_ws (workspace, stream-K where it helps)" % p.dtype
+                            if ws is not None else "gb_gemm_%s" % p.dtype)}
     if graph is not None:
-        line["config"]["launch"] = "one CUDA graph of %d launches" % args.steps
+        path["launch"] = "one CUDA graph of %d launches" % args.steps
     if mx:
-        line["config"]["entry_point"] = "gb_gemm_mxfp8" + (" (workspace)" if ws is not None else "")
-        line["config"]["scales"] = "E8M0 per 32 K elements of each row of A and column of B, codes %d..%d" % p.scale_codes
+        path["entry_point"] = "gb_gemm_mxfp8" + (" (workspace)" if ws is not None else "")
+        path["scales"] = "E8M0 per 32 K elements of each row of A and column of B, codes %d..%d" % p.scale_codes
         line["metric"] = METRIC_MX
     elif f8:
-        line["config"]["entry_point"] = "gb_gemm_fp8" + (" (workspace)" if ws is not None else "")
+        path["entry_point"] = "gb_gemm_fp8" + (" (workspace)" if ws is not None else "")
     elif epi is not None:
-        line["config"]["entry_point"] = "gb_gemm_ex"
-        line["config"]["epilogue"] = args.epilogue
+        path["entry_point"] = "gb_gemm_ex"
+        path["epilogue"] = args.epilogue
+    line["path"] = path
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(p, data, args.cpu_seconds)
         line["cpu_baseline"] = {

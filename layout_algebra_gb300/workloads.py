@@ -107,6 +107,9 @@ FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 EXTRA_WORKLOADS = {
     "gemm4096x16x4096_decode_bf16": Problem("gemm4096x16x4096_decode_bf16", 4096, 16, 4096, "bf16",
                                             dist="normal", sigma=1.0, seed=7),
+    # the 8192^3 size in fp16 without C (alpha 1, beta 0): the fp16 -> fp32 GEMM the headline
+    # metric names, beside the 8192^3 bf16 problem with C that the throughput runs use
+    "gemm8192_f16": Problem("gemm8192_f16", 8192, 8192, 8192, "f16", dist="uniform", seed=8),
 }
 
 

@@ -116,3 +116,40 @@ def test_reference_arm_json_line():
         assert k in line
     assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["value"] > 0
+
+
+def test_nvml_reader_rows_with_a_fake_library():
+    """The in-process clock sampler's row: SM clock, maximum, power in W and the four
+    reasons the bench judges, decoded from NVML's reason bits (read-only queries only)."""
+    import ctypes
+
+    class FakeNvml:
+        def __init__(self, mhz, mw, reasons):
+            self.v = (mhz, mw, reasons)
+
+        def nvmlDeviceGetClockInfo(self, h, which, out):
+            out._obj.value = self.v[0]
+            return 0
+
+        def nvmlDeviceGetPowerUsage(self, h, out):
+            out._obj.value = self.v[1]
+            return 0
+
+        def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+            out._obj.value = self.v[2]
+            return 0
+
+    r = bench.NvmlReader.__new__(bench.NvmlReader)
+    r.ct, r.h, r.index, r.max_mhz = ctypes, None, 3, 2070
+    r.lib = FakeNvml(1850, 1375500, 0x4 | 0x1)
+    r.reasons_fn = r.lib.nvmlDeviceGetCurrentClocksEventReasons
+    row = r.row()
+    assert row[:4] == ["3", "1850", "2070", "1375.50"]
+    assert row[5:] == ["Not Active", "Not Active", "Not Active", "Active"]   # power cap only
+    r.lib = FakeNvml(900, 200000, 0x8 | 0x40 | 0x20)
+    r.reasons_fn = r.lib.nvmlDeviceGetCurrentClocksEventReasons
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.samples = [(1.0, r.row())]
+    c = s.summary(0.0, 2.0)
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert c["sm_mhz"] == 900.0 and c["sm_max_mhz"] == 2070.0
