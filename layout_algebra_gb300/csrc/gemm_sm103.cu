@@ -268,9 +268,18 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
   return d;
 }
 
-// Kernel for a problem: a forced variant, else narrow tiles when the output has at most 64
-// columns, the CTA pair when it has more than 128 rows, the single CTA otherwise.  Block-
-// scaled inputs have no narrow form and take the pair or the single CTA.
+// Kernel for a problem: a forced variant, else the form that keeps the most SMs busy while
+// one wave of tiles covers the output ("CUTLASS, in depth" — "Worked example: tile choice and
+// wave quantisation": a grid smaller than the GPU leaves SMs idle):
+//   narrow 128 x 64 tiles when the output has at most 64 columns, or when its 128 x 64 tiles
+//     fit in one wave (at most one per SM): small problems, whose time is the fixed cost of a
+//     tile (set-up, the first copies' latency, the epilogue), run them on more SMs at once;
+//   the single CTA (128 x 256) when the output has at most 128 rows, or when its 128 x 256
+//     tiles fit in one wave;
+//   otherwise the CTA pair, 256 x 224 or 256 x 256 by the wave count (prefer_pair224).
+// Measured from a CUDA graph on one GB300 (default before -> after): 256^3 9.1 -> 5.5 us,
+// 512^3 10.3 -> 7.0, 1024^3 12.4 -> 10.0, 128 x 2048 x 1024 12.8 -> 9.4, 2048 x 2048 x 512
+// 12.2 -> 11.2.  Block-scaled inputs have no narrow form and take the pair or the single CTA.
 // Tile width of a CTA pair ("CUTLASS, in depth", "Worked example: tile choice and wave
 // quantisation"): a persistent grid of G pairs runs ceil(tiles / G) waves of tiles whose time
 // is proportional to the tile width, so the 224-column tile is taken when its waves cost
@@ -288,12 +297,15 @@ int choose_variant(int64_t M, int64_t N, const InType& in, int majorB, int sms) 
     std::lock_guard<std::mutex> lk(g_mu);
     forced = g_force_variant;
   }
+  const int64_t m128 = (M + gb::Cfg<false>::kTileM - 1) / gb::Cfg<false>::kTileM;
+  const int64_t narrow_tiles = m128 * ((N + gb::kNarrowTileN - 1) / gb::kNarrowTileN);
+  const int64_t single_tiles = m128 * ((N + gb::Cfg<false>::kTileN - 1) / gb::Cfg<false>::kTileN);
   int v;
   if (forced != 0)
     v = forced;
-  else if (N <= gb::kNarrowTileN)
+  else if (N <= gb::kNarrowTileN || narrow_tiles <= sms)
     v = kVariantNarrow;
-  else if (M <= gb::Cfg<false>::kTileM)
+  else if (M <= gb::Cfg<false>::kTileM || single_tiles <= sms)
     v = kVariantSingle;
   else
     v = (!in.mx && majorB == GB_K_MAJOR && prefer_pair224(M, N, sms / 2)) ? kVariantPair224 : kVariantPair;

@@ -90,10 +90,16 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
 def test_variant_choice_by_shape():
     """Default choice (a plan made without a GPU assumes 152 SMs, 76 CTA pairs)."""
     G.set_kernel_variant(0)
-    assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 1
+    # small outputs: narrow 128 x 64 tiles while they fit in one wave (one per SM)
+    assert G.plan("f16", 128, 512, 64, 64, "K", 64, "K")["variant"] == 4      # 8 tiles
+    assert G.plan("f16", 256, 256, 256, 256, "K", 256, "K")["variant"] == 4   # 8 tiles
+    assert G.plan("f16", 1024, 1216, 64, 64, "K", 64, "K")["variant"] == 4    # 8 x 19 = 152 tiles
+    # then the single CTA while its 128 x 256 tiles fit in one wave
+    assert G.plan("f16", 1024, 1280, 64, 64, "K", 64, "K")["variant"] == 1    # 160 narrow, 40 single
+    assert G.plan("f16", 2048, 2048, 512, 512, "K", 512, "K")["variant"] == 1  # 128 single tiles
+    assert G.plan("f16", 19456, 256, 64, 64, "K", 64, "K")["variant"] == 1    # 152 single tiles
     # CTA pairs: 224 columns when ceil(tiles / 76) x width is smaller than with 256
-    assert G.plan("f16", 129, 512, 64, 64, "K", 64, "K")["variant"] == 5      # 3 x 224 vs 2 x 256 tiles, 1 wave
-    assert G.plan("f16", 19456, 256, 64, 64, "K", 64, "K")["variant"] == 2    # 2 waves of 224 vs 1 of 256
+    assert G.plan("f16", 19584, 256, 64, 64, "K", 64, "K")["variant"] == 2    # 3 waves of 224 vs 2 of 256
     p = G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "K")                 # 4 waves of 224 vs 4 of 256
     assert p["variant"] == 5 and (p["m_tiles"], p["n_tiles"], p["tile_n"]) == (16, 19, 224)
     assert p["b_box"] == [64, 112] and (p["instr_desc"] >> 17) & 63 == 224 >> 3
