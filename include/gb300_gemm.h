@@ -5,16 +5,17 @@
  * K x N, C and D are M x N; 16-bit inputs (fp16 or bf16, named by the symbol), products
  * accumulated in fp32, alpha/beta applied in fp32, D rounded to nearest even.
  *
- * A CTA (or a pair of CTAs on two SMs) owns an output tile (128 x 256, or 256 x 256 for
- * a pair) and walks K in steps of 64 with A/B slices staged in shared memory ("CUTLASS,
- * in depth" — "The problem CUTLASS solves", tiling); tile and element addressing come
- * from shape:stride layouts divided into (tile, grid) modes ("Day 84: CUTLASS and CuTe
- * layouts" — "A layout is a shape and a stride").  The pair variant is used when
- * M > 128, the single-CTA variant otherwise, and narrow single-CTA tiles when N <= 64
- * (gb_set_kernel_variant overrides this).  With K-major B (16-bit or FP8 inputs), a pair
- * uses 256 x 224 tiles instead of 256 x 256 when that needs fewer tile-columns in all of its
- * persistent waves ("CUTLASS, in depth" — "Worked example: tile choice and wave
- * quantisation"): ceil(tiles / pairs) x width, pairs = half the device's SMs.
+ * A CTA (or a pair of CTAs on two SMs) owns an output tile (128 x 64 or 128 x 256 for one
+ * CTA; 256 x 224, 256 x 256 or 256 x 512 for a pair) and walks K in steps of 64 with A/B
+ * slices staged in shared memory ("CUTLASS, in depth" — "The problem CUTLASS solves",
+ * tiling); tile and element addressing come from shape:stride layouts divided into (tile,
+ * grid) modes ("Day 84: CUTLASS and CuTe layouts" — "A layout is a shape and a stride").
+ * The form is chosen by shape ("CUTLASS, in depth" — "Worked example: tile choice and wave
+ * quantisation"; gb_set_kernel_variant overrides it): narrow 128 x 64 tiles when N <= 64 or
+ * when those tiles fit in one wave (one per SM), else the single CTA when M <= 128 or its
+ * 128 x 256 tiles fit in one wave, else the pair width whose persistent waves of tiles cost
+ * least (ceil(tiles / pairs) waves, pairs = half the device's SMs, times the measured cost of
+ * a tile of that width; 224 needs K-major B).
  *
  * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
  * "One notation, and no more transposes"):
@@ -107,7 +108,7 @@ gb_status gb_gemm_bf16_ws(int64_t M, int64_t N, int64_t K, float alpha,
                           float beta, const void* C, void* D,
                           void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace size for the *_ws calls on the current device (one 128 x 256 fp32 partial and
+/* Workspace size for the *_ws calls on the current device (one 128 x 512 fp32 partial and
    one flag per SM).  GB_ERR_UNSUPPORTED_ARCH without a compute capability 10.3 device. */
 gb_status gb_gemm_workspace_bytes(size_t* bytes);
 
@@ -210,7 +211,7 @@ gb_status gb_mx_pack_scales(int operand, int64_t rows, int64_t K, const void* sr
    same result as gb_gemm_f16_ws / gb_gemm_bf16_ws (dtype = GB_F16 or GB_BF16), but its
    stream-K scratch lives in a static array inside this library instead of a caller
    workspace; it calls no allocating routine.
-   Limits and sharing: the array holds about 20 MiB (one 128 x 256 fp32 partial and one
+   Limits and sharing: the array holds about 40 MiB (one 128 x 512 fp32 partial and one
    flag for each of up to 160 SMs) and every GPU that loads the library keeps it until
    the process exits; a device with more SMs gets GB_ERR_SCRATCH_LIMIT.  All calls on a
    device share the one array and it keeps the last call's contents, so calls that may run
@@ -281,8 +282,8 @@ const char* gb_status_string(int status);
    Pure host computation (no GPU needed), same validation as the GEMM call except the
    pointer and device checks. */
 typedef struct {
-  int64_t m_tiles, n_tiles, k_blocks;   /* grid of tile_m x 256 output tiles, K steps of 64 */
-  int64_t tile_m, tile_n, tile_k;       /* 128 (single) or 256 (pair), 256, 64 */
+  int64_t m_tiles, n_tiles, k_blocks;   /* grid of tile_m x tile_n output tiles, K steps of 64 */
+  int64_t tile_m, tile_n, tile_k;       /* 128 (single) or 256 (pair); 64, 224, 256 or 512; 64 */
   int64_t a_dim[2], a_row_bytes;        /* A copy: extents (inner first), row pitch */
   int64_t a_box[2], a_boxes;            /* box extents (inner first), boxes per stage per CTA */
   int64_t b_dim[2], b_row_bytes;
@@ -291,7 +292,7 @@ typedef struct {
   int64_t d_elem_stride[2];             /* D offset step per row and per column */
   uint32_t instr_desc;                  /* tensor-core instruction descriptor */
   int32_t vector_epilogue;              /* 1 when 16-byte C/D accesses are legal */
-  int32_t variant;                      /* 1: single CTA, 2: CTA pair */
+  int32_t variant;                      /* the kernel variant (see gb_set_kernel_variant) */
 } gb_gemm_plan;
 
 gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t lda, int majorA,
@@ -306,18 +307,19 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
 gb_status gb_set_wait_timeout_ns(uint64_t ns);
 gb_status gb_debug_skip_k_block(int64_t k_block);
 
-/* Kernel variant for later calls (process-wide): 0 chooses by shape (the default: 4 when N
-   <= 64, else 1 when M <= 128, else 5 or 2 by the wave count above), 1 the single-CTA
-   128 x 256 kernel, 2 the CTA-pair 256 x 256 kernel, 4 the single-CTA kernel with narrow
-   128 x 64 tiles and eight 24 KiB stages (for outputs with few columns; with a workspace,
-   stream-K spreads K over the SMs), 5 the CTA-pair kernel with 256 x 224 tiles (K-major B;
-   with MN-major B it runs as 2).  Block-scaled FP8 has no form 4 or 5 and runs as 2
-   (M > 128) or 1.  Every variant copies each tile into one CTA only (no copy multicast).
-   GB_ERR_INVALID_ARG for other values (3 included). */
+/* Kernel variant for later calls (process-wide): 0 chooses by shape (the default, as
+   described at the top of this file), 1 the single-CTA 128 x 256 kernel, 2 the CTA-pair
+   256 x 256 kernel, 4 the single-CTA kernel with narrow 128 x 64 tiles and eight 24 KiB
+   stages (for outputs with few columns; with a workspace, stream-K spreads K over the SMs),
+   5 the CTA-pair kernel with 256 x 224 tiles (K-major B; with MN-major B it runs as 2), 6
+   the CTA-pair kernel with 256 x 512 tiles (two 256-column MMAs per k-block of A, one
+   accumulator filling Tensor Memory, eight epilogue warps).  Block-scaled FP8 has no form
+   4, 5 or 6 and runs as 2 (M > 128) or 1.  Every variant copies each tile into one CTA only
+   (no copy multicast).  GB_ERR_INVALID_ARG for other values (3 included). */
 gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2, 4 or
-   5) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2, 4, 5
+   or 6) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
    in-tile element (r, c) (r < tile_m, c < tile_n, both from gb_gemm_make_plan), or -1
    when the element lies outside M x N.  out is a device buffer of tile_m * tile_n int64.
    Asynchronous on stream. */

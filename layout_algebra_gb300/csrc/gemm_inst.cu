@@ -5,7 +5,7 @@
 #include "gemm_launch.cuh"
 
 #ifndef GB_INST_GROUP
-#error "GB_INST_GROUP must be defined (0..9)"
+#error "GB_INST_GROUP must be defined (0..11)"
 #endif
 
 namespace gb {
@@ -47,6 +47,12 @@ GB_SINGLE(true, kIn16, kShapeNarrow)
 GB_SINGLE(false, kIn16, kShapeNarrow)
 GB_SINGLE(true, kIn8, kShapeNarrow)
 GB_SINGLE(false, kIn8, kShapeNarrow)
+#elif GB_INST_GROUP == 10   // CTA pairs with 256 x 512 tiles
+GB_PAIR(true, kIn16, kShapeW512)
+GB_PAIR(false, kIn16, kShapeW512)
+#elif GB_INST_GROUP == 11
+GB_PAIR(true, kIn8, kShapeW512)
+GB_PAIR(false, kIn8, kShapeW512)
 #else
 #error "GB_INST_GROUP out of range"
 #endif

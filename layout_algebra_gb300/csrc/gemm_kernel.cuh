@@ -23,7 +23,7 @@
 namespace gb {
 
 constexpr int kBN = 256;             // N of one MMA instruction (and the single variant's tile)
-constexpr int kPairTileN = 256;      // output tile columns of the pair variant (256 or 512)
+constexpr int kWideTileN = 512;      // output tile columns of the wide CTA-pair shape
 constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
 constexpr int kRowsA = 128;          // A rows staged per CTA (one MMA's M per SM)
 constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
@@ -42,11 +42,12 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 //         the even CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared
 //         memory, and each CTA's TMEM holds its own 128 rows of the accumulator.  Each CTA
 //         stages its 128 A rows and its half of the tile's B rows, two k-blocks per stage.
-//         A 512-column tile (kPairTileN = 512) feeds two MMAs from one k-block of A; the
-//         accumulator then fills TMEM, the epilogue no longer overlaps the next tile, and
-//         eight epilogue warps (two per TMEM lane quarter) shorten it.  Measured on 8192^3
-//         the gain was eaten by the exposed epilogue, so 256-column tiles with the
-//         overlapped epilogue stay (kPairTileN is kept at 256).
+//  wide pair (kShapeW512): the pair with 256 x 512 tiles: each k-block of A feeds two MMAs
+//         of 256 columns, so a CTA copies 48 KiB per 2 x 128 x 256 x 64 MMA work instead of
+//         32 KiB per half of it (a third fewer copied bytes per flop, which is what bounds the
+//         pair's main loop).  The accumulator then fills TMEM: the epilogue of a tile does not
+//         overlap the next tile's main loop, so eight epilogue warps (two per TMEM lane
+//         quarter) share it, storing D through staging tiles and reading C into registers.
 // Input kinds: 16-bit (fp16/bf16, kind::f16), FP8 (kind::f8f6f4) and block-scaled FP8
 // (kind::mxf8f6f4 with one E8M0 scale per 32 K elements of each row of A and column of B).
 enum : int { kIn16 = 0, kIn8 = 1, kInMx = 2 };
@@ -58,9 +59,10 @@ constexpr int kMxTileN = 224;
 constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then B's two atoms
 
 // Kernel shapes: the standard tiles, narrow single-CTA tiles (128 x 64) for problems with few
-// output columns, and CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a
-// ragged last wave).  No shape loads a tile into several CTAs at once (no copy multicast).
-enum : int { kShapeStd = 0, kShapeNarrow = 1, kShapeN224 = 2 };
+// output columns, CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a
+// ragged last wave) and the wide CTA-pair tiles of 256 x 512.  No shape loads a tile into
+// several CTAs at once (no copy multicast).
+enum : int { kShapeStd = 0, kShapeNarrow = 1, kShapeN224 = 2, kShapeW512 = 3 };
 constexpr int kNarrowTileN = 64;
 
 template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
@@ -68,9 +70,10 @@ struct Cfg {
   static constexpr bool kMx = kIn == kInMx;
   static constexpr bool kNarrow = kShape == kShapeNarrow;
   static constexpr bool kN224 = kShape == kShapeN224;
+  static constexpr bool kW512 = kShape == kShapeW512;
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kTileN =
-      kNarrow ? kNarrowTileN : ((kMx || kN224) ? kMxTileN : (kPair ? kPairTileN : kBN));
+      kNarrow ? kNarrowTileN : ((kMx || kN224) ? kMxTileN : (kW512 ? kWideTileN : kBN));
   static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
   static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
   static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
@@ -91,10 +94,14 @@ struct Cfg {
   static constexpr int kSfOff = kAStage + kBStage;               // scale factors after A and B
   // stage bases stay 1024-byte aligned (the swizzle atom)
   static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
-  // Tile-store epilogue: per epilogue warp two 32 x 32 staging tiles of D and two of C
-  // (16-bit, 64-byte rows), written back / read in by tensor copies; used when it fits
+  // Tile-store epilogue: per epilogue warp two 32 x 32 staging tiles of D (16-bit, 64-byte
+  // rows) written back by tensor copies and, with two accumulators, two of C read in the same
+  // way (kEpiCTma); with one accumulator (eight epilogue warps) C is loaded into registers
+  // instead, which halves the staging.  Used when it fits.
   static constexpr int kEpiBufBytes = 32 * 64;
-  static constexpr int kEpiStageBytesFull = kEpiWarps * 4 * kEpiBufBytes;
+  static constexpr bool kEpiCTma = kAccBufs == 2;
+  static constexpr int kEpiBufsPerWarp = kEpiCTma ? 4 : 2;
+  static constexpr int kEpiStageBytesFull = kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes;
   static constexpr bool kEpiTma =
       1024 + kStages * kStageBytes + kEpiStageBytesFull + kCtlBytes <= 227 * 1024;
   static constexpr int kEpiStageBytes = kEpiTma ? kEpiStageBytesFull : 0;
@@ -107,6 +114,7 @@ struct Cfg {
   static_assert(!kMx || (kTileN <= 224 && kTileN % 32 == 0 && kBSub % 1024 == 0), "MX tile");
   static_assert(!kNarrow || (!kPair && !kMx), "narrow tiles: single CTA, 16-bit or FP8 inputs");
   static_assert(!kN224 || (kPair && !kMx), "224-column tiles: CTA pair, 16-bit or FP8 inputs");
+  static_assert(!kW512 || (kPair && !kMx && kAccBufs == 1), "512-column tiles: CTA pair, 16-bit or FP8 inputs");
 };
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -155,8 +163,9 @@ struct Params {
   int32_t epi_tma;
 };
 
-// Largest stream-K slot of any variant (floats): sizes the workspace.
-constexpr int kSlotFloats = kRowsA * (kPairTileN > kBN ? kPairTileN : kBN);
+// Largest stream-K slot of any variant (floats): sizes the workspace, and is the slot pitch of
+// every variant.
+constexpr int kSlotFloats = kRowsA * kWideTileN;
 
 struct Ctl {
   uint64_t full[kMaxStages];
@@ -573,8 +582,15 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
           }
         }
         ++kbc;
+        // K slices of this k-block that hold data: all four, except in a last k-block cut by a
+        // K that is not a multiple of the k-block, whose slices past K hold only the copy's zero
+        // fill and are skipped (they would add exact zeros)
+        const int32_t k_left = p.K - (sbk * C::kKB + h) * p.bk_elems;
+        const int32_t slice = p.bk_elems / (kBK / kUmmaK);
+        const int kslices = k_left >= p.bk_elems ? kBK / kUmmaK : (k_left + slice - 1) / slice;
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k) {
+          if (k >= kslices) break;
           const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
           const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
           // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and up to
@@ -650,10 +666,17 @@ __device__ __forceinline__ uint16_t from_f32(float v) {
     return __half_as_ushort(__float2half_rn(v));
 }
 
+// Two values rounded to nearest even and packed, lo in the low 16 bits: one paired
+// conversion instruction (the same rounding as from_f32 on each value).
 template <bool kBF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  return static_cast<uint32_t>(from_f32<kBF16>(lo)) |
-         (static_cast<uint32_t>(from_f32<kBF16>(hi)) << 16);
+  if constexpr (kBF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
 }
 
 // beta * c added to v from 32 C values held as four 16-byte words.
@@ -776,7 +799,7 @@ __device__ __forceinline__ uint32_t stage64_offset(int row, int chunk) {
 // column-major ([column][row]) so that a warp's 32 rows form one 128-byte access.
 template <bool kPair>
 __device__ __forceinline__ float* part_slot(const Params& p, uint32_t c, uint32_t rank) {
-  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * Cfg<kPair>::kSlotFloats;
+  return p.ws_part + (static_cast<int64_t>(c) * (kPair ? 2 : 1) + rank) * kSlotFloats;
 }
 
 template <bool kPair>
@@ -831,21 +854,33 @@ __device__ __forceinline__ uint32_t next_contributor(const Params& p, uint32_t G
 }
 
 // One 32-column run of the tile-store epilogue for this warp's 32 rows: C from its staging
-// tile (copied in two runs ahead), alpha/beta and the fused nodes, the 16-bit row written to
-// the D staging tile, one tensor copy of the 32 x 32 tile to D (clipped at M and N), and the
-// C staging tile refilled with the run two further on.  Returns false if a wait gave up.
+// tile (copied in two runs ahead) or from registers (reg_c: 32 values as four 16-byte words
+// loaded ahead when have_cw, else element by element from c_off), alpha/beta and the fused
+// nodes, the 16-bit row written to the D staging tile, one tensor copy of the 32 x 32 tile to D
+// (clipped at M and N), and the C staging tile refilled with the run two further on.  Returns
+// false if a wait gave up.
 template <bool kBF16, bool kPair>
 __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const uint32_t (&acc)[32], int ew,
                                                int lane, uint32_t stg, uint32_t& gr, uint32_t& c_phase,
                                                uint32_t& c_pending, bool tload_c, int run, int nruns, int32_t x0,
                                                int32_t y0, int valid, int64_t col0, float& amax, const void* tmC,
-                                               const void* tmD) {
+                                               const void* tmD, bool reg_c, bool have_cw, const uint4 (&cr)[4],
+                                               int64_t c_off) {
   constexpr uint32_t kBuf = 32 * 64;
   const uint32_t b = gr & 1u;
   const uint32_t sd = stg + b * kBuf, sc = stg + (2 + b) * kBuf;
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
+  if (reg_c) {
+    if (have_cw) {
+      add_c_words<kBF16>(p, cr, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[c_off + i * p.d_col]), v[i]);
+    }
+  }
   if (tload_c) {
     if (!wait_warp<kPair>(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, ctl, p.timeout_ns, kSiteEpiC))
       return false;
@@ -903,7 +938,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   // kept across tiles (gr), so a buffer is rewritten only once the copy that last read it
   // (two runs earlier) has finished reading.
   const bool tma = C::kEpiTma && p.epi_tma != 0;
-  const uint32_t stg = smem_addr(epi_smem) + static_cast<uint32_t>(ew) * 4u * C::kEpiBufBytes;
+  const uint32_t stg = smem_addr(epi_smem) + static_cast<uint32_t>(ew) * C::kEpiBufsPerWarp * C::kEpiBufBytes;
   // stream-K owner: this lane's column of this warp's share of the stage ring, where the
   // other CTAs' partials of a run are gathered (kPartBatch CTAs x 32 columns x 32 rows fp32)
   constexpr int kRingBytes = C::kStages * C::kStageBytes;
@@ -932,15 +967,16 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
     // tile-store path: the 32-row slab of this warp starts at row y0, its runs at x0 + 32 run
     const bool tstore = tma && !contributor;
-    const bool tload_c = tstore && p.has_c;
+    const bool tload_c = tstore && p.has_c && C::kEpiCTma;   // C by tensor copy into staging
+    const bool reg_c = tstore && p.has_c && !C::kEpiCTma;     // C into registers
     const int32_t y0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA + q * 32;
     const int32_t x0 = nt * C::kTileN + cbeg;
     // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
     // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
     // still runs; each later run is loaded kAhead runs before its use.  On the tile-store
-    // path the first two runs of C are copied into the staging tiles instead.
-    const bool cvec = !tstore && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
-    constexpr int kAhead = C::kAccBufs == 1 ? 4 : 2;
+    // path with C staging tiles the first two runs of C are copied into them instead.
+    const bool cvec = (!tstore || reg_c) && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
+    constexpr int kAhead = 2;
     uint4 cr[kAhead][4];
     if (cvec && cend > cbeg)
       prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
@@ -1013,7 +1049,8 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
           if (C::kEpiTma && tstore)
             ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
                                               nruns, x0, y0, row_ok ? min(32, cols_left - c0) : 0,
-                                              static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD);
+                                              static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD, reg_c,
+                                              cvec && c0 + 32 <= cend, cr[0], base + c0 * p.d_col);
           else if (row_ok)
             store_run<kBF16>(p, base + c0 * p.d_col, cvec && c0 + 32 <= cend, cr[0], acc,
                              min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
@@ -1188,7 +1225,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 
 // ------------------------------------------------------------------ host launch side
 // Index of a pair shape in DeviceState's per-shape arrays.
-constexpr int pair_shape_index(int shape) { return shape == kShapeN224 ? 1 : 0; }
+constexpr int pair_shape_index(int shape) { return shape == kShapeN224 ? 1 : (shape == kShapeW512 ? 2 : 0); }
 
 // Per-device state the launchers keep (function attributes set, co-resident clusters).
 // The host writes it only while holding its device-state lock (calls may come from several
@@ -1198,8 +1235,8 @@ struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
   bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
-  bool attr_pair[2][3][2] = {};   // [bf16 out][input kind][pair shape: standard, 224 wide]
-  int pair_clusters[2] = {};      // co-resident clusters per pair shape (0: not queried yet)
+  bool attr_pair[2][3][3] = {};   // [bf16 out][input kind][pair shape: standard, 224, 512 wide]
+  int pair_clusters[3] = {};      // co-resident clusters per pair shape (0: not queried yet)
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
   uint32_t* status = nullptr;   // device address of the status word

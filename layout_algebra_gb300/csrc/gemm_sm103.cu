@@ -134,7 +134,8 @@ std::mutex g_mu;
 uint64_t g_timeout_ns = gb::kDefaultTimeoutNs;
 int64_t g_skip_kb = -1;
 int g_force_variant = 0;   // 0: choose by shape; 1: single CTA; 2: CTA pair; 4: single CTA with
-                           // narrow tiles; 5: CTA pair with 224-column tiles (3 is not a variant)
+                           // narrow tiles; 5: CTA pair with 224-column tiles; 6: CTA pair with
+                           // 512-column tiles (3 is not a variant)
 int g_force_schedule = 0;  // 0: stream-K when a workspace is given, the tiles are fewer than the
                            // CTAs and every CTA gets two stage-blocks; 1: data-parallel only;
                            // 2: stream-K whenever possible
@@ -143,9 +144,10 @@ constexpr int kVariantSingle = 1;
 constexpr int kVariantPair = 2;
 constexpr int kVariantNarrow = 4;   // single CTA, 128 x 64 tiles (few output columns)
 constexpr int kVariantPair224 = 5;  // CTA pair, 256 x 224 tiles (K-major B, 16-bit or FP8 inputs)
+constexpr int kVariantPair512 = 6;  // CTA pair, 256 x 512 tiles (16-bit or FP8 inputs)
 
 bool is_pair(int variant) {
-  return variant == kVariantPair || variant == kVariantPair224;
+  return variant == kVariantPair || variant == kVariantPair224 || variant == kVariantPair512;
 }
 
 using gb::DeviceState;
@@ -199,11 +201,13 @@ InType in16(int dtype) { return InType{dtype == GB_BF16, dtype == GB_BF16, false
 int64_t tile_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
+  if (variant == kVariantPair512) return gb::Cfg<true, gb::kIn16, gb::kShapeW512>::kTileN;
   return is_pair(variant) ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
 }
 int64_t mma_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
+  if (variant == kVariantPair512) return gb::Cfg<true, gb::kIn16, gb::kShapeW512>::kMmaN;
   return is_pair(variant) ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
 }
 
@@ -276,22 +280,40 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
 //     tile (set-up, the first copies' latency, the epilogue), run them on more SMs at once;
 //   the single CTA (128 x 256) when the output has at most 128 rows, or when its 128 x 256
 //     tiles fit in one wave;
-//   otherwise the CTA pair, 256 x 224 or 256 x 256 by the wave count (prefer_pair224).
+//   otherwise the CTA pair, 256 x 224, 256 x 256 or 256 x 512 by the wave cost
+//     (choose_pair_width).
 // Measured from a CUDA graph on one GB300 (default before -> after): 256^3 9.1 -> 5.5 us,
 // 512^3 10.3 -> 7.0, 1024^3 12.4 -> 10.0, 128 x 2048 x 1024 12.8 -> 9.4, 2048 x 2048 x 512
 // 12.2 -> 11.2.  Block-scaled inputs have no narrow form and take the pair or the single CTA.
 // Tile width of a CTA pair ("CUTLASS, in depth", "Worked example: tile choice and wave
-// quantisation"): a persistent grid of G pairs runs ceil(tiles / G) waves of tiles whose time
-// is proportional to the tile width, so the 224-column tile is taken when its waves cost
-// less than the 256-column tile's (for 4096^3 on 76 pairs: 4 waves of 224 against 4 of 256).
-bool prefer_pair224(int64_t M, int64_t N, int pairs) {
-  if (pairs <= 0) return false;
+// quantisation"): a persistent grid of G pairs runs ceil(tiles / G) waves of tiles, and a tile
+// costs its k-blocks times the time of one k-block of that width, plus, for the 512-column tile
+// whose accumulator fills TMEM, the epilogue it cannot overlap.  The per-k-block times are the
+// measured ones of the three forms on a GB300 (16-bit inputs, data in L2-friendly order): 224
+// columns 0.324 us, 256 columns 0.339 us, 512 columns 0.645 us, and about 1 us of exposed
+// epilogue per 512-column tile.  The copy side bounds the narrower forms (a CTA copies 30 or 32
+// KiB per k-block for 128 x 224 or 128 x 256 outputs, 48 KiB for 128 x 512), which is why the
+// wide tile costs less per column.  For 4096^3 on 76 pairs: 4 waves of 224 (83 us) against 2 of
+// 512 (85 us); for 8192^3: 7 waves of 512 (585 us) against 14 of 256 (608 us).
+int choose_pair_width(int64_t M, int64_t N, int64_t K, int pairs, bool allow224, bool allow512) {
+  if (pairs <= 0) return kVariantPair;
   const int64_t m_tiles = (M + 255) / 256;
-  auto cost = [&](int64_t w) { return (m_tiles * ((N + w - 1) / w) + pairs - 1) / pairs * w; };
-  return cost(gb::kMxTileN) < cost(256);
+  const double k_blocks = static_cast<double>((K + gb::kBK - 1) / gb::kBK);
+  auto cost = [&](int64_t w, double per_kblock, double epi) {
+    const int64_t waves = (m_tiles * ((N + w - 1) / w) + pairs - 1) / pairs;
+    return static_cast<double>(waves) * (k_blocks * per_kblock + epi);
+  };
+  int v = kVariantPair;
+  double best = cost(256, 0.339, 0.0);
+  if (allow224 && cost(gb::kMxTileN, 0.324, 0.0) < best) {
+    v = kVariantPair224;
+    best = cost(gb::kMxTileN, 0.324, 0.0);
+  }
+  if (allow512 && cost(gb::kWideTileN, 0.645, 1.0) < best) v = kVariantPair512;
+  return v;
 }
 
-int choose_variant(int64_t M, int64_t N, const InType& in, int majorB, int sms) {
+int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorB, int sms) {
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -308,8 +330,9 @@ int choose_variant(int64_t M, int64_t N, const InType& in, int majorB, int sms) 
   else if (M <= gb::Cfg<false>::kTileM || single_tiles <= sms)
     v = kVariantSingle;
   else
-    v = (!in.mx && majorB == GB_K_MAJOR && prefer_pair224(M, N, sms / 2)) ? kVariantPair224 : kVariantPair;
+    v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR, !in.mx);
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
+  if (in.mx && v == kVariantPair512) v = kVariantPair;
   // 224-column tiles stage 112 B rows per CTA: K-major B only (an MN-major box is 64 wide)
   if (v == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) v = kVariantPair;
   return v;
@@ -326,6 +349,7 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
   if (in.mx && variant == kVariantNarrow) return GB_ERR_INVALID_ARG;
   if (variant == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) return GB_ERR_INVALID_ARG;
+  if (variant == kVariantPair512 && in.mx) return GB_ERR_INVALID_ARG;
   const int64_t tile_n = tile_n_of(variant, in);
   // B rows one copy stages: one CTA's share of one MMA's columns
   const int64_t rows_b = pair ? mma_n_of(variant, in) / 2 : mma_n_of(variant, in);
@@ -475,11 +499,28 @@ bool epi_tma_fits(int variant, int kind) {
     return kind == kIn8 ? Cfg<false, kIn8, kShapeNarrow>::kEpiTma : Cfg<false, kIn16, kShapeNarrow>::kEpiTma;
   if (variant == kVariantPair224)
     return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kEpiTma : Cfg<true, kIn16, kShapeN224>::kEpiTma;
+  if (variant == kVariantPair512)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeW512>::kEpiTma : Cfg<true, kIn16, kShapeW512>::kEpiTma;
   if (is_pair(variant))
     return kind == kInMx ? Cfg<true, kInMx>::kEpiTma
                          : (kind == kIn8 ? Cfg<true, kIn8>::kEpiTma : Cfg<true, kIn16>::kEpiTma);
   return kind == kInMx ? Cfg<false, kInMx>::kEpiTma
                        : (kind == kIn8 ? Cfg<false, kIn8>::kEpiTma : Cfg<false, kIn16>::kEpiTma);
+}
+
+// K-blocks one pipeline stage of the kernel instance of (variant, input kind) holds: the
+// stage-blocks of the schedule (and of the stream-K units) are counted in these.
+int stage_kblocks(int variant, int kind) {
+  using namespace gb;
+  if (variant == kVariantNarrow)
+    return kind == kIn8 ? Cfg<false, kIn8, kShapeNarrow>::kKB : Cfg<false, kIn16, kShapeNarrow>::kKB;
+  if (variant == kVariantPair224)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kKB : Cfg<true, kIn16, kShapeN224>::kKB;
+  if (variant == kVariantPair512)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeW512>::kKB : Cfg<true, kIn16, kShapeW512>::kKB;
+  if (is_pair(variant))
+    return kind == kInMx ? Cfg<true, kInMx>::kKB : (kind == kIn8 ? Cfg<true, kIn8>::kKB : Cfg<true, kIn16>::kKB);
+  return kind == kInMx ? Cfg<false, kInMx>::kKB : (kind == kIn8 ? Cfg<false, kIn8>::kKB : Cfg<false, kIn16>::kKB);
 }
 
 gb_status device_state(DeviceState** out) {
@@ -514,7 +555,7 @@ void fill_params(const DeviceState* dev, const gb_gemm_plan& pl, int64_t M, int6
   p->k_blocks = static_cast<int32_t>(pl.k_blocks);
   p->num_tiles = static_cast<int32_t>(pl.m_tiles * pl.n_tiles);   // work items: output tiles
   p->group_m = is_pair(pl.variant) ? 8 : 16;
-  const int kkb = is_pair(pl.variant) ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;
+  const int kkb = stage_kblocks(pl.variant, gb::kIn16);
   p->nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   p->dp_tiles = p->num_tiles;   // data-parallel unless the caller sets up stream-K
   p->bk_elems = 64;             // 16-bit inputs; 8-bit inputs set 128
@@ -554,6 +595,8 @@ gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
   using namespace gb;
   if (shape == kShapeN224)
     return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeN224>(dev) : prepare_pair<kBF16, kIn16, kShapeN224>(dev);
+  if (shape == kShapeW512)
+    return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeW512>(dev) : prepare_pair<kBF16, kIn16, kShapeW512>(dev);
   if (kin == kInMx) return prepare_pair<kBF16, kInMx, kShapeStd>(dev);
   return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeStd>(dev) : prepare_pair<kBF16, kIn16, kShapeStd>(dev);
 }
@@ -572,6 +615,9 @@ gb_status launch_any(bool pair, int kin, int shape, bool narrow, const Maps& m, 
   if (shape == gb::kShapeN224)
     return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeN224>(m, p, G, s)
                            : launch_pair<kBF16, gb::kIn16, gb::kShapeN224>(m, p, G, s);
+  if (shape == gb::kShapeW512)
+    return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeW512>(m, p, G, s)
+                           : launch_pair<kBF16, gb::kIn16, gb::kShapeW512>(m, p, G, s);
   if (kin == gb::kInMx) return launch_pair<kBF16, gb::kInMx, gb::kShapeStd>(m, p, G, s);
   return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeStd>(m, p, G, s)
                          : launch_pair<kBF16, gb::kIn16, gb::kShapeStd>(m, p, G, s);
@@ -663,7 +709,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
-  const int variant = choose_variant(M, N, in, majorB, dev->sms);
+  const int variant = choose_variant(M, N, K, in, majorB, dev->sms);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
@@ -685,12 +731,10 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
       // copy when K is a multiple of the k-block (and, MN-major, the operand's rows a multiple
       // of 64): fewer, larger copies keep the per-SM copy rate up (each copy costs a fixed
       // overhead).  Other operands use two-dimensional copies per k-block.
-      const int64_t depth = gb::Cfg<true>::kKB;
+      const int64_t depth = stage_kblocks(pl.variant, in.kind());
       // whole k-blocks the stage-deep maps cover; a K tail is copied per k-block (tail maps)
       const int64_t kb_full = K / in.bk();
-      const bool stage_boxes = (pl.variant == kVariantPair || pl.variant == kVariantPair224) &&
-                               gb::Cfg<true>::kNSub == 1 && gb::Cfg<true, gb::kIn16, gb::kShapeN224>::kKB == depth && depth > 1 &&
-                               kb_full >= 1;
+      const bool stage_boxes = is_pair(pl.variant) && depth > 1 && kb_full >= 1;
       maps.kb_full = static_cast<int32_t>(stage_boxes ? kb_full : pl.k_blocks);
       if (stage_boxes && majorA == GB_K_MAJOR) {
         if ((st = encode_map_kblocks(&maps.a, A, pl.a_dim, pl.a_row_bytes, pl.a_box, depth, dtype, in.f8)) != GB_OK)
@@ -728,7 +772,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
         // packed scales seen as rows of 256 bytes: a 512-byte atom of A per (128 rows,
         // k-block), two atoms of B per (224 columns, k-block); one copy takes a stage's kKB
         // consecutive k-blocks
-        const int64_t kkb = is_pair(pl.variant) ? gb::Cfg<true, gb::kInMx>::kKB : gb::Cfg<false, gb::kInMx>::kKB;
+        const int64_t kkb = stage_kblocks(pl.variant, gb::kInMx);
         const int64_t a_rows = 2 * ((M + 127) / 128) * pl.k_blocks;
         const int64_t b_rows = 4 * pl.n_tiles * pl.k_blocks;
         const int64_t a_dim[2] = {256, a_rows}, b_dim[2] = {256, b_rows};
@@ -760,7 +804,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     p.vec8_ok = (pl.d_elem_stride[1] == 1 && N % 16 == 0) ? 1 : 0;
   }
   const bool pair = is_pair(pl.variant);
-  const int shape = pl.variant == kVariantPair224 ? gb::kShapeN224 : gb::kShapeStd;
+  const int shape = pl.variant == kVariantPair224 ? gb::kShapeN224
+                    : (pl.variant == kVariantPair512 ? gb::kShapeW512 : gb::kShapeStd);
   const bool bf = dtype == GB_BF16;
   const bool narrow = pl.variant == kVariantNarrow;
   int slots;   // CTAs (clusters) that can run at once
@@ -781,7 +826,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
     std::lock_guard<std::mutex> lk(g_mu);
     sched = g_force_schedule;
   }
-  const int kkb = pair ? gb::Cfg<true>::kKB : gb::Cfg<false>::kKB;   // the same for every input kind
+  const int kkb = stage_kblocks(pl.variant, in.kind());
   p.nsb = static_cast<int32_t>((pl.k_blocks + kkb - 1) / kkb);
   bool sk = workspace != nullptr && p.nsb > 0 && sched != 1;
   // default: only an under-filled GPU gains (fewer tiles than CTAs, the decode-like shapes);
@@ -952,7 +997,7 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && n > 0) sms = n;
   }
   cudaGetLastError();
-  return make_plan(dtype, choose_variant(M, N, in16(dtype), majorB, sms), M, N, K, lda, majorA, ldb, majorB, plan);
+  return make_plan(dtype, choose_variant(M, N, K, in16(dtype), majorB, sms), M, N, K, lda, majorA, ldb, majorB, plan);
 }
 
 gb_status gb_set_wait_timeout_ns(uint64_t ns) {

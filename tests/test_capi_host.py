@@ -37,7 +37,7 @@ def test_status_strings():
     assert "10.3" in G.status_string(3)
 
 
-@pytest.fixture(params=[1, 2, 5], ids=["single", "pair", "pair224"])
+@pytest.fixture(params=[1, 2, 5, 6], ids=["single", "pair", "pair224", "pair512"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param
@@ -59,10 +59,11 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     want = 2 if (variant == 5 and majors[1] == "MN") else variant
     grid = grid1 if want == 1 else grid2
     tile_m = 128 if want == 1 else 256
-    tile_n = 224 if want == 5 else 256
-    if want == 5:
-        grid = (grid[0], -(-N // 224), grid[2])
-    rows_b = {1: 256, 2: 128, 3: 64, 5: 112}[want]    # B rows one copy box stages per CTA
+    tile_n = {5: 224, 6: 512}.get(want, 256)
+    if want in (5, 6):
+        grid = (grid[0], -(-N // tile_n), grid[2])
+    rows_b = {1: 256, 2: 128, 5: 112, 6: 128}[want]    # B rows one copy box stages per CTA
+    mma_n = 256 if want == 6 else tile_n                # the 512-column tile takes two MMAs
     assert p["variant"] == want and p["tile_m"] == tile_m and p["tile_n"] == tile_n
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
     # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
@@ -83,7 +84,7 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     d = p["instr_desc"]
     assert (d >> 4) & 3 == 1 and (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0
     assert (d >> 15) & 1 == (majors[0] == "MN") and (d >> 16) & 1 == (majors[1] == "MN")
-    assert (d >> 17) & 63 == tile_n >> 3 and (d >> 24) & 31 == tile_m >> 4
+    assert (d >> 17) & 63 == mma_n >> 3 and (d >> 24) & 31 == tile_m >> 4
     assert p["vector_epilogue"] == 1
 
 
@@ -98,21 +99,25 @@ def test_variant_choice_by_shape():
     assert G.plan("f16", 1024, 1280, 64, 64, "K", 64, "K")["variant"] == 1    # 160 narrow, 40 single
     assert G.plan("f16", 2048, 2048, 512, 512, "K", 512, "K")["variant"] == 1  # 128 single tiles
     assert G.plan("f16", 19456, 256, 64, 64, "K", 64, "K")["variant"] == 1    # 152 single tiles
-    # CTA pairs: 224 columns when ceil(tiles / 76) x width is smaller than with 256
+    # CTA pairs: the width whose waves of tiles cost least (per-k-block times 0.324 / 0.339 /
+    # 0.645 us for 224 / 256 / 512 columns, plus 1 us of exposed epilogue per 512-column tile)
     assert G.plan("f16", 19584, 256, 64, 64, "K", 64, "K")["variant"] == 2    # 3 waves of 224 vs 2 of 256
-    p = G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "K")                 # 4 waves of 224 vs 4 of 256
+    p = G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "K")                 # 4 x 224: 83 us, 2 x 512: 85
     assert p["variant"] == 5 and (p["m_tiles"], p["n_tiles"], p["tile_n"]) == (16, 19, 224)
     assert p["b_box"] == [64, 112] and (p["instr_desc"] >> 17) & 63 == 224 >> 3
-    assert G.plan("bf16", 8192, 8192, 8192, 8192, "K", 8192, "K")["variant"] == 2   # 16 x 224 = 14 x 256
+    p = G.plan("bf16", 8192, 8192, 8192, 8192, "K", 8192, "K")                # 7 x 512: 585 us, 14 x 256: 608
+    assert p["variant"] == 6 and (p["m_tiles"], p["n_tiles"], p["tile_n"]) == (32, 16, 512)
+    assert p["b_box"] == [64, 128] and (p["instr_desc"] >> 17) & 63 == 256 >> 3
     assert G.plan("f16", 5000, 3000, 4104, 4104, "K", 4104, "K")["variant"] == 5
-    assert G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "MN")["variant"] == 2   # MN-major B
+    assert G.plan("f16", 16384, 1024, 4096, 16384, "MN", 1024, "MN")["variant"] == 6   # 2 x 512 vs 4 x 256
+    assert G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "MN")["variant"] == 6   # MN-major B: no 224
     # at most 64 output columns: narrow 128 x 64 tiles
     p = G.plan("f16", 4096, 16, 4096, 4096, "K", 4096, "K")
     assert p["variant"] == 4 and (p["tile_m"], p["tile_n"]) == (128, 64)
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 1, 64)
     assert p["b_box"] == [64, 64] and (p["instr_desc"] >> 17) & 63 == 64 >> 3
     with pytest.raises(G.GemmError):
-        G.set_kernel_variant(6)
+        G.set_kernel_variant(7)
     # 3 was a form whose B tiles were copied into two CTA pairs at once (copy multicast); it
     # is gone, and asking for it is an argument error
     assert G.lib().gb_set_kernel_variant(3) == 1

@@ -2,8 +2,8 @@
 from several host threads at once, each on its own CUDA stream, so the library's one-time
 per-device set-up (device probe, function attributes, co-resident cluster counts) and the
 stream-K launch counter are reached concurrently.  The problems take different kernel forms
-by the default choice (single CTA, narrow tiles, CTA pair, 224-column pair, stream-K with a
-workspace).  Integer-valued operands make every output unique, so each repetition's D must
+by the default choice (single CTA, narrow tiles, CTA pair, 224- and 512-column pairs, stream-K
+with a workspace).  Integer-valued operands make every output unique, so each repetition's D must
 equal the oracle's rounded result bit for bit.  Exits non-zero on any mismatch."""
 import os
 import sys
@@ -24,18 +24,23 @@ REPEAT = 4
 
 # (problem, with a stream-K workspace, kernel form the default choice gives)
 CASES = [
-    (W.Problem("t_single", 128, 512, 64, "f16", dist="int2", seed=701), False, 1),
+    (W.Problem("t_single", 128, 9792, 64, "f16", dist="int2", seed=701), False, 1),
     (W.Problem("t_narrow", 1024, 48, 256, "bf16", dist="int2", seed=702), False, 4),
-    (W.Problem("t_pair224", 600, 700, 320, "f16", has_c=True, beta=1.0, dist="int2", c_dist="int2",
+    (W.Problem("t_pair224", 2560, 2816, 64, "f16", has_c=True, beta=1.0, dist="int2", c_dist="int2",
                seed=703), False, 5),
-    (W.Problem("t_pair", 700, 600, 200, "bf16", majorB="MN", dist="int2", seed=704), False, 2),
-    (W.Problem("t_sk_f16", 256, 512, 8192, "f16", dist="int2", seed=705), True, 5),
-    (W.Problem("t_sk_bf16", 512, 256, 8192, "bf16", has_c=True, beta=1.0, dist="int2",
-               c_dist="int2", seed=706), True, 5),
+    (W.Problem("t_pair", 2560, 2816, 64, "bf16", majorB="MN", dist="int2", seed=704), False, 2),
+    (W.Problem("t_pair512", 2560, 2048, 4096, "f16", majorB="MN", dist="int2", seed=707), False, 6),
+    (W.Problem("t_sk_f16", 256, 512, 8192, "f16", dist="int2", seed=705), True, 4),
+    (W.Problem("t_sk_bf16", 1280, 1536, 4096, "bf16", has_c=True, beta=1.0, dist="int2",
+               c_dist="int2", seed=706), True, 1),
 ]
 
 
 def expected(p, data):
+    # the oracle reads the same logical operands stored K-major (contiguous k loop)
+    pk = p.with_(majorA="K", majorB="K", lda=None, ldb=None)
+    if pk != p:
+        p, data = pk, W.make(pk)
     code = O.dtype_code(p.dtype)
     C = W.bits(data["C"]) if data["C"] is not None else None
     ref, _ = O.gemm(p.M, p.N, p.K, p.alpha, W.bits(data["A"]), data["lda"],
