@@ -294,26 +294,34 @@ uint32_t make_idesc(const InType& in, int majorA, int majorB, int tile_m, int mm
 // epilogue per 512-column tile.  The copy side bounds the narrower forms (a CTA copies 30 or 32
 // KiB per k-block for 128 x 224 or 128 x 256 outputs, 48 KiB for 128 x 512), which is why the
 // wide tile costs less per column.  For 4096^3 on 76 pairs: 4 waves of 224 (83 us) against 2 of
-// 512 (85 us); for 8192^3: 7 waves of 512 (585 us) against 14 of 256 (608 us).
-int choose_pair_width(int64_t M, int64_t N, int64_t K, int pairs, bool allow224, bool allow512) {
+// 512 (85 us); for 8192^3: 7 waves of 512 (585 us) against 14 of 256 (608 us).  A K-major
+// operand whose rows do not start on 128-byte lines (a leading dimension that is not a multiple
+// of 128 bytes: every 128-byte copy row then spans two lines) makes the copies slower, the more
+// so the more bytes a tile copies per flop: measured on 5000 x 3000 x 4104, 1.33 times the
+// per-k-block time for 224 columns and 1.29 for 512.
+int choose_pair_width(int64_t M, int64_t N, int64_t K, int pairs, bool allow224, bool allow512,
+                      bool split_rows) {
   if (pairs <= 0) return kVariantPair;
   const int64_t m_tiles = (M + 255) / 256;
   const double k_blocks = static_cast<double>((K + gb::kBK - 1) / gb::kBK);
+  const double narrow_factor = split_rows ? 1.33 : 1.0, wide_factor = split_rows ? 1.29 : 1.0;
   auto cost = [&](int64_t w, double per_kblock, double epi) {
     const int64_t waves = (m_tiles * ((N + w - 1) / w) + pairs - 1) / pairs;
     return static_cast<double>(waves) * (k_blocks * per_kblock + epi);
   };
   int v = kVariantPair;
-  double best = cost(256, 0.339, 0.0);
-  if (allow224 && cost(gb::kMxTileN, 0.324, 0.0) < best) {
+  double best = cost(256, 0.339 * narrow_factor, 0.0);
+  const double c224 = cost(gb::kMxTileN, 0.324 * narrow_factor, 0.0);
+  if (allow224 && c224 < best) {
     v = kVariantPair224;
-    best = cost(gb::kMxTileN, 0.324, 0.0);
+    best = c224;
   }
-  if (allow512 && cost(gb::kWideTileN, 0.645, 1.0) < best) v = kVariantPair512;
+  if (allow512 && cost(gb::kWideTileN, 0.645 * wide_factor, 1.0) < best) v = kVariantPair512;
   return v;
 }
 
-int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorB, int sms) {
+int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorA, int64_t lda, int majorB,
+                   int64_t ldb, int sms) {
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -330,7 +338,9 @@ int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorB
   else if (M <= gb::Cfg<false>::kTileM || single_tiles <= sms)
     v = kVariantSingle;
   else
-    v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR, !in.mx);
+    v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR, !in.mx,
+                          (majorA == GB_K_MAJOR && (lda * in.bytes) % 128 != 0) ||
+                              (majorB == GB_K_MAJOR && (ldb * in.bytes) % 128 != 0));
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
   if (in.mx && v == kVariantPair512) v = kVariantPair;
   // 224-column tiles stage 112 B rows per CTA: K-major B only (an MN-major box is 64 wide)
@@ -709,7 +719,7 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
-  const int variant = choose_variant(M, N, K, in, majorB, dev->sms);
+  const int variant = choose_variant(M, N, K, in, majorA, lda, majorB, ldb, dev->sms);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
@@ -791,6 +801,11 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   Params p;
   fill_params(dev, pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
   p.bk_elems = in.bk();
+  if (K > 0) {
+    const int64_t slice = in.bk() / (gb::kBK / gb::kUmmaK);   // K elements of one MMA instruction
+    const int64_t tail = K - (pl.k_blocks - 1) * in.bk();     // 1 .. bk elements in the last k-block
+    p.tail_kslices = static_cast<int32_t>((tail + slice - 1) / slice);
+  }
   p.kb_boxes = maps.kb_boxes;
   p.kb_full = K > 0 ? maps.kb_full : 0;
   p.epi_tma = maps.epi_tma;
@@ -997,7 +1012,8 @@ gb_status gb_gemm_make_plan(int dtype, int64_t M, int64_t N, int64_t K, int64_t 
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) == cudaSuccess && n > 0) sms = n;
   }
   cudaGetLastError();
-  return make_plan(dtype, choose_variant(M, N, K, in16(dtype), majorB, sms), M, N, K, lda, majorA, ldb, majorB, plan);
+  return make_plan(dtype, choose_variant(M, N, K, in16(dtype), majorA, lda, majorB, ldb, sms), M, N, K, lda, majorA,
+                   ldb, majorB, plan);
 }
 
 gb_status gb_set_wait_timeout_ns(uint64_t ns) {
