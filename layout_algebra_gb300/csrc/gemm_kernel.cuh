@@ -857,19 +857,32 @@ __device__ __forceinline__ uint32_t next_contributor(const Params& p, uint32_t G
   return c;
 }
 
+// The 32 x 32 block of C at rows y0.., columns x.. as a warp loads it with coalesced 16-byte
+// loads: lane l takes, in slice i, row y0 + 8 i + l / 4 at columns x + 8 (l % 4) .. + 7 (zeros
+// outside M x N; N is a multiple of 8).  Each load instruction covers 8 whole 64-byte row
+// segments, where one row per lane would touch 32 lines per instruction.
+__device__ __forceinline__ void load_c_slab(const Params& p, int32_t y0, int32_t x, int lane, uint4 (&cr)[4]) {
+  const int32_t row = y0 + (lane >> 2), col = x + 8 * (lane & 3);
+  const uint4* src = reinterpret_cast<const uint4*>(p.C + static_cast<int64_t>(row) * p.d_row + col);
+  const int64_t step = p.d_row;   // 8 rows, in 16-byte words (d_row halves / 8 per word)
+  const int32_t rows_left = col < p.N ? p.M - row : 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    cr[i] = 8 * i < rows_left ? __ldg(src + i * step) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 // One 32-column run of the tile-store epilogue for this warp's 32 rows: C from its staging
-// tile (copied in two runs ahead) or from registers (reg_c: 32 values as four 16-byte words
-// loaded ahead when have_cw, else element by element from c_off), alpha/beta and the fused
-// nodes, the 16-bit row written to the D staging tile, one tensor copy of the 32 x 32 tile to D
-// (clipped at M and N), and the C staging tile refilled with the run two further on.  Returns
-// false if a wait gave up.
+// tile (copied in two runs ahead) or from a slab of registers (reg_c: loaded ahead by
+// load_c_slab, passed through the D staging tile to give each lane its row), alpha/beta and the
+// fused nodes, the 16-bit row written to the D staging tile, one tensor copy of the 32 x 32 tile
+// to D (clipped at M and N), and the C staging tile refilled with the run two further on.
+// Returns false if a wait gave up.
 template <bool kBF16, bool kPair>
 __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const uint32_t (&acc)[32], int ew,
                                                int lane, uint32_t stg, uint32_t& gr, uint32_t& c_phase,
                                                uint32_t& c_pending, bool tload_c, int run, int nruns, int32_t x0,
                                                int32_t y0, int valid, int64_t col0, float& amax, const void* tmC,
-                                               const void* tmD, bool reg_c, bool have_cw, const uint4 (&cr)[4],
-                                               int64_t c_off) {
+                                               const void* tmD, bool reg_c, const uint4 (&cr)[4]) {
   constexpr uint32_t kBuf = 32 * 64;
   const uint32_t b = gr & 1u;
   const uint32_t sd = stg + b * kBuf, sc = stg + (2 + b) * kBuf;
@@ -877,13 +890,18 @@ __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const 
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
   if (reg_c) {
-    if (have_cw) {
-      add_c_words<kBF16>(p, cr, v);
-    } else {
+    // the D staging tile is free once the copy that last read it (two runs back) is done; the C
+    // slab goes through it, and every lane has read its row back before D is written there
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < valid) v[i] = fmaf(p.beta, to_f32<kBF16>(p.C[c_off + i * p.d_col]), v[i]);
-    }
+    for (int i = 0; i < 4; ++i) st_shared_u4(sd + stage64_offset(8 * i + (lane >> 2), lane & 3), cr[i]);
+    __syncwarp();
+    uint4 cw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cw[j] = ld_shared_u4(sd + stage64_offset(lane, j));
+    add_c_words<kBF16>(p, cw, v);
+    __syncwarp();
   }
   if (tload_c) {
     if (!wait_warp<kPair>(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, ctl, p.timeout_ns, kSiteEpiC))
@@ -977,20 +995,25 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const int32_t x0 = nt * C::kTileN + cbeg;
     // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
     // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
-    // still runs; each later run is loaded kAhead runs before its use.  On the tile-store
-    // path with C staging tiles the first two runs of C are copied into them instead.
-    const bool cvec = (!tstore || reg_c) && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
-    constexpr int kAhead = 2;
+    // still runs; each later run is loaded kAhead runs before its use (on the tile-store path
+    // with register C as coalesced slabs, else one row per lane).  On the tile-store path with
+    // C staging tiles the first two runs of C are copied into them instead.
+    const bool cvec = !tstore && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
+    // (register C of the wide tile: one run ahead, which keeps it within the 168 registers a
+    // thread of its 320 has; two ahead spilled and measured slower)
+    constexpr int kAhead = C::kEpiCTma ? 2 : 1;
     uint4 cr[kAhead][4];
-    if (cvec && cend > cbeg)
+    if ((cvec || reg_c) && row_ok && cend > cbeg)
       prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
 #pragma unroll
-    for (int a = 0; a < kAhead; ++a)
+    for (int a = 0; a < kAhead; ++a) {
+      if (reg_c && cbeg + 32 * a < cend) load_c_slab(p, y0, x0 + 32 * a, lane, cr[a]);
       if (cvec && cbeg + 32 * a + 32 <= cend) {
         const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg + 32 * a);
 #pragma unroll
         for (int j = 0; j < 4; ++j) cr[a][j] = __ldg(src + j);
       }
+    }
     if constexpr (C::kEpiTma) {
       if (tload_c && lane == 0) {
         for (int a = 0; a < 2 && a < nruns; ++a) {
@@ -1054,7 +1077,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
             ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
                                               nruns, x0, y0, row_ok ? min(32, cols_left - c0) : 0,
                                               static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD, reg_c,
-                                              cvec && c0 + 32 <= cend, cr[0], base + c0 * p.d_col);
+                                              cr[0]);
           else if (row_ok)
             store_run<kBF16>(p, base + c0 * p.d_col, cvec && c0 + 32 <= cend, cr[0], acc,
                              min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
@@ -1065,6 +1088,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
             for (int j = 0; j < 4; ++j) cr[a][j] = cr[a + 1][j];
           const int cn0 = c0 + 32 * kAhead;
+          if (reg_c && cn0 < cend) load_c_slab(p, y0, x0 + (cn0 - cbeg), lane, cr[kAhead - 1]);
           if (cvec && cn0 + 32 <= cend) {
             const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
 #pragma unroll
