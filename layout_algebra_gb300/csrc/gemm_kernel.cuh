@@ -161,8 +161,6 @@ struct Params {
   // 1: the epilogue stages each 32 x 32 run of D in shared memory and writes it with a
   // tensor copy (tmD), and reads C the same way (tmC); 16-bit D, row-major, N % 8 == 0
   int32_t epi_tma;
-  // MMA instructions (32-byte K slices, 1..4) of the last k-block that reach elements below K
-  int32_t tail_kslices;
 };
 
 // Largest stream-K slot of any variant (floats): sizes the workspace, and is the slot pitch of
@@ -584,11 +582,12 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
           }
         }
         ++kbc;
-        // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and up to
-        // 256 columns; the N sub-tiles share the A slice
-        auto issue_slice = [&](int k) {
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k) {
           const uint64_t da = da0 + ((h * C::kAHalf) >> 4) + k * ka;
           const uint32_t acc = (sbk != item.sb0 || h != 0 || k != 0) ? 1u : 0u;
+          // one instruction covers 32 bytes of K (16 16-bit or 32 8-bit elements) and up to
+          // 256 columns; the N sub-tiles share the A slice
 #pragma unroll
           for (int j = 0; j < C::kNSub; ++j) {
             const uint64_t db = db0 + ((h * C::kBHalf + j * C::kBSub) >> 4) + k * kb_;
@@ -610,16 +609,6 @@ __device__ void run_mma(const Params& p, uint8_t* smem, Ctl* ctl, uint32_t tmem_
               tc_mma_f16(dt, da, db, p.idesc, acc);
             }
           }
-        };
-        if (sbk * C::kKB + h != p.k_blocks - 1) {
-#pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) issue_slice(k);
-        } else {
-          // the last k-block: when K is not a multiple of the k-block its K slices past K hold
-          // only the copy's zero fill and are skipped (they would add exact zeros)
-#pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            if (k < p.tail_kslices) issue_slice(k);
         }
       }
       issued_any = true;

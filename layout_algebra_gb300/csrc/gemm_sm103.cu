@@ -804,11 +804,6 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   Params p;
   fill_params(dev, pl, M, N, K, alpha, majorA, majorB, beta, C, D, &p);
   p.bk_elems = in.bk();
-  if (K > 0) {
-    const int64_t slice = in.bk() / (gb::kBK / gb::kUmmaK);   // K elements of one MMA instruction
-    const int64_t tail = K - (pl.k_blocks - 1) * in.bk();     // 1 .. bk elements in the last k-block
-    p.tail_kslices = static_cast<int32_t>((tail + slice - 1) / slice);
-  }
   p.kb_boxes = maps.kb_boxes;
   p.kb_full = K > 0 ? maps.kb_full : 0;
   p.epi_tma = maps.epi_tma;
