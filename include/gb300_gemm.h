@@ -6,7 +6,7 @@
  * accumulated in fp32, alpha/beta applied in fp32, D rounded to nearest even.
  *
  * A CTA (or a pair of CTAs on two SMs) owns an output tile (128 x 64 or 128 x 256 for one
- * CTA; 256 x 224, 256 x 256 or 256 x 512 for a pair) and walks K in steps of 64 with A/B
+ * CTA; 256 x 224, 256 x 256, 256 x 448 or 256 x 512 for a pair) and walks K in steps of 64 with A/B
  * slices staged in shared memory ("CUTLASS, in depth" — "The problem CUTLASS solves",
  * tiling); tile and element addressing come from shape:stride layouts divided into (tile,
  * grid) modes ("Day 84: CUTLASS and CuTe layouts" — "A layout is a shape and a stride").
@@ -283,7 +283,7 @@ const char* gb_status_string(int status);
    pointer and device checks. */
 typedef struct {
   int64_t m_tiles, n_tiles, k_blocks;   /* grid of tile_m x tile_n output tiles, K steps of 64 */
-  int64_t tile_m, tile_n, tile_k;       /* 128 (single) or 256 (pair); 64, 224, 256 or 512; 64 */
+  int64_t tile_m, tile_n, tile_k;       /* 128 (single) or 256 (pair); 64, 224, 256, 448 or 512; 64 */
   int64_t a_dim[2], a_row_bytes;        /* A copy: extents (inner first), row pitch */
   int64_t a_box[2], a_boxes;            /* box extents (inner first), boxes per stage per CTA */
   int64_t b_dim[2], b_row_bytes;
@@ -313,13 +313,14 @@ gb_status gb_debug_skip_k_block(int64_t k_block);
    stages (for outputs with few columns; with a workspace, stream-K spreads K over the SMs),
    5 the CTA-pair kernel with 256 x 224 tiles (K-major B; with MN-major B it runs as 2), 6
    the CTA-pair kernel with 256 x 512 tiles (two 256-column MMAs per k-block of A, one
-   accumulator filling Tensor Memory, eight epilogue warps).  Block-scaled FP8 has no form
-   4, 5 or 6 and runs as 2 (M > 128) or 1.  Every variant copies each tile into one CTA only
+   accumulator filling Tensor Memory, eight epilogue warps), 7 the same with 256 x 448 tiles
+   (two 224-column MMAs; K-major B; with MN-major B it runs as 6).  Block-scaled FP8 has no
+   form 4, 5, 6 or 7 and runs as 2 (M > 128) or 1.  Every variant copies each tile into one CTA only
    (no copy multicast).  GB_ERR_INVALID_ARG for other values (3 included). */
 gb_status gb_set_kernel_variant(int variant);
 
-/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2, 4, 5
-   or 6) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
+/* Test hook: evaluate, on the device, the D-offset map the epilogue of `variant` (1, 2, 4, 5,
+   6 or 7) uses for tile (m_tile, n_tile) of an M x N problem: out[r*tile_n + c] = offset of
    in-tile element (r, c) (r < tile_m, c < tile_n, both from gb_gemm_make_plan), or -1
    when the element lies outside M x N.  out is a device buffer of tile_m * tile_n int64.
    Asynchronous on stream. */

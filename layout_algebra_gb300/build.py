@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["layout.cpp", "layout_capi.cpp", "host_staging.cpp", "gemm_sm103.cu", "gemm_inst.cu"]
 HEADERS = ["layout.hpp", "ptx.cuh", "gemm_kernel.cuh", "gemm_launch.cuh"]
-INST_GROUPS = 12   # GB_INST_GROUP values of gemm_inst.cu
+INST_GROUPS = 14   # GB_INST_GROUP values of gemm_inst.cu
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -5,7 +5,7 @@
 #include "gemm_launch.cuh"
 
 #ifndef GB_INST_GROUP
-#error "GB_INST_GROUP must be defined (0..11)"
+#error "GB_INST_GROUP must be defined (0..13)"
 #endif
 
 namespace gb {
@@ -53,6 +53,12 @@ GB_PAIR(false, kIn16, kShapeW512)
 #elif GB_INST_GROUP == 11
 GB_PAIR(true, kIn8, kShapeW512)
 GB_PAIR(false, kIn8, kShapeW512)
+#elif GB_INST_GROUP == 12   // CTA pairs with 256 x 448 tiles
+GB_PAIR(true, kIn16, kShapeW448)
+GB_PAIR(false, kIn16, kShapeW448)
+#elif GB_INST_GROUP == 13
+GB_PAIR(true, kIn8, kShapeW448)
+GB_PAIR(false, kIn8, kShapeW448)
 #else
 #error "GB_INST_GROUP out of range"
 #endif

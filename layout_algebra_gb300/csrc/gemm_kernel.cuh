@@ -24,6 +24,7 @@ namespace gb {
 
 constexpr int kBN = 256;             // N of one MMA instruction (and the single variant's tile)
 constexpr int kWideTileN = 512;      // output tile columns of the wide CTA-pair shape
+constexpr int kWide448TileN = 448;   // ... and of its 2 x 224-column form (K-major B)
 constexpr int kBK = 64;              // one 128-byte swizzle row of 16-bit elements
 constexpr int kRowsA = 128;          // A rows staged per CTA (one MMA's M per SM)
 constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
@@ -42,8 +43,8 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 //         the even CTA issues tcgen05.mma.cta_group::2 (M = 256) reading both CTAs' shared
 //         memory, and each CTA's TMEM holds its own 128 rows of the accumulator.  Each CTA
 //         stages its 128 A rows and its half of the tile's B rows, two k-blocks per stage.
-//  wide pair (kShapeW512): the pair with 256 x 512 tiles: each k-block of A feeds two MMAs
-//         of 256 columns, so a CTA copies 48 KiB per 2 x 128 x 256 x 64 MMA work instead of
+//  wide pair (kShapeW512, kShapeW448): the pair with 256 x 512 (or 256 x 448) tiles: each
+//         k-block of A feeds two MMAs of 256 (224) columns, so a CTA copies 48 KiB per 2 x 128 x 256 x 64 MMA work instead of
 //         32 KiB per half of it (a third fewer copied bytes per flop, which is what bounds the
 //         pair's main loop).  The accumulator then fills TMEM: the epilogue of a tile does not
 //         overlap the next tile's main loop, so eight epilogue warps (two per TMEM lane
@@ -60,9 +61,9 @@ constexpr int kMxSfBytes = 512 + 1024;   // one k-block's scales: A's atom, then
 
 // Kernel shapes: the standard tiles, narrow single-CTA tiles (128 x 64) for problems with few
 // output columns, CTA-pair tiles of 256 x 224 (for problems whose 256-column tiles leave a
-// ragged last wave) and the wide CTA-pair tiles of 256 x 512.  No shape loads a tile into
-// several CTAs at once (no copy multicast).
-enum : int { kShapeStd = 0, kShapeNarrow = 1, kShapeN224 = 2, kShapeW512 = 3 };
+// ragged last wave) and the wide CTA-pair tiles of 256 x 512 and 256 x 448.  No shape loads a
+// tile into several CTAs at once (no copy multicast).
+enum : int { kShapeStd = 0, kShapeNarrow = 1, kShapeN224 = 2, kShapeW512 = 3, kShapeW448 = 4 };
 constexpr int kNarrowTileN = 64;
 
 template <bool kPair, int kIn = kIn16, int kShape = kShapeStd>
@@ -71,10 +72,12 @@ struct Cfg {
   static constexpr bool kNarrow = kShape == kShapeNarrow;
   static constexpr bool kN224 = kShape == kShapeN224;
   static constexpr bool kW512 = kShape == kShapeW512;
+  static constexpr bool kW448 = kShape == kShapeW448;
   static constexpr int kTileM = kPair ? 256 : 128;
   static constexpr int kTileN =
-      kNarrow ? kNarrowTileN : ((kMx || kN224) ? kMxTileN : (kW512 ? kWideTileN : kBN));
-  static constexpr int kNSub = kTileN > kBN ? kTileN / kBN : 1;   // MMAs per K step (along N)
+      kNarrow ? kNarrowTileN
+              : ((kMx || kN224) ? kMxTileN : (kW512 ? kWideTileN : (kW448 ? kWide448TileN : kBN)));
+  static constexpr int kNSub = kW448 ? 2 : (kTileN > kBN ? kTileN / kBN : 1);   // MMAs per K step (along N)
   static constexpr int kMmaN = kTileN / kNSub;                     // N of one MMA
   static constexpr int kRowsBSub = kPair ? kMmaN / 2 : kMmaN;     // B rows a CTA stages per MMA
   static constexpr int kRowsB = kRowsBSub * kNSub;                // B rows a CTA stages per k-block
@@ -115,6 +118,8 @@ struct Cfg {
   static_assert(!kNarrow || (!kPair && !kMx), "narrow tiles: single CTA, 16-bit or FP8 inputs");
   static_assert(!kN224 || (kPair && !kMx), "224-column tiles: CTA pair, 16-bit or FP8 inputs");
   static_assert(!kW512 || (kPair && !kMx && kAccBufs == 1), "512-column tiles: CTA pair, 16-bit or FP8 inputs");
+  static_assert(!kW448 || (kPair && !kMx && kAccBufs == 1 && kMmaN == kMxTileN && kBSub % 1024 == 0),
+                "448-column tiles: CTA pair, two 224-column MMAs, 16-bit or FP8 inputs");
 };
 static_assert(kBK == kSwz, "a K-major stage row is exactly one swizzle span");
 
@@ -1242,7 +1247,9 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
 
 // ------------------------------------------------------------------ host launch side
 // Index of a pair shape in DeviceState's per-shape arrays.
-constexpr int pair_shape_index(int shape) { return shape == kShapeN224 ? 1 : (shape == kShapeW512 ? 2 : 0); }
+constexpr int pair_shape_index(int shape) {
+  return shape == kShapeN224 ? 1 : (shape == kShapeW512 ? 2 : (shape == kShapeW448 ? 3 : 0));
+}
 
 // Per-device state the launchers keep (function attributes set, co-resident clusters).
 // The host writes it only while holding its device-state lock (calls may come from several
@@ -1252,8 +1259,8 @@ struct DeviceState {
   bool probed = false;
   int major = 0, minor = 0, sms = 0;
   bool attr_single[2][3][2] = {};   // [bf16 out][input kind][narrow]
-  bool attr_pair[2][3][3] = {};   // [bf16 out][input kind][pair shape: standard, 224, 512 wide]
-  int pair_clusters[3] = {};      // co-resident clusters per pair shape (0: not queried yet)
+  bool attr_pair[2][3][4] = {};   // [bf16 out][input kind][pair shape: standard, 224, 512, 448 wide]
+  int pair_clusters[4] = {};      // co-resident clusters per pair shape (0: not queried yet)
   uint32_t epoch = 0;      // stream-K launch counter (flags compare against it)
   bool dbg_attr = false;
   uint32_t* status = nullptr;   // device address of the status word

@@ -145,9 +145,11 @@ constexpr int kVariantPair = 2;
 constexpr int kVariantNarrow = 4;   // single CTA, 128 x 64 tiles (few output columns)
 constexpr int kVariantPair224 = 5;  // CTA pair, 256 x 224 tiles (K-major B, 16-bit or FP8 inputs)
 constexpr int kVariantPair512 = 6;  // CTA pair, 256 x 512 tiles (16-bit or FP8 inputs)
+constexpr int kVariantPair448 = 7;  // CTA pair, 256 x 448 tiles (K-major B, 16-bit or FP8 inputs)
 
 bool is_pair(int variant) {
-  return variant == kVariantPair || variant == kVariantPair224 || variant == kVariantPair512;
+  return variant == kVariantPair || variant == kVariantPair224 || variant == kVariantPair512 ||
+         variant == kVariantPair448;
 }
 
 using gb::DeviceState;
@@ -202,12 +204,14 @@ int64_t tile_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
   if (variant == kVariantPair512) return gb::Cfg<true, gb::kIn16, gb::kShapeW512>::kTileN;
+  if (variant == kVariantPair448) return gb::Cfg<true, gb::kIn16, gb::kShapeW448>::kTileN;
   return is_pair(variant) ? gb::Cfg<true>::kTileN : gb::Cfg<false>::kTileN;
 }
 int64_t mma_n_of(int variant, const InType& in) {
   if (variant == kVariantNarrow) return gb::kNarrowTileN;
   if (in.mx || variant == kVariantPair224) return gb::kMxTileN;
   if (variant == kVariantPair512) return gb::Cfg<true, gb::kIn16, gb::kShapeW512>::kMmaN;
+  if (variant == kVariantPair448) return gb::Cfg<true, gb::kIn16, gb::kShapeW448>::kMmaN;
   return is_pair(variant) ? gb::Cfg<true>::kMmaN : gb::Cfg<false>::kMmaN;
 }
 
@@ -316,7 +320,14 @@ int choose_pair_width(int64_t M, int64_t N, int64_t K, int pairs, bool allow224,
     v = kVariantPair224;
     best = c224;
   }
-  if (allow512 && cost(gb::kWideTileN, 0.645 * wide_factor, 1.0) < best) v = kVariantPair512;
+  const double c512 = cost(gb::kWideTileN, 0.645 * wide_factor, 1.0);
+  if (allow512 && c512 < best) {
+    v = kVariantPair512;
+    best = c512;
+  }
+  // 2 x 224 columns: the 512-column tile's costs scaled by 7/8 (K-major B, like 224)
+  if (allow512 && allow224 && cost(gb::kWide448TileN, 0.645 * 0.875 * wide_factor, 0.875) < best)
+    v = kVariantPair448;
   return v;
 }
 
@@ -345,7 +356,8 @@ int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorA
                           (majorA == GB_K_MAJOR && (lda * in.bytes) % 128 != 0) ||
                               (majorB == GB_K_MAJOR && (ldb * in.bytes) % 128 != 0));
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
-  if (in.mx && v == kVariantPair512) v = kVariantPair;
+  if (in.mx && (v == kVariantPair512 || v == kVariantPair448)) v = kVariantPair;
+  if (v == kVariantPair448 && majorB != GB_K_MAJOR) v = kVariantPair512;
   // 224-column tiles stage 112 B rows per CTA: K-major B only (an MN-major box is 64 wide)
   if (v == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) v = kVariantPair;
   return v;
@@ -362,7 +374,8 @@ gb_status make_plan(int dtype, int variant, int64_t M, int64_t N, int64_t K, int
   const int64_t tile_m = pair ? gb::Cfg<true>::kTileM : gb::Cfg<false>::kTileM;
   if (in.mx && variant == kVariantNarrow) return GB_ERR_INVALID_ARG;
   if (variant == kVariantPair224 && (in.mx || majorB != GB_K_MAJOR)) return GB_ERR_INVALID_ARG;
-  if (variant == kVariantPair512 && in.mx) return GB_ERR_INVALID_ARG;
+  if ((variant == kVariantPair512 || variant == kVariantPair448) && in.mx) return GB_ERR_INVALID_ARG;
+  if (variant == kVariantPair448 && majorB != GB_K_MAJOR) return GB_ERR_INVALID_ARG;
   const int64_t tile_n = tile_n_of(variant, in);
   // B rows one copy stages: one CTA's share of one MMA's columns
   const int64_t rows_b = pair ? mma_n_of(variant, in) / 2 : mma_n_of(variant, in);
@@ -514,6 +527,8 @@ bool epi_tma_fits(int variant, int kind) {
     return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kEpiTma : Cfg<true, kIn16, kShapeN224>::kEpiTma;
   if (variant == kVariantPair512)
     return kind == kIn8 ? Cfg<true, kIn8, kShapeW512>::kEpiTma : Cfg<true, kIn16, kShapeW512>::kEpiTma;
+  if (variant == kVariantPair448)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeW448>::kEpiTma : Cfg<true, kIn16, kShapeW448>::kEpiTma;
   if (is_pair(variant))
     return kind == kInMx ? Cfg<true, kInMx>::kEpiTma
                          : (kind == kIn8 ? Cfg<true, kIn8>::kEpiTma : Cfg<true, kIn16>::kEpiTma);
@@ -531,6 +546,8 @@ int stage_kblocks(int variant, int kind) {
     return kind == kIn8 ? Cfg<true, kIn8, kShapeN224>::kKB : Cfg<true, kIn16, kShapeN224>::kKB;
   if (variant == kVariantPair512)
     return kind == kIn8 ? Cfg<true, kIn8, kShapeW512>::kKB : Cfg<true, kIn16, kShapeW512>::kKB;
+  if (variant == kVariantPair448)
+    return kind == kIn8 ? Cfg<true, kIn8, kShapeW448>::kKB : Cfg<true, kIn16, kShapeW448>::kKB;
   if (is_pair(variant))
     return kind == kInMx ? Cfg<true, kInMx>::kKB : (kind == kIn8 ? Cfg<true, kIn8>::kKB : Cfg<true, kIn16>::kKB);
   return kind == kInMx ? Cfg<false, kInMx>::kKB : (kind == kIn8 ? Cfg<false, kIn8>::kKB : Cfg<false, kIn16>::kKB);
@@ -610,6 +627,8 @@ gb_status prepare_pair_any(int kin, int shape, DeviceState* dev) {
     return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeN224>(dev) : prepare_pair<kBF16, kIn16, kShapeN224>(dev);
   if (shape == kShapeW512)
     return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeW512>(dev) : prepare_pair<kBF16, kIn16, kShapeW512>(dev);
+  if (shape == kShapeW448)
+    return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeW448>(dev) : prepare_pair<kBF16, kIn16, kShapeW448>(dev);
   if (kin == kInMx) return prepare_pair<kBF16, kInMx, kShapeStd>(dev);
   return kin == kIn8 ? prepare_pair<kBF16, kIn8, kShapeStd>(dev) : prepare_pair<kBF16, kIn16, kShapeStd>(dev);
 }
@@ -631,6 +650,9 @@ gb_status launch_any(bool pair, int kin, int shape, bool narrow, const Maps& m, 
   if (shape == gb::kShapeW512)
     return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeW512>(m, p, G, s)
                            : launch_pair<kBF16, gb::kIn16, gb::kShapeW512>(m, p, G, s);
+  if (shape == gb::kShapeW448)
+    return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeW448>(m, p, G, s)
+                           : launch_pair<kBF16, gb::kIn16, gb::kShapeW448>(m, p, G, s);
   if (kin == gb::kInMx) return launch_pair<kBF16, gb::kInMx, gb::kShapeStd>(m, p, G, s);
   return kin == gb::kIn8 ? launch_pair<kBF16, gb::kIn8, gb::kShapeStd>(m, p, G, s)
                          : launch_pair<kBF16, gb::kIn16, gb::kShapeStd>(m, p, G, s);
@@ -818,7 +840,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   }
   const bool pair = is_pair(pl.variant);
   const int shape = pl.variant == kVariantPair224 ? gb::kShapeN224
-                    : (pl.variant == kVariantPair512 ? gb::kShapeW512 : gb::kShapeStd);
+                    : (pl.variant == kVariantPair512 ? gb::kShapeW512
+                                                     : (pl.variant == kVariantPair448 ? gb::kShapeW448 : gb::kShapeStd));
   const bool bf = dtype == GB_BF16;
   const bool narrow = pl.variant == kVariantNarrow;
   int slots;   // CTAs (clusters) that can run at once

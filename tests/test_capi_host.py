@@ -37,7 +37,7 @@ def test_status_strings():
     assert "10.3" in G.status_string(3)
 
 
-@pytest.fixture(params=[1, 2, 5, 6], ids=["single", "pair", "pair224", "pair512"])
+@pytest.fixture(params=[1, 2, 5, 6, 7], ids=["single", "pair", "pair224", "pair512", "pair448"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param
@@ -55,15 +55,16 @@ def test_plans_of_the_workloads(variant, name, M, N, K, majors, grid1, grid2):
     lda = K if majors[0] == "K" else M
     ldb = K if majors[1] == "K" else N
     p = G.plan("f16", M, N, K, lda, majors[0], ldb, majors[1])
-    # 224-column tiles need K-major B: a forced 224 variant with MN-major B runs as the pair
-    want = 2 if (variant == 5 and majors[1] == "MN") else variant
+    # 224-column tiles need K-major B: a forced 224 (448) variant with MN-major B runs as the
+    # pair (the 512-column pair)
+    want = {5: 2, 7: 6}.get(variant, variant) if majors[1] == "MN" else variant
     grid = grid1 if want == 1 else grid2
     tile_m = 128 if want == 1 else 256
-    tile_n = {5: 224, 6: 512}.get(want, 256)
-    if want in (5, 6):
+    tile_n = {5: 224, 6: 512, 7: 448}.get(want, 256)
+    if want in (5, 6, 7):
         grid = (grid[0], -(-N // tile_n), grid[2])
-    rows_b = {1: 256, 2: 128, 5: 112, 6: 128}[want]    # B rows one copy box stages per CTA
-    mma_n = 256 if want == 6 else tile_n                # the 512-column tile takes two MMAs
+    rows_b = {1: 256, 2: 128, 5: 112, 6: 128, 7: 112}[want]    # B rows one copy box stages per CTA
+    mma_n = {6: 256, 7: 224}.get(want, tile_n)                 # the wide tiles take two MMAs
     assert p["variant"] == want and p["tile_m"] == tile_m and p["tile_n"] == tile_n
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == grid
     # a grid mode of extent 1 is only ever indexed at 0: its stride is immaterial
@@ -108,8 +109,9 @@ def test_variant_choice_by_shape():
     p = G.plan("bf16", 8192, 8192, 8192, 8192, "K", 8192, "K")                # 7 x 512: 585 us, 14 x 256: 608
     assert p["variant"] == 6 and (p["m_tiles"], p["n_tiles"], p["tile_n"]) == (32, 16, 512)
     assert p["b_box"] == [64, 128] and (p["instr_desc"] >> 17) & 63 == 256 >> 3
-    # rows of 4104 halves (8208 bytes) are not 128-byte aligned: the wide tile copies fewer bytes per flop
-    assert G.plan("f16", 5000, 3000, 4104, 4104, "K", 4104, "K")["variant"] == 6
+    # rows of 4104 halves (8208 bytes) are not 128-byte aligned: a wide tile copies fewer bytes per
+    # flop, and 7 columns of 448 fill their 2 waves better than 6 of 512
+    assert G.plan("f16", 5000, 3000, 4104, 4104, "K", 4104, "K")["variant"] == 7
     assert G.plan("f16", 16384, 1024, 4096, 16384, "MN", 1024, "MN")["variant"] == 6   # 2 x 512 vs 4 x 256
     assert G.plan("f16", 4096, 4096, 4096, 4096, "K", 4096, "MN")["variant"] == 6   # MN-major B: no 224
     # at most 64 output columns: narrow 128 x 64 tiles
@@ -118,7 +120,7 @@ def test_variant_choice_by_shape():
     assert (p["m_tiles"], p["n_tiles"], p["k_blocks"]) == (32, 1, 64)
     assert p["b_box"] == [64, 64] and (p["instr_desc"] >> 17) & 63 == 64 >> 3
     with pytest.raises(G.GemmError):
-        G.set_kernel_variant(7)
+        G.set_kernel_variant(8)
     # 3 was a form whose B tiles were copied into two CTA pairs at once (copy multicast); it
     # is gone, and asking for it is an argument error
     assert G.lib().gb_set_kernel_variant(3) == 1

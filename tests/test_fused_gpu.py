@@ -20,7 +20,7 @@ DEV = torch.device("cuda", 0)
 FP8 = {"e4m3": (O.E4M3, 448.0), "e5m2": (O.E5M2, 57344.0)}
 
 
-@pytest.fixture(params=[1, 2, 4, 5, 6], ids=["single", "pair", "narrow", "pair224", "pair512"])
+@pytest.fixture(params=[1, 2, 4, 5, 6, 7], ids=["single", "pair", "narrow", "pair224", "pair512", "pair448"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param

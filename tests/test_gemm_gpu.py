@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
-@pytest.fixture(params=[1, 2, 4, 5, 6], ids=["single", "pair", "narrow", "pair224", "pair512"])
+@pytest.fixture(params=[1, 2, 4, 5, 6, 7], ids=["single", "pair", "narrow", "pair224", "pair512", "pair448"])
 def variant(request):
     """Run a test with the single-CTA kernel and with the CTA-pair kernel."""
     G.set_kernel_variant(request.param)
@@ -369,7 +369,7 @@ def test_wait_timeout_is_reported_and_context_survives(variant):
 # --------------------------------------------------------------------------- device-side maps
 
 
-@pytest.mark.parametrize("var", [1, 2, 4, 5, 6])
+@pytest.mark.parametrize("var", [1, 2, 4, 5, 6, 7])
 @pytest.mark.parametrize("M,N,tile", [(5000, 3000, (19, 11)), (5000, 3000, (0, 0)),
                                       (256, 128, (0, 0)), (8192, 8192, (17, 30))])
 def test_epilogue_map_matches_host_layout(var, M, N, tile):

@@ -20,7 +20,7 @@ DEV = torch.device("cuda", 0)
 ATOM = "((32,4),4):((16,4),1)"    # (row in 128, scale in k-block) -> byte of a 512-byte atom
 
 
-@pytest.fixture(params=[1, 2, 4, 5, 6], ids=["single", "pair", "narrow_falls_back", "pair224_falls_back", "pair512_falls_back"])
+@pytest.fixture(params=[1, 2, 4, 5, 6, 7], ids=["single", "pair", "narrow_falls_back", "pair224_falls_back", "pair512_falls_back", "pair448_falls_back"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param

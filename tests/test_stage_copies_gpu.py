@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 
 
-@pytest.fixture(params=[2, 5, 6], ids=["pair", "pair224", "pair512"])
+@pytest.fixture(params=[2, 5, 6, 7], ids=["pair", "pair224", "pair512", "pair448"])
 def pair(request):
     G.set_kernel_variant(request.param)
     yield

@@ -20,7 +20,7 @@ def workspace():
     return G.make_workspace(DEV)
 
 
-@pytest.fixture(params=[1, 2, 4, 5, 6], ids=["single", "pair", "narrow", "pair224", "pair512"])
+@pytest.fixture(params=[1, 2, 4, 5, 6, 7], ids=["single", "pair", "narrow", "pair224", "pair512", "pair448"])
 def variant(request):
     G.set_kernel_variant(request.param)
     yield request.param

@@ -72,7 +72,7 @@ def forced_stream_k():
     G.set_schedule(0)
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 4, 5, 6], ids=["auto", "single", "pair", "narrow", "pair224", "pair512"])
+@pytest.mark.parametrize("variant", [0, 1, 2, 4, 5, 6, 7], ids=["auto", "single", "pair", "narrow", "pair224", "pair512", "pair448"])
 def test_no_alloc_matches_existing_entry_points_on_two_calls(cases, forced_stream_k, variant):
     workspace = G.make_workspace(DEV)
     G.set_kernel_variant(variant)
