@@ -851,46 +851,30 @@ __device__ __forceinline__ uint32_t next_contributor(const Params& p, uint32_t G
   return c;
 }
 
-// The 32 x 32 block of C at rows y0.., columns x.. as a warp loads it with coalesced 16-byte
-// loads: lane l takes, in slice i, row y0 + 8 i + l / 4 at columns x + 8 (l % 4) .. + 7 (zeros
-// outside M x N; N is a multiple of 8).  Each load instruction covers 8 whole 64-byte row
-// segments, where one row per lane would touch 32 lines per instruction.
-__device__ __forceinline__ void load_c_slab(const Params& p, int32_t y0, int32_t x, int lane, uint4 (&cr)[4]) {
-  const int32_t row = y0 + (lane >> 2), col = x + 8 * (lane & 3);
-  const uint4* src = reinterpret_cast<const uint4*>(p.C + static_cast<int64_t>(row) * p.d_row + col);
-  const int64_t step = p.d_row;   // 8 rows, in 16-byte words (d_row halves / 8 per word)
-  const int32_t rows_left = col < p.N ? p.M - row : 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    cr[i] = 8 * i < rows_left ? __ldg(src + i * step) : make_uint4(0u, 0u, 0u, 0u);
-}
-
 // One 32-column run of the tile-store epilogue for this warp's 32 rows: C from its staging
-// tile (copied in two runs ahead) or from a slab of registers (reg_c: loaded ahead by
-// load_c_slab, passed through the D staging tile to give each lane its row), alpha/beta and the
-// fused nodes, the 16-bit row written to the D staging tile, one tensor copy of the 32 x 32 tile
-// to D (clipped at M and N), and the C staging tile refilled with the run two further on.
-// Returns false if a wait gave up.
+// tile (tload_c: copied in two runs ahead into tiles of its own; cd_c: copied one run ahead into
+// the D staging tile this run then writes), alpha/beta and the fused nodes, the 16-bit row
+// written to the D staging tile, one tensor copy of the 32 x 32 tile to D (clipped at M and N),
+// and the next C copy issued.  Returns false if a wait gave up.
 template <bool kBF16, bool kPair>
 __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const uint32_t (&acc)[32], int ew,
                                                int lane, uint32_t stg, uint32_t& gr, uint32_t& c_phase,
                                                uint32_t& c_pending, bool tload_c, int run, int nruns, int32_t x0,
                                                int32_t y0, int valid, int64_t col0, float& amax, const void* tmC,
-                                               const void* tmD, bool reg_c, const uint4 (&cr)[4]) {
+                                               const void* tmD, bool cd_c) {
   constexpr uint32_t kBuf = 32 * 64;
   const uint32_t b = gr & 1u;
   const uint32_t sd = stg + b * kBuf, sc = stg + (2 + b) * kBuf;
   float v[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
-  if (reg_c) {
-    // the D staging tile is free once the copy that last read it (two runs back) is done; the C
-    // slab goes through it, and every lane has read its row back before D is written there
-    if (lane == 0) bulk_wait_group_read<1>();
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 4; ++i) st_shared_u4(sd + stage64_offset(8 * i + (lane >> 2), lane & 3), cr[i]);
-    __syncwarp();
+  if (cd_c) {
+    // this run's C tile, copied into the D staging tile before (every lane reads its row before
+    // D is written there)
+    if (!wait_warp<kPair>(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, ctl, p.timeout_ns, kSiteEpiC))
+      return false;
+    c_phase ^= 1u << b;
+    c_pending &= ~(1u << b);
     uint4 cw[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) cw[j] = ld_shared_u4(sd + stage64_offset(lane, j));
@@ -919,6 +903,7 @@ __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const 
   fence_proxy_async_smem();
   __syncwarp();
   const bool refill = tload_c && run + 2 < nruns;
+  const bool next_c = cd_c && run + 1 < nruns;
   if (lane == 0) {
     tma_store_2d(tmD, sd, x0 + 32 * run, y0);
     bulk_commit_group();
@@ -929,8 +914,17 @@ __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const 
       mbar_arrive_expect_tx(bar, kBuf);
       tma_load_2d(sc, tmC, bar, x0 + 32 * (run + 2), y0);
     }
+    // the next run's C goes into the other D staging tile once the store of the run before
+    // this one has read it
+    if (next_c) {
+      bulk_wait_group_read<1>();
+      const uint32_t bar = smem_addr(&ctl->c_full[ew][b ^ 1u]);
+      mbar_arrive_expect_tx(bar, kBuf);
+      tma_load_2d(stg + (b ^ 1u) * kBuf, tmC, bar, x0 + 32 * (run + 1), y0);
+    }
   }
   if (refill) c_pending |= 1u << b;
+  if (next_c) c_pending |= 1u << (b ^ 1u);
   ++gr;
   return true;
 }
@@ -984,30 +978,28 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     // tile-store path: the 32-row slab of this warp starts at row y0, its runs at x0 + 32 run
     const bool tstore = tma && !contributor;
     const bool tload_c = tstore && p.has_c && C::kEpiCTma;   // C by tensor copy into staging
-    const bool reg_c = tstore && p.has_c && !C::kEpiCTma;     // C into registers
+    const bool cd_c = tstore && p.has_c && !C::kEpiCTma;      // C by tensor copy into the D tiles
     const int32_t y0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA + q * 32;
     const int32_t x0 = nt * C::kTileN + cbeg;
     // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
     // pulled into L2 and the first kAhead 32-column runs into registers while the main loop
-    // still runs; each later run is loaded kAhead runs before its use (on the tile-store path
-    // with register C as coalesced slabs, else one row per lane).  On the tile-store path with
-    // C staging tiles the first two runs of C are copied into them instead.
+    // still runs; each later run is loaded kAhead runs before its use.  On the tile-store path
+    // the first C tiles are copied into staging tiles instead: two runs into C tiles of their
+    // own (tload_c), or, with one accumulator (whose eight warps have no room for C tiles),
+    // the first run into the D staging tile it will write (cd_c; each later run one run ahead).
     const bool cvec = !tstore && p.has_c && p.vec_ok && row_ok && item.sb0 == 0;
-    // (register C of the wide tile: one run ahead, which keeps it within the 168 registers a
-    // thread of its 320 has; two ahead spilled and measured slower)
+    // (one run ahead with one accumulator: its 320 threads have 168 registers each)
     constexpr int kAhead = C::kEpiCTma ? 2 : 1;
     uint4 cr[kAhead][4];
-    if ((cvec || reg_c) && row_ok && cend > cbeg)
+    if ((cvec || cd_c) && row_ok && cend > cbeg)
       prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
 #pragma unroll
-    for (int a = 0; a < kAhead; ++a) {
-      if (reg_c && cbeg + 32 * a < cend) load_c_slab(p, y0, x0 + 32 * a, lane, cr[a]);
+    for (int a = 0; a < kAhead; ++a)
       if (cvec && cbeg + 32 * a + 32 <= cend) {
         const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cbeg + 32 * a);
 #pragma unroll
         for (int j = 0; j < 4; ++j) cr[a][j] = __ldg(src + j);
       }
-    }
     if constexpr (C::kEpiTma) {
       if (tload_c && lane == 0) {
         for (int a = 0; a < 2 && a < nruns; ++a) {
@@ -1018,6 +1010,16 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
         }
       }
       if (tload_c) c_pending |= (nruns > 0 ? 1u << (gr & 1u) : 0u) | (nruns > 1 ? 1u << ((gr + 1) & 1u) : 0u);
+      if (cd_c && nruns > 0) {
+        if (lane == 0) {
+          // the D staging tile of the first run is free once the store two runs back has read it
+          bulk_wait_group_read<1>();
+          const uint32_t bar = smem_addr(&ctl->c_full[ew][gr & 1u]);
+          mbar_arrive_expect_tx(bar, C::kEpiBufBytes);
+          tma_load_2d(stg + (gr & 1u) * C::kEpiBufBytes, tmC, bar, x0, y0);
+        }
+        c_pending |= 1u << (gr & 1u);
+      }
     }
     const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
     const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
@@ -1070,8 +1072,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
           if (C::kEpiTma && tstore)
             ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
                                               nruns, x0, y0, row_ok ? min(32, cols_left - c0) : 0,
-                                              static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD, reg_c,
-                                              cr[0]);
+                                              static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD, cd_c);
           else if (row_ok)
             store_run<kBF16>(p, base + c0 * p.d_col, cvec && c0 + 32 <= cend, cr[0], acc,
                              min(32, cols_left - c0), static_cast<int64_t>(nt) * C::kTileN + c0, amax);
@@ -1082,7 +1083,6 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
             for (int j = 0; j < 4; ++j) cr[a][j] = cr[a + 1][j];
           const int cn0 = c0 + 32 * kAhead;
-          if (reg_c && cn0 < cend) load_c_slab(p, y0, x0 + (cn0 - cbeg), lane, cr[kAhead - 1]);
           if (cvec && cn0 + 32 <= cend) {
             const uint4* src = reinterpret_cast<const uint4*>(p.C + base + cn0);
 #pragma unroll
