@@ -332,7 +332,7 @@ int choose_pair_width(int64_t M, int64_t N, int64_t K, int pairs, bool allow224,
 }
 
 int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorA, int64_t lda, int majorB,
-                   int64_t ldb, int sms) {
+                   int64_t ldb, int sms, bool heavy_epilogue = false) {
   int forced;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -351,8 +351,12 @@ int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorA
   else
     // FP8 k-blocks run at twice the 16-bit MMA rate, so the 512-column tile's exposed epilogue
     // weighs twice as much against its main loop: measured slower for FP8 (8192^3 E4M3: 424 us
-    // against 380 with 256 columns), so FP8 takes it only when forced
-    v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR, !in.mx && !in.f8,
+    // against 380 with 256 columns), so FP8 takes it only when forced.  An epilogue with GELU
+    // or an FP8 output (per-thread stores) does more work per element than the main loop can hide once
+    // nothing overlaps it: measured on 8192^3 bf16 with C, bias and GELU, 747 us with 512
+    // columns against 664 with 256, so such epilogues keep two accumulators as well
+    v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR,
+                          !in.mx && !in.f8 && !heavy_epilogue,
                           (majorA == GB_K_MAJOR && (lda * in.bytes) % 128 != 0) ||
                               (majorB == GB_K_MAJOR && (ldb * in.bytes) % 128 != 0));
   if (in.mx && v == kVariantNarrow) v = M > gb::Cfg<false>::kTileM ? kVariantPair : kVariantSingle;
@@ -744,7 +748,9 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
-  const int variant = choose_variant(M, N, K, in, majorA, lda, majorB, ldb, dev->sms);
+  const bool heavy_epilogue =
+      epi && (epi->activation == GB_ACT_GELU || epi->out_format != GB_OUT_INPUT_TYPE);
+  const int variant = choose_variant(M, N, K, in, majorA, lda, majorB, ldb, dev->sms, heavy_epilogue);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
 
