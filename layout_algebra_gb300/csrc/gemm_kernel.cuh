@@ -31,7 +31,7 @@ constexpr int kUmmaK = 16;           // K of one kind::f16 MMA
 constexpr int kSwz = 64;             // elements per 128-byte swizzle span
 constexpr int kChunkBytes = kSwz * kBK * 2;   // one 64-wide MN-major box: 64 K-rows x 128 B
 constexpr int kTmemCols = 512;       // all of Tensor Memory: accumulators of 512 fp32 columns
-constexpr int kCtlBytes = 512;
+constexpr int kCtlBytes = 1024;
 constexpr int kMaxStages = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -110,6 +110,13 @@ struct Cfg {
   static constexpr int kEpiStageBytes = kEpiTma ? kEpiStageBytesFull : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiStageBytes + kCtlBytes;
   static constexpr uint32_t kAccEmptyArrivals = kEpiWarps * (kPair ? 2 : 1);
+  // Wide pair forms: during a tile's epilogue the two ring stages that held its last two
+  // k-blocks are idle (the next tile's copies go into the other two first), so each warp
+  // borrows kRingBufs staging tiles in each of them: with its own two, every run of the tile
+  // (up to kEpiNB) has a staging tile of its own and C is copied in several runs ahead.
+  static constexpr int kRingFit = kStageBytes / (kEpiWarps * kEpiBufBytes);
+  static constexpr int kRingBufs = (kW512 || kW448) ? (kRingFit < 3 ? kRingFit : 3) : 0;
+  static constexpr int kEpiNB = 2 + 2 * kRingBufs;
   static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
   static_assert(kStages <= kMaxStages, "control block");
@@ -183,7 +190,8 @@ struct Ctl {
   uint32_t tmem_base;
   int32_t abort;
   uint32_t* status;           // copy of Params::status for the wait helpers
-  uint64_t c_full[8][2];      // tile-store epilogue: C staging tile landed (per warp, buffer)
+  uint64_t c_full[8][8];      // tile-store epilogue: C staging tile landed (per warp, buffer)
+  uint64_t epi_ring;          // epilogue warps done with the ring stages they borrowed
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 static_assert(kCtlBytes % 8 == 0, "control block alignment");
@@ -197,7 +205,19 @@ enum : uint32_t {
   kSiteTail = 6,      // copy stage waiting for the last releases before exit
   kSiteFixup = 7,     // tile owner waiting for another CTA's stream-K partial
   kSiteEpiC = 8,      // epilogue waiting for a C tile copied into its staging buffer
+  kSiteRing = 9,      // copy stage waiting for the epilogue to return borrowed ring stages
 };
+
+// The epilogue borrows ring stages (wide pair forms, with C: its copies then run several runs
+// ahead): every tile is whole (no stream-K) and has at least kStages stage-blocks, so the copy
+// stage reaches the borrowed stages only with the third stage-block of the next tile, and
+// waits there for their return.  (Without C the two staging tiles of a warp suffice; the
+// hold-off of the next tile's copies would cost more than it saves.)
+template <class C>
+__device__ __forceinline__ bool ring_epilogue(const Params& p) {
+  return C::kRingBufs > 0 && C::kEpiTma && p.epi_tma != 0 && p.has_c != 0 && p.dp_tiles == p.num_tiles &&
+         p.nsb >= C::kStages;
+}
 
 // Record the first failing wait, and stop this CTA (and its peer, in a pair).
 template <bool kPair>
@@ -410,15 +430,25 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
   int64_t gkb = 0;
   uint32_t issued = 0, issued_parity = 0;
   bool ok = true;
+  const bool ring = ring_epilogue<C>(p);
+  int32_t it = 0;
   Sched sched;
   sched.init(p, cluster, nclusters);
   Item item;
-  while (ok && sched.next(p, nclusters, item)) {
+  for (; ok && sched.next(p, nclusters, item); ++it) {
     int32_t mt, nt;
     tile_coords(p, item.tile, mt, nt);
     const int32_t a_row0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA;
     const int32_t b_row0 = nt * C::kTileN + static_cast<int32_t>(prank) * C::kRowsBSub;
     for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
+      // the previous tile's epilogue holds the stages of its last two k-blocks, which this
+      // tile's third and fourth stage-blocks are about to reuse
+      if (ring && it > 0 && sb == item.sb0 + 2 &&
+          !wait_one<kPair>(smem_addr(&ctl->epi_ring), static_cast<uint32_t>((it - 1) & 1), ctl, p.timeout_ns,
+                           kSiteRing)) {
+        ok = false;
+        break;
+      }
       if (!wait_one<kPair>(smem_addr(&ctl->empty[stage]), phase ^ 1u, ctl, p.timeout_ns, kSiteEmpty)) {
         ok = false;
         break;
@@ -929,6 +959,63 @@ __device__ __forceinline__ bool tile_store_run(const Params& p, Ctl* ctl, const 
   return true;
 }
 
+// One 32-column run of the wide pair forms' epilogue with borrowed ring stages: run `run` of
+// the tile uses staging tile b = run % NB (address buf(b)), whose C copy (if any) was issued
+// several runs earlier; D is written over C in that tile and stored by one tensor copy; then
+// the C copy of run + NB - 1 is issued into the tile of the run before this one once that
+// run's store has read it.  Returns false if a wait gave up.
+template <bool kBF16, bool kPair, int kNB, class BufAddr>
+__device__ __forceinline__ bool ring_store_run(const Params& p, Ctl* ctl, const uint32_t (&acc)[32], int ew,
+                                               int lane, const BufAddr& buf, uint32_t& c_phase,
+                                               uint32_t& c_pending, int run, int nruns, int32_t x0, int32_t y0,
+                                               int valid, int64_t col0, float& amax, const void* tmC,
+                                               const void* tmD) {
+  constexpr uint32_t kBuf = 32 * 64;
+  const uint32_t b = static_cast<uint32_t>(run % kNB);
+  const uint32_t sd = buf(b);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(acc[i]);
+  if (p.has_c) {
+    if (!wait_warp<kPair>(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, ctl, p.timeout_ns, kSiteEpiC))
+      return false;
+    c_phase ^= 1u << b;
+    c_pending &= ~(1u << b);
+    uint4 cw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cw[j] = ld_shared_u4(sd + stage64_offset(lane, j));
+    add_c_words<kBF16>(p, cw, v);
+    __syncwarp();
+  } else if (run >= kNB) {
+    // the store of run - NB, which read this staging tile, must be done with it
+    if (lane == 0) bulk_wait_group_read<kNB - 1>();
+    __syncwarp();
+  }
+  if (p.fused) fused_nodes<kBF16>(p, valid, col0, amax, v);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_u4(sd + stage64_offset(lane, j),
+                 make_uint4(pack2<kBF16>(v[8 * j + 0], v[8 * j + 1]), pack2<kBF16>(v[8 * j + 2], v[8 * j + 3]),
+                            pack2<kBF16>(v[8 * j + 4], v[8 * j + 5]), pack2<kBF16>(v[8 * j + 6], v[8 * j + 7])));
+  fence_proxy_async_smem();
+  __syncwarp();
+  const int ahead = run + kNB - 1;
+  const bool next_c = p.has_c && run >= 1 && ahead < nruns;
+  if (lane == 0) {
+    tma_store_2d(tmD, sd, x0 + 32 * run, y0);
+    bulk_commit_group();
+    if (next_c) {
+      const uint32_t nb = static_cast<uint32_t>(ahead % kNB);
+      bulk_wait_group_read<1>();   // the store of run - 1 has read tile nb
+      const uint32_t bar = smem_addr(&ctl->c_full[ew][nb]);
+      mbar_arrive_expect_tx(bar, kBuf);
+      tma_load_2d(buf(nb), tmC, bar, x0 + 32 * ahead, y0);
+    }
+  }
+  if (next_c) c_pending |= 1u << (ahead % kNB);
+  return true;
+}
+
 template <bool kBF16, bool kPair, int kIn, int kShape>
 __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int warp, int lane,
                              uint32_t rank, uint32_t cluster, uint32_t nclusters, uint8_t* epi_smem,
@@ -958,6 +1045,10 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
                             static_cast<uint32_t>(ew) * kPartBatch * 4096u + static_cast<uint32_t>(lane) * 4u;
   uint32_t gr = 0, c_phase = 0;
   uint32_t c_pending = 0;            // staging buffers with a C copy issued, not yet waited for
+  // borrowed ring stages (wide pair forms): the stages of the tile's last two k-blocks, found
+  // from the stage-blocks this CTA's copy stage has issued up to the end of the tile
+  const bool ring_ok = ring_epilogue<C>(p);
+  int64_t sb_done = 0;
   int32_t it = 0;
   float amax = 0.0f;                 // this thread's max |v| (fused epilogue)
   Sched sched;
@@ -977,8 +1068,22 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const bool owner_with_parts = item.sb0 == 0 && item.sb1 < p.nsb;
     // tile-store path: the 32-row slab of this warp starts at row y0, its runs at x0 + 32 run
     const bool tstore = tma && !contributor;
+    const bool ring = tstore && ring_ok;                      // staging in borrowed ring stages
     const bool tload_c = tstore && p.has_c && C::kEpiCTma;   // C by tensor copy into staging
-    const bool cd_c = tstore && p.has_c && !C::kEpiCTma;      // C by tensor copy into the D tiles
+    const bool cd_c = tstore && p.has_c && !C::kEpiCTma && !ring;   // C by tensor copy into the D tiles
+    sb_done += item.sb1 - item.sb0;
+    const uint32_t ring_base = smem_addr(epi_smem) - static_cast<uint32_t>(kRingBytes);
+    const int s_last = static_cast<int>((sb_done - 1) % C::kStages);
+    const uint32_t slot_a = ring_base + static_cast<uint32_t>(((s_last + C::kStages - 1) % C::kStages) * C::kStageBytes);
+    const uint32_t slot_b = ring_base + static_cast<uint32_t>(s_last * C::kStageBytes);
+    // staging tile b of this warp: its own two, then kRingBufs in each borrowed stage
+    auto ring_buf = [&](uint32_t b) -> uint32_t {
+      if (b < 2u) return stg + b * C::kEpiBufBytes;
+      constexpr uint32_t kPer = C::kRingBufs > 0 ? C::kRingBufs : 1;
+      const uint32_t i = b - 2u;
+      const uint32_t slot = i < kPer ? slot_a : slot_b;
+      return slot + (static_cast<uint32_t>(ew) * kPer + i % kPer) * C::kEpiBufBytes;
+    };
     const int32_t y0 = mt * C::kTileM + static_cast<int32_t>(prank) * kRowsA + q * 32;
     const int32_t x0 = nt * C::kTileN + cbeg;
     // C in 16-byte words when rows are contiguous and aligned (vec_ok): the tile's C rows are
@@ -991,7 +1096,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     // (one run ahead with one accumulator: its 320 threads have 168 registers each)
     constexpr int kAhead = C::kEpiCTma ? 2 : 1;
     uint4 cr[kAhead][4];
-    if ((cvec || cd_c) && row_ok && cend > cbeg)
+    if ((cvec || cd_c || (ring && p.has_c)) && row_ok && cend > cbeg)
       prefetch_l2_bulk(p.C + base + cbeg, static_cast<uint32_t>(((cend - cbeg) * 2 + 15) & ~15));
 #pragma unroll
     for (int a = 0; a < kAhead; ++a)
@@ -1020,11 +1125,33 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
         }
         c_pending |= 1u << (gr & 1u);
       }
+      if (C::kRingBufs > 0 && ring && p.has_c) {
+        // the first two runs' C into this warp's own staging tiles (free: the previous tile's
+        // stores have read them), while the main loop still runs
+        if (lane == 0)
+          for (int a = 0; a < 2 && a < nruns; ++a) {
+            const uint32_t bar = smem_addr(&ctl->c_full[ew][a]);
+            mbar_arrive_expect_tx(bar, C::kEpiBufBytes);
+            tma_load_2d(ring_buf(static_cast<uint32_t>(a)), tmC, bar, x0 + 32 * a, y0);
+          }
+        c_pending |= (nruns > 0 ? 1u : 0u) | (nruns > 1 ? 2u : 0u);
+      }
     }
     const int buf = C::kAccBufs == 2 ? (it & 1) : 0;
     const uint32_t use = C::kAccBufs == 2 ? ((it >> 1) & 1) : (it & 1);
     if (!wait_warp<kPair>(smem_addr(&ctl->acc_full[buf]), use, ctl, p.timeout_ns, kSiteAccFull)) break;
     tc_fence_after_sync();
+    if (C::kRingBufs > 0 && ring && p.has_c) {
+      // every MMA of this tile has completed, so the borrowed stages are free: the C of the
+      // runs up to NB - 1 into them
+      if (lane == 0)
+        for (int a = 2; a < C::kEpiNB && a < nruns; ++a) {
+          const uint32_t bar = smem_addr(&ctl->c_full[ew][a]);
+          mbar_arrive_expect_tx(bar, C::kEpiBufBytes);
+          tma_load_2d(ring_buf(static_cast<uint32_t>(a)), tmC, bar, x0 + 32 * a, y0);
+        }
+      for (int a = 2; a < C::kEpiNB && a < nruns; ++a) c_pending |= 1u << a;
+    }
     uint32_t c_lo = 1, c_hi = 0;
     if (owner_with_parts) {
       c_lo = sk_owner_of(p, nclusters, static_cast<int64_t>(item.tile) * p.nsb + item.sb1);
@@ -1033,6 +1160,23 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     }
     float* mine = contributor ? part_slot<kPair>(p, cluster, rank) : nullptr;
     bool ok = true;
+    // with one accumulator and C, it is released once this warp has read its last columns from
+    // TMEM (the rest of that run works on registers), so the next tile's MMAs overlap that run
+    // (measured: 1 % faster with C; without C, whose runs are short, 0.5-1.5 % slower)
+    const bool early = C::kAccBufs == 1 && p.has_c != 0;
+    bool released = false;
+    auto release_acc = [&]() {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
+        if constexpr (kPair)
+          mbar_arrive_cluster(map_to_cta(ae, 0));
+        else
+          mbar_arrive(ae);
+      }
+      released = true;
+    };
 #pragma unroll
     for (int run = 0; run < kRuns; ++run) {
       const int c0 = cbeg + 32 * run;
@@ -1045,6 +1189,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[i] = 0u;
         }
+        if (early && c0 + 32 >= cend) release_acc();
         if (contributor) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) __stcg(mine + (c0 + i) * 128 + lrow, __uint_as_float(acc[i]));
@@ -1069,7 +1214,11 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
               for (int i = 0; i < 32; ++i)
                 acc[i] = __float_as_uint(__uint_as_float(acc[i]) + ld_shared_f32(part_buf + (k * 32 + i) * 128));
           }
-          if (C::kEpiTma && tstore)
+          if (C::kRingBufs > 0 && ring)
+            ok = ring_store_run<kBF16, kPair, (C::kEpiNB > 2 ? C::kEpiNB : 2)>(
+                p, ctl, acc, ew, lane, ring_buf, c_phase, c_pending, run, nruns, x0, y0,
+                row_ok ? min(32, cols_left - c0) : 0, static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD);
+          else if (C::kEpiTma && tstore)
             ok = tile_store_run<kBF16, kPair>(p, ctl, acc, ew, lane, stg, gr, c_phase, c_pending, tload_c, run,
                                               nruns, x0, y0, row_ok ? min(32, cols_left - c0) : 0,
                                               static_cast<int64_t>(nt) * C::kTileN + c0, amax, tmC, tmD, cd_c);
@@ -1093,14 +1242,16 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     }
     if (!ok) break;
     if (contributor) fence_acq_rel_gpu();   // this thread's partial before the hand-off
-    tc_fence_before_sync();
+    if (!released) release_acc();          // a warp with no columns in this tile
+    if (C::kRingBufs > 0 && ring_ok) {
+      // return the borrowed stages once every store of this tile has read its staging tile
+      if (lane == 0) {
+        bulk_wait_group_read<0>();
+        mbar_arrive(smem_addr(&ctl->epi_ring));
+      }
+    }
     __syncwarp();
     if (lane == 0) {
-      const uint32_t ae = smem_addr(&ctl->acc_empty[buf]);
-      if constexpr (kPair)
-        mbar_arrive_cluster(map_to_cta(ae, 0));
-      else
-        mbar_arrive(ae);
       if (contributor) mbar_arrive(smem_addr(&ctl->part_done));
       if (owner_with_parts) mbar_arrive(smem_addr(&ctl->fix_done));
     }
@@ -1132,7 +1283,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     // tiles (outstanding only after an abort) has landed, before the CTA finishes
     if (tma && lane == 0) {
       bulk_wait_group<0>();
-      for (uint32_t b = 0; b < 2; ++b)
+      for (uint32_t b = 0; b < 8; ++b)
         if (c_pending & (1u << b))
           wait_drain(smem_addr(&ctl->c_full[ew][b]), (c_phase >> b) & 1u, p.timeout_ns, p.status);
     }
@@ -1181,10 +1332,9 @@ __global__ void __launch_bounds__(Cfg<kPair, kIn, kShape>::kThreads, 1)
     mbar_init(smem_addr(&ctl->part_done), C::kEpiWarps);
     mbar_init(smem_addr(&ctl->fix_done), C::kEpiWarps);
     if constexpr (C::kEpiTma)
-      for (int w = 0; w < C::kEpiWarps; ++w) {
-        mbar_init(smem_addr(&ctl->c_full[w][0]), 1);
-        mbar_init(smem_addr(&ctl->c_full[w][1]), 1);
-      }
+      for (int w = 0; w < C::kEpiWarps; ++w)
+        for (int b = 0; b < 8; ++b) mbar_init(smem_addr(&ctl->c_full[w][b]), 1);
+    mbar_init(smem_addr(&ctl->epi_ring), C::kEpiWarps);
     ctl->abort = 0;
     ctl->status = p.status;
     fence_barrier_init();

@@ -161,6 +161,29 @@ def test_multi_tile_ragged_all_majors(variant, dtype, majors):
     check(p, data, run(p, data))
 
 
+@pytest.mark.parametrize("var", [6, 7], ids=["pair512", "pair448"])
+@pytest.mark.parametrize("has_c", [True, False], ids=["C", "noC"])
+@pytest.mark.parametrize("majors", [("K", "K"), ("MN", "MN")])
+def test_wide_forms_several_tiles_per_pair(var, has_c, majors):
+    # 20 x 4 = 80 tiles on 76 pairs: four pairs run a second tile, whose copies reuse the
+    # ring stages that the first tile's epilogue borrowed as staging; ragged last row and
+    # column of tiles (36 rows, 40 columns short), 5 k-blocks
+    tile_n = 512 if var == 6 else 448
+    M, N, K = 20 * 256 - 36, 4 * tile_n - 40, 320
+    lda = K if majors[0] == "K" else M + 4
+    ldb = K if majors[1] == "K" else N
+    p = W.Problem("wide", M, N, K, "bf16", majorA=majors[0], majorB=majors[1], has_c=has_c,
+                  alpha=1.25, beta=0.5 if has_c else 0.0, dist="normal", c_dist="normal",
+                  seed=91 + var, lda=lda, ldb=ldb)
+    data = W.make(p)
+    G.set_kernel_variant(var)
+    try:
+        D = run(p, data)
+    finally:
+        G.set_kernel_variant(0)
+    check(p, data, D)
+
+
 @pytest.mark.parametrize("majors", [("K", "K"), ("MN", "MN"), ("MN", "K"), ("K", "MN")])
 def test_integer_ragged_exact(variant, majors):
     M, N, K = 129, 77, 40
