@@ -16,7 +16,7 @@
  * 128 x 256 tiles fit in one wave, else the pair width whose persistent waves of tiles cost
  * least (ceil(tiles / pairs) waves, pairs = half the device's SMs, times the measured cost of
  * a tile of that width; 224 needs K-major B; the 448- and 512-column tiles, whose epilogue
- * nothing overlaps, are left to 16-bit inputs whose epilogue has no GELU and no FP8 output).
+ * nothing overlaps, are left to 16-bit inputs with the plain alpha/beta epilogue).
  *
  * Operand layouts (a matrix is named after its stride-1 mode, "Layouts as Algebra" —
  * "One notation, and no more transposes"):

@@ -351,10 +351,10 @@ int choose_variant(int64_t M, int64_t N, int64_t K, const InType& in, int majorA
   else
     // FP8 k-blocks run at twice the 16-bit MMA rate, so the 512-column tile's exposed epilogue
     // weighs twice as much against its main loop: measured slower for FP8 (8192^3 E4M3: 424 us
-    // against 380 with 256 columns), so FP8 takes it only when forced.  An epilogue with GELU
-    // or an FP8 output (per-thread stores) does more work per element than the main loop can hide once
-    // nothing overlaps it: measured on 8192^3 bf16 with C, bias and GELU, 747 us with 512
-    // columns against 664 with 256, so such epilogues keep two accumulators as well
+    // against 380 with 256 columns), so FP8 takes it only when forced.  A fused epilogue (bias,
+    // activation, amax or an FP8 output) does more work per element, which nothing overlaps on
+    // the wide tiles: measured on 8192^3 bf16 with C, bias and GELU 747 us with 512 columns
+    // against 664 with 256, bias and ReLU 685 against 640, so these keep two accumulators
     v = choose_pair_width(M, N, K, sms / 2, !in.mx && majorB == GB_K_MAJOR,
                           !in.mx && !in.f8 && !heavy_epilogue,
                           (majorA == GB_K_MAJOR && (lda * in.bytes) % 128 != 0) ||
@@ -748,8 +748,8 @@ gb_status gemm_entry(int dtype, int64_t M, int64_t N, int64_t K, float alpha, co
   if ((st = device_state(&dev)) != GB_OK) return st;
   if (workspace && static_cast<int64_t>(workspace_size) < workspace_bytes_for(dev->sms))
     return GB_ERR_INVALID_ARG;
-  const bool heavy_epilogue =
-      epi && (epi->activation == GB_ACT_GELU || epi->out_format != GB_OUT_INPUT_TYPE);
+  const bool heavy_epilogue = epi && (epi->bias != nullptr || epi->activation != GB_ACT_NONE ||
+                                      epi->amax != nullptr || epi->out_format != GB_OUT_INPUT_TYPE);
   const int variant = choose_variant(M, N, K, in, majorA, lda, majorB, ldb, dev->sms, heavy_epilogue);
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return GB_ERR_UNSUPPORTED_ARCH;
