@@ -85,7 +85,9 @@ struct Cfg {
   static constexpr int kAccStride = (kMx || kN224) ? 256 : kTileN;   // TMEM columns between them
   static constexpr int kKB = (kPair && kNSub == 1) ? 2 : 1;       // k-blocks per stage
   // narrow tiles: 24 KiB k-blocks, eight in flight
-  static constexpr int kStages = kNarrow ? 8 : ((kPair && kNSub == 1) ? 3 : 4);
+  // 448-column pair tiles: five 44 KiB stages, the epilogue staging entirely in borrowed stages
+  static constexpr int kStages = kNarrow ? 8 : ((kPair && kNSub == 1) ? 3 : (kW448 ? 5 : 4));
+  static constexpr bool kEpiOwn = !kW448;   // staging tiles of its own beside the stages
   static constexpr int kEpiWarps = kAccBufs == 1 ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;            // producer, MMA, epilogue warps
   static constexpr int kAHalf = kRowsA * kBK * 2;                // one k-block of A (bytes)
@@ -104,7 +106,7 @@ struct Cfg {
   static constexpr int kEpiBufBytes = 32 * 64;
   static constexpr bool kEpiCTma = kAccBufs == 2;
   static constexpr int kEpiBufsPerWarp = kEpiCTma ? 4 : 2;
-  static constexpr int kEpiStageBytesFull = kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes;
+  static constexpr int kEpiStageBytesFull = kEpiOwn ? kEpiWarps * kEpiBufsPerWarp * kEpiBufBytes : 0;
   static constexpr bool kEpiTma =
       1024 + kStages * kStageBytes + kEpiStageBytesFull + kCtlBytes <= 227 * 1024;
   static constexpr int kEpiStageBytes = kEpiTma ? kEpiStageBytesFull : 0;
@@ -114,9 +116,12 @@ struct Cfg {
   // k-blocks are idle (the next tile's copies go into the other two first), so each warp
   // borrows kRingBufs staging tiles in each of them: with its own two, every run of the tile
   // (up to kEpiNB) has a staging tile of its own and C is copied in several runs ahead.
+  // (448 columns: no staging of its own; the warps' tiles are packed across both borrowed
+  // stages, kRingTiles per stage)
   static constexpr int kRingFit = kStageBytes / (kEpiWarps * kEpiBufBytes);
   static constexpr int kRingBufs = (kW512 || kW448) ? (kRingFit < 3 ? kRingFit : 3) : 0;
-  static constexpr int kEpiNB = 2 + 2 * kRingBufs;
+  static constexpr int kRingTiles = kStageBytes / kEpiBufBytes;
+  static constexpr int kEpiNB = kEpiOwn ? 2 + 2 * kRingBufs : (2 * kRingTiles) / kEpiWarps;
   static constexpr int kSlotFloats = kRowsA * kTileN;       // one CTA's stream-K partial
   static_assert(kSmemBytes <= 227 * 1024, "shared-memory budget per CTA");
   static_assert(kStages <= kMaxStages, "control block");
@@ -209,14 +214,15 @@ enum : uint32_t {
 };
 
 // The epilogue borrows ring stages (wide pair forms, with C: its copies then run several runs
-// ahead): every tile is whole (no stream-K) and has at least kStages stage-blocks, so the copy
-// stage reaches the borrowed stages only with the third stage-block of the next tile, and
-// waits there for their return.  (Without C the two staging tiles of a warp suffice; the
-// hold-off of the next tile's copies would cost more than it saves.)
+// ahead; 448-column tiles always, having no staging of their own): every tile is whole (no
+// stream-K) and has at least kStages stage-blocks, so the copy stage reaches the borrowed stages
+// only with stage-block kStages - 2 of the next tile, and waits there for their return.
+// (Without C the two staging tiles of a 512-column tile's warp suffice; the hold-off of the next
+// tile's copies would cost more than it saves.)
 template <class C>
 __device__ __forceinline__ bool ring_epilogue(const Params& p) {
-  return C::kRingBufs > 0 && C::kEpiTma && p.epi_tma != 0 && p.has_c != 0 && p.dp_tiles == p.num_tiles &&
-         p.nsb >= C::kStages;
+  return C::kRingBufs > 0 && C::kEpiTma && p.epi_tma != 0 && (p.has_c != 0 || !C::kEpiOwn) &&
+         p.dp_tiles == p.num_tiles && p.nsb >= C::kStages;
 }
 
 // Record the first failing wait, and stop this CTA (and its peer, in a pair).
@@ -442,8 +448,8 @@ __device__ void run_producer(const Params& p, const void* tmA, const void* tmB, 
     const int32_t b_row0 = nt * C::kTileN + static_cast<int32_t>(prank) * C::kRowsBSub;
     for (int32_t sb = item.sb0; sb < item.sb1; ++sb, ++gkb) {
       // the previous tile's epilogue holds the stages of its last two k-blocks, which this
-      // tile's third and fourth stage-blocks are about to reuse
-      if (ring && it > 0 && sb == item.sb0 + 2 &&
+      // tile's stage-blocks kStages - 2 and kStages - 1 are about to reuse
+      if (ring && it > 0 && sb == item.sb0 + C::kStages - 2 &&
           !wait_one<kPair>(smem_addr(&ctl->epi_ring), static_cast<uint32_t>((it - 1) & 1), ctl, p.timeout_ns,
                            kSiteRing)) {
         ok = false;
@@ -1034,7 +1040,8 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
   // barriers its C copies complete on.  Runs alternate between the two buffers by a count
   // kept across tiles (gr), so a buffer is rewritten only once the copy that last read it
   // (two runs earlier) has finished reading.
-  const bool tma = C::kEpiTma && p.epi_tma != 0;
+  // without staging of its own, the tile-store epilogue needs the borrowed stages
+  const bool tma = C::kEpiTma && p.epi_tma != 0 && (C::kEpiOwn || ring_epilogue<C>(p));
   const uint32_t stg = smem_addr(epi_smem) + static_cast<uint32_t>(ew) * C::kEpiBufsPerWarp * C::kEpiBufBytes;
   // stream-K owner: this lane's column of this warp's share of the stage ring, where the
   // other CTAs' partials of a run are gathered (kPartBatch CTAs x 32 columns x 32 rows fp32)
@@ -1078,6 +1085,12 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     const uint32_t slot_b = ring_base + static_cast<uint32_t>(s_last * C::kStageBytes);
     // staging tile b of this warp: its own two, then kRingBufs in each borrowed stage
     auto ring_buf = [&](uint32_t b) -> uint32_t {
+      if constexpr (!C::kEpiOwn) {
+        // this warp's tiles packed across both stages, kRingTiles in each
+        const uint32_t t = static_cast<uint32_t>(ew * C::kEpiNB) + b;
+        return t < static_cast<uint32_t>(C::kRingTiles) ? slot_a + t * C::kEpiBufBytes
+                                                         : slot_b + (t - C::kRingTiles) * C::kEpiBufBytes;
+      }
       if (b < 2u) return stg + b * C::kEpiBufBytes;
       constexpr uint32_t kPer = C::kRingBufs > 0 ? C::kRingBufs : 1;
       const uint32_t i = b - 2u;
@@ -1125,7 +1138,7 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
         }
         c_pending |= 1u << (gr & 1u);
       }
-      if (C::kRingBufs > 0 && ring && p.has_c) {
+      if (C::kRingBufs > 0 && C::kEpiOwn && ring && p.has_c) {
         // the first two runs' C into this warp's own staging tiles (free: the previous tile's
         // stores have read them), while the main loop still runs
         if (lane == 0)
@@ -1144,13 +1157,14 @@ __device__ void run_epilogue(const Params& p, Ctl* ctl, uint32_t tmem_base, int 
     if (C::kRingBufs > 0 && ring && p.has_c) {
       // every MMA of this tile has completed, so the borrowed stages are free: the C of the
       // runs up to NB - 1 into them
+      constexpr int kFirst = C::kEpiOwn ? 2 : 0;
       if (lane == 0)
-        for (int a = 2; a < C::kEpiNB && a < nruns; ++a) {
+        for (int a = kFirst; a < C::kEpiNB && a < nruns; ++a) {
           const uint32_t bar = smem_addr(&ctl->c_full[ew][a]);
           mbar_arrive_expect_tx(bar, C::kEpiBufBytes);
           tma_load_2d(ring_buf(static_cast<uint32_t>(a)), tmC, bar, x0 + 32 * a, y0);
         }
-      for (int a = 2; a < C::kEpiNB && a < nruns; ++a) c_pending |= 1u << a;
+      for (int a = kFirst; a < C::kEpiNB && a < nruns; ++a) c_pending |= 1u << a;
     }
     uint32_t c_lo = 1, c_hi = 0;
     if (owner_with_parts) {
