@@ -506,7 +506,7 @@ def run_gb300(args):
     # end to end through the public API with pinned host buffers
     A_h, B_h = data["A"].pin_memory(), data["B"].pin_memory()
     C_h = data["C"].pin_memory() if data["C"] is not None else None
-    D_h = torch.empty(p.M * p.N, dtype=out_dt, pin_memory=True)
+    D_h = torch.empty(p.M * p.N, dtype=D.dtype, pin_memory=True)
 
     if mx:
         SFA_h, SFB_h = data["SFA"].pin_memory(), data["SFB"].pin_memory()
@@ -521,6 +521,15 @@ def run_gb300(args):
             Dd = G.gemm_mxfp8(Ad, Bd, p.M, p.N, p.K, lda=lda, ldb=ldb, sfa=pa, sfb=pb, a_format=p.a_fmt,
                               b_format=p.b_fmt, out_dtype=out_dt, alpha=p.alpha, beta=p.beta, C=Cd,
                               workspace=ws)
+            D_h.copy_(Dd, non_blocking=True)
+        elif epi is not None:
+            # the fused epilogue has no host-operand form: host copies, gb_gemm_ex, D back
+            Ad, Bd = A_h.to(dev, non_blocking=True), B_h.to(dev, non_blocking=True)
+            Cd = C_h.to(dev, non_blocking=True) if C_h is not None else None
+            Dd = G.gemm_fused(Ad, Bd, p.M, p.N, p.K, lda=lda, ldb=ldb, majorA=p.majorA, majorB=p.majorB,
+                              alpha=p.alpha, beta=p.beta, C=Cd, bias=bias, activation="gelu",
+                              amax=amax if fp8 else None, out_format="e4m3" if fp8 else "input",
+                              out_scale=16.0 if fp8 else 1.0)
             D_h.copy_(Dd, non_blocking=True)
         elif f8:
             # gb_gemm_fp8_host: host buffers in, D out (staging and overlap in the library)
@@ -549,7 +558,7 @@ def run_gb300(args):
     e2e_s, e2e_flops = aggregate(e0.elapsed_time(e1) / 1e3, float(p.flops) * e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size()
               for t in (data["A"], data["B"], data["C"], data.get("SFA"), data.get("SFB")) if t is not None)
-    d2h = p.M * p.N * 2
+    d2h = D_h.numel() * D_h.element_size()
     st, detail = G.last_device_status()
     if st != 0:
         raise RuntimeError("device status %d (%#x) in the end-to-end region" % (st, detail))
@@ -611,7 +620,9 @@ def run_gb300(args):
         "e2e": {"value": e2e_flops / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "entry_point": ("host copies + gb_gemm_mxfp8 (no host form)" if mx else
-                                "gb_gemm_fp8_host" if f8 else "gb_gemm_%s_host" % p.dtype)},
+                                "gb_gemm_fp8_host" if f8 else
+                                "host copies + gb_gemm_ex (no host form)" if epi is not None else
+                                "gb_gemm_%s_host" % p.dtype)},
         "roofline": roofline, "clocks": clocks, "gpu_launches": args.steps,
     }
     # how the timed launches were made (kept out of "config", which names the workload only
