@@ -101,8 +101,9 @@ struct Cfg {
   static constexpr int kStageBytes = ((kSfOff + kSfBytes * kKB) + 1023) / 1024 * 1024;
   // Tile-store epilogue: per epilogue warp two 32 x 32 staging tiles of D (16-bit, 64-byte
   // rows) written back by tensor copies and, with two accumulators, two of C read in the same
-  // way (kEpiCTma); with one accumulator (eight epilogue warps) C is loaded into registers
-  // instead, which halves the staging.  Used when it fits.
+  // way (kEpiCTma); with one accumulator (eight epilogue warps) C is copied into the D staging
+  // tiles themselves (or into borrowed stages, below), which halves the staging.  Used when it
+  // fits.
   static constexpr int kEpiBufBytes = 32 * 64;
   static constexpr bool kEpiCTma = kAccBufs == 2;
   static constexpr int kEpiBufsPerWarp = kEpiCTma ? 4 : 2;
