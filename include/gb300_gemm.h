@@ -91,9 +91,9 @@ gb_status gb_gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
    schedules": split-K and stream-K divide K across CTAs when output tiles are too few to
    fill the GPU, at the cost of a reduction and a workspace).  Each CTA first runs whole
    tiles, then an even contiguous share of the remaining (tile, stage-block) units (a
-   stage-block is the k-blocks one pipeline stage holds: two for CTA pairs, one for single
-   CTAs); the CTA that holds a tile's first unit adds the other CTAs' fp32 partials, in CTA
-   order, before the epilogue.
+   stage-block is the k-blocks one pipeline stage holds: two for the 224- and 256-column CTA
+   pairs, one for single CTAs and the 448- and 512-column pairs); the CTA that holds a tile's
+   first unit adds the other CTAs' fp32 partials, in CTA order, before the epilogue.
    workspace: device memory of at least gb_gemm_workspace_bytes() bytes, 256-byte aligned,
    zero-filled before its first use and not shared by calls that may run at the same time
    (it is reused as is by later calls; each launch tags its hand-offs with a new number).
